@@ -1,0 +1,421 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each check takes the oracle module as an argument. The mutation tests at the bottom
+plant plausible mistakes in a copy of the oracle and show that some pin then fails.
+"""
+import copy
+import itertools
+import json
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+
+import moe_synth
+from oracle import moe_oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+_LOGIT = {"ln3": math.log(3.0), "0": 0.0, "-ln3": -math.log(3.0), "ln9": math.log(9.0),
+          "-ln9": -math.log(9.0)}
+
+
+# ---------------------------------------------------------------------------- checks ----
+
+def check_route_closed_form(o):
+    g = _load("route_closed_form.json")
+    bias = np.array(g["bias"])
+    for c in g["cases"]:
+        z = np.array([[_LOGIT[v] for v in c["logits"]]])
+        r = o.route_from_logits(z, bias, c["k"])
+        np.testing.assert_allclose(r["scores"][0], c["scores"], rtol=0, atol=1e-14)
+        assert r["idx"][0].tolist() == c["idx"], (r["idx"][0], c)
+        np.testing.assert_allclose(r["gates"][0], c["gates"], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(r["gap"][0], c["gap"], rtol=0, atol=1e-14)
+
+
+def _brute_topk(u_row, k):
+    """Best k-subset by sum of u; among equal sums the lexicographically smallest index
+    set wins. Ordered by descending u, lower index first on equal u."""
+    E = len(u_row)
+    best, best_set = None, None
+    for comb in itertools.combinations(range(E), k):
+        s = math.fsum(u_row[list(comb)])
+        if best is None or s > best + 0.0:
+            best, best_set = s, comb
+    return sorted(best_set, key=lambda e: (-u_row[e], e))
+
+
+def check_topk_brute_force(o):
+    rng = np.random.default_rng(11)
+    for E, k in [(5, 1), (5, 2), (6, 3), (8, 4), (8, 8), (7, 6)]:
+        s = rng.uniform(0.01, 0.99, size=(40, E))
+        b = rng.uniform(-0.1, 0.1, size=E)
+        idx, gap = o.select_topk(s, b, k)
+        u = s + b
+        for t in range(40):
+            assert idx[t].tolist() == _brute_topk(u[t], k), (E, k, t)
+            rest = sorted(set(range(E)) - set(idx[t].tolist()))
+            if rest:
+                assert gap[t] == pytest.approx(u[t, idx[t, -1]] - max(u[t, rest]), abs=1e-15)
+
+
+def _brute_moe(x, wr, b, wu, wd, k):
+    """Whole layer by scalar loops on tiny sizes (no matrix library calls)."""
+    T, H = x.shape
+    E, F = wu.shape[0], wu.shape[1]
+    y = np.zeros((T, H))
+    for t in range(T):
+        s = []
+        for e in range(E):
+            z = math.fsum(x[t, i] * wr[e, i] for i in range(H))
+            s.append(1.0 / (1.0 + math.exp(-z)))
+        s = np.array(s)
+        chosen = _brute_topk(s + b, k)
+        tot = math.fsum(s[e] for e in chosen)
+        for e in chosen:
+            hid = []
+            for f in range(F):
+                a = math.fsum(x[t, i] * wu[e, f, i] for i in range(H))
+                hid.append(max(a, 0.0) ** 2)
+            for i in range(H):
+                y[t, i] += (s[e] / tot) * math.fsum(wd[e, i, f] * hid[f] for f in range(F))
+    return y
+
+
+def _tiny_layer(seed, T=5, H=4, E=6, k=2, F=3):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, H))
+    wr = rng.standard_normal((E, H)) / 2
+    b = rng.uniform(-0.1, 0.1, E)
+    wu = rng.standard_normal((E, F, H))
+    wd = rng.standard_normal((E, H, F))
+    return x, wr, b, wu, wd, k
+
+
+def check_layer_brute_force(o):
+    for seed in range(4):
+        x, wr, b, wu, wd, k = _tiny_layer(seed)
+        got = o.moe_layer(x, wr, b, wu, wd, k)["y"]
+        np.testing.assert_allclose(got, _brute_moe(x, wr, b, wu, wd, k), rtol=1e-11, atol=1e-11)
+
+
+def check_ffn_closed_form(o):
+    g = _load("ffn_closed_form.json")
+    out = o.expert_ffn(np.array([g["x"]]), np.array(g["w_up"]), np.array(g["w_down"]))
+    np.testing.assert_array_equal(out[0], g["o"])
+
+
+def check_single_expert_is_dense_ffn(o):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((7, 5))
+    wr = rng.standard_normal((1, 5))
+    wu = rng.standard_normal((1, 4, 5))
+    wd = rng.standard_normal((1, 5, 4))
+    got = o.moe_layer(x, wr, np.zeros(1), wu, wd, 1)["y"]
+    ref = np.zeros((7, 5))
+    for t in range(7):
+        hid = [max(math.fsum(x[t, i] * wu[0, f, i] for i in range(5)), 0.0) ** 2 for f in range(4)]
+        ref[t] = [math.fsum(wd[0, i, f] * hid[f] for f in range(4)) for i in range(5)]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def check_identical_experts(o):
+    """With every expert equal, any renormalised routing gives the dense FFN."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((9, 6))
+    wr = rng.standard_normal((5, 6))
+    wu1, wd1 = rng.standard_normal((4, 6)), rng.standard_normal((6, 4))
+    wu = np.stack([wu1] * 5)
+    wd = np.stack([wd1] * 5)
+    got = o.moe_layer(x, wr, rng.uniform(-0.1, 0.1, 5), wu, wd, 3)["y"]
+    np.testing.assert_allclose(got, o.expert_ffn(x, wu1, wd1), rtol=1e-12, atol=1e-12)
+    # and that dense FFN is the closed-form one
+    ref = np.maximum(x @ wu1.T, 0) ** 2 @ wd1.T
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def check_k_equals_E(o):
+    rng = np.random.default_rng(6)
+    x, wr, b, wu, wd, _ = _tiny_layer(6, T=4, H=3, E=4, F=2)
+    r = o.moe_layer(x, wr, b, wu, wd, 4)
+    assert all(sorted(row) == [0, 1, 2, 3] for row in r["idx"].tolist())
+    np.testing.assert_allclose(r["y"], _brute_moe(x, wr, b, wu, wd, 4), rtol=1e-11, atol=1e-11)
+    del rng
+
+
+def check_forced_expert(o):
+    rng = np.random.default_rng(8)
+    s = rng.uniform(0, 1, (50, 10))
+    b = np.zeros(10)
+    b[7] = 10.0
+    idx, _ = o.select_topk(s, b, 3)
+    assert (idx[:, 0] == 7).all()
+
+
+def check_gate_and_count_invariants(o):
+    w = moe_synth.WORKLOADS["tiny"]
+    inp = moe_synth.layer_inputs(w, with_experts=False)
+    r = o.route(inp["x"], inp["w_router"], inp["bias"], w.k)
+    np.testing.assert_allclose(r["gates"].sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert (r["gates"] > 0).all()
+    p = o.permute(r["idx"], w.E)
+    assert int(p["counts"].sum()) == w.T * w.k == int(p["offsets"][-1])
+    assert p["offsets"][0] == 0 and (np.diff(p["offsets"]) == p["counts"]).all()
+    # permute o unpermute is the identity
+    xp = o.gather_rows(inp["x"], p["row_token"])
+    for t in range(w.T):
+        for j in range(w.k):
+            assert (xp[p["slot_row"][t * w.k + j]] == inp["x"][t]).all()
+    # each token at most once per segment, in ascending order
+    for e in range(w.E):
+        seg = p["row_token"][p["offsets"][e]:p["offsets"][e + 1]]
+        assert (np.diff(seg) > 0).all()
+        for t in seg:
+            assert e in r["idx"][t]
+    assert sorted(p["slot_row"].tolist()) == list(range(w.T * w.k))
+
+
+def check_latent_identity(o):
+    """l = H with W_in = W_out = I reduces LatentMoE to the standard layer."""
+    x, wr, b, wu, wd, k = _tiny_layer(9, T=6, H=4, E=5, F=3)
+    eye = np.eye(4)
+    lat = o.latent_moe(x, eye, eye, wr, b, wu, wd, k, router_on_latent=True)
+    std = o.moe_layer(x, wr, b, wu, wd, k)
+    np.testing.assert_allclose(lat["y"], std["y"], rtol=1e-13, atol=1e-13)
+    lat_h = o.latent_moe(x, eye, eye, wr, b, wu, wd, k, router_on_latent=False)
+    np.testing.assert_allclose(lat_h["y"], std["y"], rtol=1e-13, atol=1e-13)
+
+
+def check_latent_brute_force(o):
+    """A non-trivial projection: brute-force layer on x W_in^T, then W_out."""
+    rng = np.random.default_rng(12)
+    T, H, L, E, k, F = 4, 6, 3, 5, 2, 2
+    x = rng.standard_normal((T, H))
+    w_in = rng.standard_normal((L, H))
+    w_out = rng.standard_normal((H, L))
+    wr = rng.standard_normal((E, L))
+    b = rng.uniform(-0.1, 0.1, E)
+    wu = rng.standard_normal((E, F, L))
+    wd = rng.standard_normal((E, L, F))
+    got = o.latent_moe(x, w_in, w_out, wr, b, wu, wd, k)["y"]
+    xl = np.array([[math.fsum(x[t, i] * w_in[l, i] for i in range(H)) for l in range(L)]
+                   for t in range(T)])
+    yl = _brute_moe(xl, wr, b, wu, wd, k)
+    ref = np.array([[math.fsum(yl[t, l] * w_out[h, l] for l in range(L)) for h in range(H)]
+                    for t in range(T)])
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-10)
+
+
+def check_combine_weights(o):
+    yp = np.arange(12.0).reshape(6, 2)
+    slot_row = np.array([5, 0, 2, 3, 1, 4])
+    gates = np.array([0.25, 0.75, 0.5, 0.5, 1.0, 0.0])
+    y = o.combine(yp, slot_row, gates, 3, 2)
+    # token 0: 0.25*yp[5] + 0.75*yp[0]; token 1: 0.5*yp[2] + 0.5*yp[3]; token 2: yp[1]
+    np.testing.assert_array_equal(y, [[2.5, 3.5], [5.0, 6.0], [2.0, 3.0]])
+
+
+def check_e2m1_table(o):
+    """Exhaustive E2M1: decode all 16 codes from the bit fields, then check nearest/even."""
+    table = []
+    for code in range(16):
+        s, ex, m = code >> 3, (code >> 1) & 3, code & 1
+        mag = (m * 0.5) if ex == 0 else (1 + m * 0.5) * 2.0 ** (ex - 1)
+        table.append((-1.0 if s else 1.0) * mag)
+    pos = sorted(set(abs(v) for v in table))
+    assert pos == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    probes = np.concatenate([np.array(pos), (np.array(pos[1:]) + np.array(pos[:-1])) / 2,
+                             np.random.default_rng(1).uniform(0, 8, 500)])
+    for v in probes:
+        got = float(o.e2m1_round(v))
+        d = [abs(v - p) for p in pos]
+        best = min(d)
+        cands = [i for i, di in enumerate(d) if di == best]
+        want = pos[cands[0]] if len(cands) == 1 else pos[[c for c in cands if c % 2 == 0][0]]
+        if v > 6:
+            want = 6.0
+        assert got == want, (v, got, want)
+        assert float(o.e2m1_round(-v)) == -want
+
+
+def check_e4m3_table(o):
+    """Exhaustive E4M3: decode the 254 finite codes from the bit fields (S.1111.111 is
+    NaN), then check that rounding picks the nearest value, ties to the even code."""
+    vals = {}
+    for code in range(128):
+        ex, m = (code >> 3) & 15, code & 7
+        if ex == 15 and m == 7:
+            continue
+        v = m * 2.0 ** -9 if ex == 0 else (1 + m / 8) * 2.0 ** (ex - 7)
+        vals[code] = v
+    assert max(vals.values()) == 448.0 and min(v for v in vals.values() if v) == 2.0 ** -9
+    codes = sorted(vals, key=lambda c: vals[c])
+    mags = [vals[c] for c in codes]
+    probes = list(mags) + [(a + b) / 2 for a, b in zip(mags, mags[1:])]
+    probes += list(np.random.default_rng(2).uniform(0, 460, 400))
+    probes += list(np.exp(np.random.default_rng(3).uniform(-8, 6, 400)))
+    for v in probes:
+        got = float(o.e4m3_round(v))
+        if v >= 448:
+            assert got == 448.0
+            continue
+        d = [abs(v - p) for p in mags]
+        best = min(d)
+        cands = [i for i, di in enumerate(d) if di == best]
+        if len(cands) == 1:
+            want = mags[cands[0]]
+        else:
+            want = [mags[i] for i in cands if codes[i] % 2 == 0][0]
+        assert got == want, (v, got, want)
+
+
+def check_nvfp4_block(o):
+    g = _load("nvfp4_block.json")
+    q = o.nvfp4_quantize(np.array([g["values"]], dtype=np.float32), np.float32(g["g"]))
+    assert q["sb"].tolist() == [[g["block_scale"]]]
+    np.testing.assert_array_equal(q["q"][0], g["codes_value"])
+    np.testing.assert_array_equal(q["deq"][0], g["codes_value"])
+
+
+def check_nvfp4_bounds(o):
+    rng = np.random.default_rng(4)
+    a = (rng.standard_normal((64, 128)) * np.exp(rng.uniform(-4, 4, (64, 1)))).astype(np.float32)
+    a[3, 16:32] = 0.0                                     # an all-zero block
+    q = o.nvfp4_quantize(a)
+    g = float(q["g"])
+    assert g == pytest.approx(float(np.abs(a).max()) / 2688.0, rel=1e-6)
+    assert q["sb"].max() <= 448.0
+    assert (q["q"][3, 16:32] == 0).all() and q["sb"][3, 1] == 0
+    assert np.isin(np.abs(q["q"]), [0, 0.5, 1, 1.5, 2, 3, 4, 6]).all()
+    blocks = a.reshape(64, 8, 16).astype(np.float64)
+    deq = q["deq"].reshape(64, 8, 16)
+    step = np.where(np.abs(blocks) < 2 * q["sb"][:, :, None] * g, 0.5, 2.0)   # coarsest spacing
+    scale = (q["sb"] * g)[:, :, None]
+    inside = np.abs(blocks) <= 6 * scale
+    err = np.abs(deq - blocks)
+    assert (err[inside] <= (0.5 * step * scale)[inside] * (1 + 1e-6) + 1e-30).all()
+    # values on the scaled grid survive exactly
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -6, -4, -3, -2, -1.5, -1, -0.5, 0], np.float32)
+    blk = (grid * np.float32(2.0 ** -3)).reshape(1, 16)
+    q2 = o.nvfp4_quantize(blk, np.float32(2.0 ** -3))
+    np.testing.assert_array_equal(q2["deq"], blk.astype(np.float64))
+
+
+ALL_CHECKS = [check_route_closed_form, check_topk_brute_force, check_layer_brute_force,
+              check_ffn_closed_form, check_single_expert_is_dense_ffn, check_identical_experts,
+              check_k_equals_E, check_forced_expert, check_gate_and_count_invariants,
+              check_latent_identity, check_latent_brute_force, check_combine_weights,
+              check_e2m1_table, check_e4m3_table, check_nvfp4_block, check_nvfp4_bounds]
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(check):
+    check(moe_oracle)
+
+
+def test_latent_expert_scaling_formula():
+    # E' = E*H/l and k' = k*H/l (Nemotron 3 notes §2.2): 128 experts, top-6, H/l = 4
+    assert moe_synth.latent_scaled(128, 6, 4096, 1024) == (512, 24)
+    w = moe_synth.WORKLOADS["latent"]
+    assert (w.E, w.k, w.latent, w.H) == (512, 24, 1024, 4096)
+
+
+# ------------------------------------------------------------------ planted mistakes ----
+
+def _mutant(**overrides):
+    m = types.ModuleType("mutant")
+    m.__dict__.update({k: v for k, v in vars(moe_oracle).items() if not k.startswith("__")})
+    for name, fn in overrides.items():
+        m.__dict__[name] = fn
+    # re-bind functions so internal calls see the mutated globals
+    for k, v in list(m.__dict__.items()):
+        if isinstance(v, types.FunctionType):
+            m.__dict__[k] = types.FunctionType(v.__code__, m.__dict__, v.__name__,
+                                               v.__defaults__, v.__closure__)
+    for name, fn in overrides.items():
+        m.__dict__[name] = types.FunctionType(fn.__code__, m.__dict__, fn.__name__,
+                                              fn.__defaults__, fn.__closure__)
+    return m
+
+
+def _gates_biased(scores, idx):          # mistake: bias leaks into the gates
+    sel = np.take_along_axis(np.asarray(scores) + 0.1, idx.astype(np.int64), axis=1)
+    return sel / sel.sum(axis=1, keepdims=True)
+
+
+def _ffn_plain_relu(rows, w_up_e, w_down_e):  # mistake: ReLU instead of squared ReLU
+    return np.maximum(_f64(rows) @ _f64(w_up_e).T, 0.0) @ _f64(w_down_e).T
+
+
+def _grouped_wrong_expert(x_perm, offsets, w_up, w_down):  # mistake: off-by-one expert
+    xp = _f64(x_perm)
+    E = len(offsets) - 1
+    out = np.zeros((xp.shape[0], np.asarray(w_down).shape[1]))
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            out[a:b] = expert_ffn(xp[a:b], w_up[e], w_down[(e + 1) % E])
+    return out
+
+
+def _select_high_index_wins(scores, bias, k):  # mistake: higher index wins exact ties
+    s = np.asarray(scores, dtype=np.float64)
+    u = s + np.asarray(bias)[None, :]
+    T, E = s.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    gap = np.full(T, np.inf)
+    for t in range(T):
+        order = np.lexsort((-np.arange(E), -u[t]))
+        idx[t] = order[:k]
+        if k < E:
+            gap[t] = u[t, order[k - 1]] - u[t, order[k]]
+    return idx, gap
+
+
+def _combine_no_gates(y_perm, slot_row, gates, T, k):   # mistake: unweighted mean
+    yp = _f64(y_perm)
+    sr = np.asarray(slot_row, dtype=np.int64).reshape(T, k)
+    return sum(yp[sr[:, j]] for j in range(k)) / k
+
+
+def _sigmoid_sign(z):                     # mistake: sign error in the sigmoid
+    return 1.0 / (1.0 + np.exp(np.asarray(z, dtype=np.float64)))
+
+
+def _e2m1_ties_away(v):                   # mistake: ties rounded away from zero
+    v = np.asarray(v, dtype=np.float64)
+    m = np.abs(v)
+    q = np.where(m < 2.0, 0.5, np.where(m < 4.0, 1.0, 2.0))
+    return np.copysign(np.minimum(np.floor(m / q + 0.5) * q, 6.0), v)
+
+
+_f64 = moe_oracle._f64
+
+MUTANTS = {
+    "gates_use_bias": ({"gates_from_scores": _gates_biased}, check_route_closed_form),
+    "plain_relu": ({"expert_ffn": _ffn_plain_relu}, check_ffn_closed_form),
+    "plain_relu_layer": ({"expert_ffn": _ffn_plain_relu}, check_layer_brute_force),
+    "wrong_expert_index": ({"grouped_ffn": _grouped_wrong_expert}, check_layer_brute_force),
+    "tie_high_index": ({"select_topk": _select_high_index_wins}, check_route_closed_form),
+    "combine_unweighted": ({"combine": _combine_no_gates}, check_combine_weights),
+    "combine_unweighted_layer": ({"combine": _combine_no_gates}, check_layer_brute_force),
+    "sigmoid_sign": ({"sigmoid": _sigmoid_sign}, check_route_closed_form),
+    "e2m1_ties_away": ({"e2m1_round": _e2m1_ties_away}, check_e2m1_table),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name):
+    overrides, check = MUTANTS[name]
+    m = _mutant(**copy.copy(overrides))
+    with pytest.raises(AssertionError):
+        check(m)
