@@ -1,0 +1,518 @@
+"""Benchmark of the routed MoE layer forward pass on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload nano_decode|nano_prefill|latent|tiny]
+
+One step = one whole layer forward (route, permute, grouped expert FFN, combine; the
+LatentMoE workload adds its two projections) over one batch of seeded synthetic tokens,
+through the library's C ABI. Prints one JSON line.
+
+The default workload is the Nano-shaped decode layer: 64 tokens, H=2688, 128 experts,
+top-6, F=1856. Inputs and weights are resident in HBM before the timed region starts. L2 is
+flushed (a 512 MiB write) before every timed step. Each step is timed with CUDA events on
+the launching stream; the grouped expert FFN, the dominant kernel, is timed the same way.
+
+--impl reference times the fp64 CPU oracle on the host's cores, on a bounded sample of the
+same workload, and prints the same line with "impl": "reference".
+
+Under torchrun (N > 1) each rank runs an independent replica of the layer on its own GPU.
+The layer shards by tokens with no exchange. There is no data-path collective: ranks only
+meet at the timing barriers and the max-over-ranks of the elapsed time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and % of roofline (128 experts top-6, bf16) on 1 B300"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ------------------------------------------------------------------- algorithmic counts ----
+
+def counts_from_routing(idx: np.ndarray, E: int) -> np.ndarray:
+    return np.bincount(idx.reshape(-1), minlength=E)
+
+
+def layer_algorithmic(w: moe_synth.Workload, counts: np.ndarray) -> dict:
+    """FLOPs and bytes the method must do/move (weights touched + layer input/output)."""
+    D, rows = w.D, w.rows
+    touched = int((counts > 0).sum())
+    f_router = 2.0 * w.T * (w.latent if (w.latent and w.router_on_latent) else w.H) * w.E
+    f_experts = 4.0 * rows * D * w.F
+    f_proj = 4.0 * w.T * w.H * w.latent if w.latent else 0.0
+    b_weights = touched * 2.0 * D * w.F * 2
+    b_router = w.E * (D if (w.latent and w.router_on_latent) else w.H) * 2.0
+    b_proj = 2.0 * w.H * w.latent * 2 if w.latent else 0.0
+    b_io = 2.0 * w.T * w.H * 2
+    # per grouped-GEMM launch (up and down alike): one expert matrix per touched expert,
+    # plus the permuted activations read and written
+    ffn_bytes_per_launch = touched * D * w.F * 2.0 + rows * (D + w.F) * 2.0
+    return {"flops": f_router + f_experts + f_proj, "bytes": b_weights + b_router + b_proj + b_io,
+            "touched": touched, "ffn_flops_per_launch": 2.0 * rows * D * w.F,
+            "ffn_bytes_per_launch": ffn_bytes_per_launch}
+
+
+# ------------------------------------------------------------------------ clock sampler ----
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines: list[tuple[float, str]] = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        for ts, line in self.lines:
+            if self.t0 is not None and not (self.t0 - 0.05 <= ts <= (self.t1 or ts) + 0.05):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------ ours (GPU) ----
+
+def run_ours(args, w: moe_synth.Workload):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_mixture_experts_57_b300 as moe
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = moe.lib()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    inp = moe_synth.layer_inputs(w)
+    d = {k: moe_synth.to_torch(v, dev) for k, v in inp.items()}
+    T, H, E, k, F, D = w.T, w.H, w.E, w.k, w.F, w.D
+    rows = T * k
+    P = lambda t: t.data_ptr()  # noqa: E731
+
+    # device buffers
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+    tie = torch.empty((T,), dtype=torch.uint8, device=dev)
+    counts = torch.empty((E,), dtype=torch.int32, device=dev)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    row_token = torch.empty((rows,), dtype=torch.int32, device=dev)
+    slot_row = torch.empty((rows,), dtype=torch.int32, device=dev)
+    x_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev)
+    y_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev)
+    ws_route = torch.empty(L.moe_route_workspace_size(T, D, E, k), dtype=torch.uint8, device=dev)
+    ws_perm = torch.empty(L.moe_permute_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
+    ws_ffn = torch.empty(L.moe_grouped_ffn_workspace_size(rows, D, F, E), dtype=torch.uint8,
+                         device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if w.latent:
+        ws_lat = torch.empty(L.latent_moe_workspace_size(T, H, w.latent, E, k, F,
+                                                         int(w.router_on_latent)),
+                             dtype=torch.uint8, device=dev)
+    else:
+        ws_fwd = torch.empty(L.moe_forward_workspace_size(T, H, E, k, F), dtype=torch.uint8,
+                             device=dev)
+
+    def chk(code, what):
+        if code != 0:
+            raise moe.MoeError(code, what)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    # one step; for the standard layer the four calls are issued one by one so the grouped
+    # FFN can be bracketed by events on the launching stream
+    def step(e_ffn0=None, e_ffn1=None):
+        if w.latent:
+            if e_ffn0 is not None:
+                e_ffn0.record(stream)
+            chk(L.latent_moe(P(d["x"]), P(d["w_in"]), P(d["w_out"]), P(d["w_router"]),
+                             P(d["bias"]), int(w.router_on_latent), P(d["w_up"]), P(d["w_down"]),
+                             T, H, w.latent, E, k, F, P(y), P(idx), P(gates), P(ws_lat),
+                             ws_lat.numel(), sp), "latent_moe")
+            if e_ffn1 is not None:
+                e_ffn1.record(stream)
+            return
+        chk(L.moe_route(P(d["x"]), P(d["w_router"]), P(d["bias"]), T, H, E, k, P(idx), P(gates),
+                        P(tie), P(ws_route), ws_route.numel(), sp), "moe_route")
+        chk(L.moe_permute(P(idx), P(d["x"]), T, H, E, k, P(counts), P(offsets), P(row_token),
+                          P(slot_row), P(x_perm), P(ws_perm), ws_perm.numel(), sp), "moe_permute")
+        if e_ffn0 is not None:
+            e_ffn0.record(stream)
+        chk(L.moe_grouped_ffn(P(x_perm), P(offsets), P(d["w_up"]), P(d["w_down"]), rows, H, F, E,
+                              P(y_perm), P(ws_ffn), ws_ffn.numel(), sp), "moe_grouped_ffn")
+        if e_ffn1 is not None:
+            e_ffn1.record(stream)
+        chk(L.moe_combine(P(y_perm), rows, P(slot_row), P(gates), T, H, k, P(y), sp),
+            "moe_combine")
+
+    launches_per_step = (11 if w.latent else 9)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+
+    K = args.steps
+    s_ev = [ev() for _ in range(K)]
+    e_ev = [ev() for _ in range(K)]
+    f0 = [ev() for _ in range(K)]
+    f1 = [ev() for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        s_ev[i].record(stream)
+        step(f0[i], f1[i])
+        e_ev[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks.mark("t1")
+    time.sleep(0.25)
+    clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(s_ev, e_ev)]
+    ffn_ms = [a.elapsed_time(b) for a, b in zip(f0, f1)]
+    ms = statistics.mean(step_ms)
+    ffn = statistics.mean(ffn_ms)
+    if world > 1:
+        t = torch.tensor([ms, ffn], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ffn = float(t[0]), float(t[1])
+    assert moe.get_device_status() == 0
+
+    # ---- end to end through the C ABI: pinned host x in, host y out, every step
+    x_host = d["x"].cpu().pin_memory()
+    y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(d["x"])
+    e2e_ms = []
+    for i in range(args.warmup + K):
+        flush.zero_()
+        a, b = ev(), ev()
+        a.record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        if w.latent:
+            chk(L.latent_moe(P(x_dev), P(d["w_in"]), P(d["w_out"]), P(d["w_router"]),
+                             P(d["bias"]), int(w.router_on_latent), P(d["w_up"]), P(d["w_down"]),
+                             T, H, w.latent, E, k, F, P(y), None, None, P(ws_lat),
+                             ws_lat.numel(), sp), "latent_moe")
+        else:
+            chk(L.moe_forward(P(x_dev), P(d["w_router"]), P(d["bias"]), P(d["w_up"]),
+                              P(d["w_down"]), T, H, E, k, F, P(y), None, None, P(ws_fwd),
+                              ws_fwd.numel(), sp), "moe_forward")
+        y_host.copy_(y, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = float(t[0])
+    assert moe.get_device_status() == 0
+
+    routing = idx.cpu().numpy()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    peaks, peak_src = load_peaks()
+    alg = layer_algorithmic(w, counts_from_routing(routing, E))
+    launches = 1 if w.latent else 2   # grouped GEMM launches inside the FFN bracket
+    if w.latent:
+        bound = "tensor"
+        dom_units = alg["flops"]
+        achieved = dom_units / (ffn / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    elif alg["ffn_flops_per_launch"] / peaks["bf16_tflops"] / 1e12 > \
+            alg["ffn_bytes_per_launch"] / peaks["hbm_gbs"] / 1e9:
+        bound = "tensor"
+        achieved = alg["ffn_flops_per_launch"] * launches / (ffn / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        bound = "hbm"
+        achieved = alg["ffn_bytes_per_launch"] * launches / (ffn / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    roof_ms = max(alg["flops"] / (peaks["bf16_tflops"] * 1e12),
+                  alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    traffic = read_traffic(w.name)
+    out = {
+        "metric": METRIC,
+        "value": world * T / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded, random-init weights of the named shape)",
+        "config": {"workload": w.name, "T": T, "H": H, "E": E, "k": k, "F": F,
+                   "latent": w.latent or None, "bias": w.bias, "l2": "flushed before every step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": ("whole latent layer (tcgen05 GEMMs dominate)" if w.latent
+                                else "grouped expert GEMM (tcgen05), up + down launches"),
+                     "peak_source": peak_src,
+                     "ffn_ms": ffn, "launches_timed": launches},
+        "layer_roofline": {"time_ms": roof_ms, "frac": roof_ms / ms,
+                           "tflops": alg["flops"] / (ms / 1e3) / 1e12,
+                           "hbm_gbs": alg["bytes"] / (ms / 1e3) / 1e9,
+                           "touched_experts": alg["touched"], "peak_source": peak_src},
+        "e2e": {"value": world * T / (e2e / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
+                "ms_per_step": e2e},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks.summary(),
+        "wall_s": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, inp, routing, budget_s=args.cpu_budget)
+    if world > 1:
+        dist.destroy_process_group()
+    return out
+
+
+def read_traffic(workload: str):
+    """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it still
+    describes the current kernel source (else null)."""
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}.md")
+    try:
+        with open(path) as f:
+            txt = f.read()
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        if line.startswith("traffic_bytes_per_launch:"):
+            vals["t"] = float(line.split(":", 1)[1])
+        if line.startswith("kernel_source_sha256:"):
+            vals["h"] = line.split(":", 1)[1].strip()
+    if "t" not in vals or vals.get("h") != kernel_source_hash():
+        return None
+    return vals["t"]
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    p = os.path.join(ROOT, "sparse_mixture_experts_57_b300", "csrc")
+    h = hashlib.sha256()
+    for name in ("grouped_gemm.cu", "tc.cuh"):
+        with open(os.path.join(p, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------------- oracle (CPU) legs ----
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return 1
+
+
+def _oracle_sample(w, inp, toks):
+    """The oracle's layer on a subset of tokens: route them, run their experts, combine."""
+    from oracle import moe_oracle as O
+    x = inp["x"][toks]
+    if w.latent:
+        x_lat = O.latent_project_in(x, inp["w_in"])
+        r = O.route(x_lat if w.router_on_latent else x, inp["w_router"], inp["bias"], w.k)
+        y_lat = O.moe_tokens(x_lat, r["idx"], r["gates"], inp["w_up"], inp["w_down"])
+        return y_lat @ O.widen_bf16(inp["w_out"]).T
+    r = O.route(x, inp["w_router"], inp["bias"], w.k)
+    return O.moe_tokens(x, r["idx"], r["gates"], inp["w_up"], inp["w_down"])
+
+
+def cpu_baseline(w, inp, routing=None, budget_s=20.0) -> dict:
+    """Time the oracle as it stands on a bounded sample of the workload (host cores)."""
+    rng = np.random.default_rng(123)
+    n = min(w.T, 4)
+    done_tokens, t_total = 0, 0.0
+    while True:
+        toks = np.sort(rng.choice(w.T, n, replace=False))
+        t0 = time.perf_counter()
+        _oracle_sample(w, inp, toks)
+        t_total += time.perf_counter() - t0
+        done_tokens += n
+        if t_total >= budget_s or done_tokens >= w.T:
+            break
+    return {"value": done_tokens / t_total, "unit": "tokens/s", "cores": _blas_threads(),
+            "kind": "oracle",
+            "sample": f"{done_tokens} of {w.T} tokens ({n} per call), fp64 numpy oracle: route, "
+                      f"expert FFNs of the chosen experts, combine; {t_total:.1f} s",
+            "cpu_model": _cpu_model()}
+
+
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    inp = moe_synth.layer_inputs(w)
+    rng = np.random.default_rng(7)
+    n = min(w.T, 2)
+    for _ in range(args.warmup):
+        _oracle_sample(w, inp, np.sort(rng.choice(w.T, n, replace=False)))
+    times = []
+    for _ in range(args.steps):
+        toks = np.sort(rng.choice(w.T, n, replace=False))
+        t0 = time.perf_counter()
+        _oracle_sample(w, inp, toks)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = n / (ms / 1e3)
+    cores = _blas_threads()
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F,
+                       "latent": w.latent or None, "bias": w.bias},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"{n} tokens of {w.T} per step through the fp64 oracle",
+                             "cpu_model": _cpu_model()},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="nano_decode",
+                    choices=[k for k, v in moe_synth.WORKLOADS.items() if not v.nvfp4])
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = moe_synth.WORKLOADS[args.workload]
+    if args.steps is None:
+        # enough steps for about two seconds of timed work (clock samples land inside it)
+        args.steps = {"nano_decode": 2000, "tiny": 2000}.get(w.name, 500) \
+            if args.impl == "ours" else 5
+    args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
+    out = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

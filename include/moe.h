@@ -1,0 +1,167 @@
+/*
+ * moe.h: C ABI of the B300 (sm_103a) routed Mixture-of-Experts layer forward pass.
+ *
+ * The layer follows "NVIDIA Nemotron 3: Efficient and Open Intelligence" (papercache
+ * notes) §2.1-§2.2 with Fig. 3b, the two "Nemotron 3 Nano" summaries (papers.lianghsun.dev
+ * §2.2, aux-loss-free balancing; shd-paper.top 技术框架, route -> experts -> weighted
+ * combination), and the news piece "NVIDIA AI发布了Nemotron 3" (混合Mamba Transformer
+ * MoE架构: a learned router picks 6 of 128 routable experts).
+ *
+ * Conventions shared by every call:
+ *  - bfloat16 tensors are passed as uint16_t bit patterns. All matrices are row-major.
+ *    Weights are stored [out_features, in_features], so the contraction axis is the
+ *    contiguous one.
+ *  - All tensor pointers are DEVICE pointers, owned by the caller. No call allocates or
+ *    frees device memory. Scratch comes from a caller-provided workspace of at least the
+ *    size that the matching *_workspace_size() reports. Outputs and workspace must not
+ *    overlap the inputs.
+ *  - Calls are asynchronous on `stream`. A call returns after its kernels are enqueued.
+ *    The return code covers argument checks and launch errors only.
+ *  - Faults found on the device (an expert index out of range, a duplicate expert in one
+ *    token's list, a pipeline wait that ran out of time) set a device status word. Read
+ *    it with moe_get_device_status().
+ *  - Sizes: H, F and the latent size L must be multiples of 64. Tensor pointers must be
+ *    16-byte aligned. 1 <= E <= 1024 and 1 <= k <= min(E, 32). T*k must fit in int32.
+ *    T == 0 is allowed and does nothing.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size, bad index   */
+  MOE_ERR_UNSUPPORTED = 2,  /* size or alignment outside what the kernels handle        */
+  MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than *_workspace_size()     */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed              */
+  MOE_ERR_TIMEOUT = 5       /* a device pipeline wait exceeded its limit (device word)  */
+};
+
+/* Text for a status code. The string is static and must not be freed. */
+const char* moe_status_string(int status);
+
+/* Synchronise `stream`, then read and clear the current device's status word. The word
+ * holds MOE_OK or the first error that a kernel recorded since it was last cleared. */
+int moe_get_device_status(cudaStream_t stream, int* status_out);
+
+/* ---------------------------------------------------------------------------------------
+ * moe_route: the learned router with aux-loss-free, bias-corrected top-k.
+ *   z[t,e] = sum_d x[t,d] * w_router[e,d]   (bf16 inputs, fp32 accumulation)
+ *   s = sigmoid(z); u = s + bias[e] (bias for SELECTION only)
+ *   topk_idx[t,:] = the k experts with the largest u, in descending u; the lower expert
+ *                   index wins exact ties
+ *   gates[t,j]    = s[t,topk_idx[t,j]] / sum_j' s[t,topk_idx[t,j']]
+ *   tie_flag[t]   = 1 when u_(k) - u_(k+1) < 1e-5 (a near-tie diagnostic; may be NULL)
+ * Pages: Nemotron 3 Nano summary §2.2 (aux-loss-free balancing), news piece (learned
+ * router, top-6 of 128). The sigmoid/bias/renormalisation details are this library's
+ * reading of the aux-loss-free scheme.
+ * Layout: x [T,D] bf16, w_router [E,D] bf16, bias [E] fp32; topk_idx [T,k] int32,
+ * gates [T,k] fp32, tie_flag [T] uint8. Workspace: moe_route_workspace_size().
+ * ------------------------------------------------------------------------------------- */
+size_t moe_route_workspace_size(int T, int D, int E, int k);
+int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias,
+              int T, int D, int E, int k,
+              int32_t* topk_idx, float* gates, uint8_t* tie_flag,
+              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * moe_permute: dispatch of the routed (token, slot) pairs into expert-contiguous order.
+ *   counts[e]        rows routed to expert e
+ *   offsets[e]       exclusive prefix sum of counts; offsets[E] = T*k
+ *   row_token[r]     token of permuted row r (rows of one expert in ascending token order)
+ *   slot_row[t*k+j]  permuted row that holds (token t, slot j); -1 if topk_idx was invalid
+ *   x_perm[r,:]      = x[row_token[r],:]
+ * Pages: shd-paper.top summary 技术框架 (the selected experts process their tokens in
+ * parallel); NVIDIA Nemotron 3 notes §2.2 (token dispatch to experts).
+ * Layout: topk_idx [T,k] int32, x [T,H] bf16; outputs as above, x_perm [T*k,H] bf16.
+ * Invalid or duplicate expert indices are reported on the device status word
+ * (MOE_ERR_INVALID_ARG). Workspace: moe_permute_workspace_size().
+ * ------------------------------------------------------------------------------------- */
+size_t moe_permute_workspace_size(int T, int E, int k);
+int moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int H, int E, int k,
+                int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
+                uint16_t* x_perm, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * moe_grouped_ffn: every expert's FFN on its segment of permuted rows.
+ *   for rows r in [offsets[e], offsets[e+1]):
+ *     h[r,:]      = max(0, x_perm[r,:] . w_up[e]^T)^2     (squared ReLU, stored bf16)
+ *     y_perm[r,:] = h[r,:] . w_down[e]^T
+ * Pages: NVIDIA Nemotron 3 notes §2.2 (each expert matrix is H x C; decode-sized batches
+ * are bound by reading expert weights). The activation is this library's reading.
+ * Layout: x_perm [rows,H] bf16, offsets [E+1] int32 (device), w_up [E,F,H] bf16,
+ * w_down [E,H,F] bf16, y_perm [rows,H] bf16. fp32 accumulation on tcgen05 tensor cores.
+ * Workspace: moe_grouped_ffn_workspace_size() (holds h).
+ * ------------------------------------------------------------------------------------- */
+size_t moe_grouped_ffn_workspace_size(int rows, int H, int F, int E);
+int moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets,
+                    const uint16_t* w_up, const uint16_t* w_down,
+                    int rows, int H, int F, int E, uint16_t* y_perm,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * moe_combine: the combination layer, the gate-weighted sum back in token order.
+ *   y[t,:] = sum_j gates[t*k+j] * y_perm[slot_row[t*k+j],:]   (fp32 accumulation)
+ * Pages: shd-paper.top summary 技术框架 (weighted combination of the experts' outputs).
+ * Rows with slot_row outside [0, rows) are skipped.
+ * Layout: y_perm [rows,H] bf16, slot_row [T*k] int32, gates [T*k] fp32, y [T,H] bf16.
+ * ------------------------------------------------------------------------------------- */
+int moe_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row,
+                const float* gates, int T, int H, int k, uint16_t* y,
+                cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * moe_linear: y[t,:] = x[t,:] . w^T (bf16 in, fp32 accumulation, bf16 out).
+ * Used for the LatentMoE projections, which the pages keep in BF16 (NVIDIA Nemotron 3
+ * notes §2.4). Layout: x [T,K] bf16, w [N,K] bf16, y [T,N] bf16. K and N multiples of 64.
+ * ------------------------------------------------------------------------------------- */
+int moe_linear(const uint16_t* x, const uint16_t* w, int T, int K, int N, uint16_t* y,
+               cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * moe_forward: route + permute + grouped FFN + combine, the whole routed MoE layer.
+ * Layout: x [T,H], w_router [E,H], bias [E] fp32, w_up [E,F,H], w_down [E,H,F], y [T,H].
+ * topk_idx_out [T,k] and gates_out [T,k] are optional copies of the routing (NULL to skip).
+ * Workspace: moe_forward_workspace_size().
+ * ------------------------------------------------------------------------------------- */
+size_t moe_forward_workspace_size(int T, int H, int E, int k, int F);
+int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                const uint16_t* w_up, const uint16_t* w_down,
+                int T, int H, int E, int k, int F, uint16_t* y,
+                int32_t* topk_idx_out, float* gates_out,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * latent_moe: the LatentMoE layer (NVIDIA Nemotron 3 notes §2.2, Fig. 3b).
+ *   x_lat = x . w_in^T                      (H -> L, bf16 projection)
+ *   route x_lat (router_on_latent = 1, w_router [Ep,L]) or x (router_on_latent = 0,
+ *   w_router [Ep,H]) to Ep experts with kp active, run the experts in L
+ *   (w_up [Ep,F,L], w_down [Ep,L,F]), combine in L,
+ *   y = y_lat . w_out^T                     (L -> H, bf16 projection, applied once)
+ * The pages scale experts as Ep = E*H/L and kp = k*H/L; both are free parameters here.
+ * For routing on the latent vector, x_lat is kept to about fp32 accuracy (three bf16
+ * planes hi + mid + lo), so the selection does not depend on the bf16 rounding of x_lat.
+ * The experts read the bf16 x_lat (hi).
+ * topk_idx_out / gates_out [T,kp] are optional. Workspace: latent_moe_workspace_size().
+ * ------------------------------------------------------------------------------------- */
+size_t latent_moe_workspace_size(int T, int H, int L, int Ep, int kp, int F,
+                                 int router_on_latent);
+int latent_moe(const uint16_t* x, const uint16_t* w_in, const uint16_t* w_out,
+               const uint16_t* w_router, const float* bias, int router_on_latent,
+               const uint16_t* w_up, const uint16_t* w_down,
+               int T, int H, int L, int Ep, int kp, int F, uint16_t* y,
+               int32_t* topk_idx_out, float* gates_out,
+               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -186,3 +186,19 @@ def random_gates(seed: int, T: int, k: int) -> np.ndarray:
     g = _rng(seed, 98)
     a = g.uniform(0.05, 1.0, size=(T, k))
     return (a / a.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def to_torch(a: np.ndarray, device=None):
+    """numpy array -> torch tensor (uint16 bit patterns become torch.bfloat16)."""
+    import torch
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(device) if device is not None else t
+
+
+def from_torch_bf16(t) -> np.ndarray:
+    """torch.bfloat16 tensor -> numpy uint16 bit patterns."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

@@ -1,0 +1,22 @@
+"""B300-native (sm_103a) routed Mixture-of-Experts layer forward pass.
+
+The compute lives in libmoe.so (hand-written CUDA: tcgen05 tensor-core grouped GEMMs fed by
+TMA, warp-level router top-k, deterministic permutation and combine). This package is the
+thin Python binding of its C ABI (include/moe.h). Torch supplies device memory and streams.
+"""
+from ._binding import (  # noqa: F401
+    MoeError,
+    SIGNATURES,
+    get_device_status,
+    latent_moe,
+    latent_moe_workspace_size,
+    lib,
+    moe_combine,
+    moe_forward,
+    moe_forward_workspace_size,
+    moe_grouped_ffn,
+    moe_linear,
+    moe_permute,
+    moe_route,
+    status_string,
+)

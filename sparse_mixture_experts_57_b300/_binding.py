@@ -1,0 +1,234 @@
+"""ctypes binding of libmoe's C ABI (argument marshalling only).
+
+Every function here checks tensor dtypes, devices and shapes, allocates outputs and
+workspaces with torch (device memory only), and calls the C entry point of the same
+name on the current CUDA stream. All arithmetic happens in the library's CUDA kernels.
+There is no CPU fallback: without the built library or a CUDA device, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_LIB = None
+
+_VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/moe.h
+SIGNATURES = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_get_device_status": (_I, [_VP, ctypes.POINTER(_I)]),
+    "moe_route_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "moe_route": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
+    "moe_permute": (_I, [_VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_grouped_ffn_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "moe_grouped_ffn": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _SZ, _VP]),
+    "moe_combine": (_I, [_VP, _I, _VP, _VP, _I, _I, _I, _VP, _VP]),
+    "moe_linear": (_I, [_VP, _VP, _I, _I, _I, _VP, _VP]),
+    "moe_forward_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ,
+                         _VP]),
+    "latent_moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "latent_moe": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP,
+                        _VP, _VP, _SZ, _VP]),
+}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if needed) the in-tree libmoe.so."""
+    global _LIB
+    with _lock:
+        if _LIB is None:
+            path = _build.ensure_built()
+            L = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _LIB = L
+    return _LIB
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise MoeError(code, where)
+
+
+def _cuda_tensor(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    return t
+
+
+def _workspace(nbytes: int, device, ws=None):
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return ws
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def get_device_status(stream=None) -> int:
+    out = ctypes.c_int(0)
+    _check(lib().moe_get_device_status(_stream(stream), ctypes.byref(out)),
+           "moe_get_device_status")
+    return out.value
+
+
+# ------------------------------------------------------------------------------ calls ----
+
+def moe_route(x, w_router, bias, k: int, *, workspace=None, stream=None):
+    bf = torch.bfloat16
+    _cuda_tensor(x, bf, "x", 2)
+    _cuda_tensor(w_router, bf, "w_router", 2)
+    _cuda_tensor(bias, torch.float32, "bias", 1)
+    T, D = x.shape
+    E = w_router.shape[0]
+    idx = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    gates = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    tie = torch.empty((T,), dtype=torch.uint8, device=x.device)
+    L = lib()
+    ws = _workspace(L.moe_route_workspace_size(T, D, E, k), x.device, workspace)
+    _check(L.moe_route(_ptr(x), _ptr(w_router), _ptr(bias), T, D, E, k, _ptr(idx), _ptr(gates),
+                       _ptr(tie), _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
+    return idx, gates, tie
+
+
+def moe_permute(topk_idx, x, E: int, *, workspace=None, stream=None):
+    _cuda_tensor(topk_idx, torch.int32, "topk_idx", 2)
+    _cuda_tensor(x, torch.bfloat16, "x", 2)
+    T, k = topk_idx.shape
+    H = x.shape[1]
+    dev = x.device
+    counts = torch.empty((E,), dtype=torch.int32, device=dev)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    row_token = torch.empty((T * k,), dtype=torch.int32, device=dev)
+    slot_row = torch.empty((T * k,), dtype=torch.int32, device=dev)
+    x_perm = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+    L = lib()
+    ws = _workspace(L.moe_permute_workspace_size(T, E, k), dev, workspace)
+    _check(L.moe_permute(_ptr(topk_idx), _ptr(x), T, H, E, k, _ptr(counts), _ptr(offsets),
+                         _ptr(row_token), _ptr(slot_row), _ptr(x_perm), _ptr(ws), ws.numel(),
+                         _stream(stream)), "moe_permute")
+    return {"counts": counts, "offsets": offsets, "row_token": row_token, "slot_row": slot_row,
+            "x_perm": x_perm}
+
+
+def moe_grouped_ffn(x_perm, offsets, w_up, w_down, *, out=None, workspace=None, stream=None):
+    bf = torch.bfloat16
+    _cuda_tensor(x_perm, bf, "x_perm", 2)
+    _cuda_tensor(offsets, torch.int32, "offsets", 1)
+    _cuda_tensor(w_up, bf, "w_up", 3)
+    _cuda_tensor(w_down, bf, "w_down", 3)
+    rows, H = x_perm.shape
+    E, F, _ = w_up.shape
+    y = out if out is not None else torch.empty((rows, H), dtype=bf, device=x_perm.device)
+    L = lib()
+    ws = _workspace(L.moe_grouped_ffn_workspace_size(rows, H, F, E), x_perm.device, workspace)
+    _check(L.moe_grouped_ffn(_ptr(x_perm), _ptr(offsets), _ptr(w_up), _ptr(w_down), rows, H, F,
+                             E, _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_ffn")
+    return y
+
+
+def moe_combine(y_perm, slot_row, gates, T: int, k: int, *, out=None, stream=None):
+    _cuda_tensor(y_perm, torch.bfloat16, "y_perm", 2)
+    _cuda_tensor(slot_row, torch.int32, "slot_row")
+    _cuda_tensor(gates, torch.float32, "gates")
+    rows, H = y_perm.shape
+    y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=y_perm.device)
+    _check(lib().moe_combine(_ptr(y_perm), rows, _ptr(slot_row), _ptr(gates), T, H, k, _ptr(y),
+                             _stream(stream)), "moe_combine")
+    return y
+
+
+def moe_linear(x, w, *, out=None, stream=None):
+    _cuda_tensor(x, torch.bfloat16, "x", 2)
+    _cuda_tensor(w, torch.bfloat16, "w", 2)
+    T, K = x.shape
+    N = w.shape[0]
+    y = out if out is not None else torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_linear(_ptr(x), _ptr(w), T, K, N, _ptr(y), _stream(stream)), "moe_linear")
+    return y
+
+
+def moe_forward_workspace_size(T, H, E, k, F) -> int:
+    return int(lib().moe_forward_workspace_size(T, H, E, k, F))
+
+
+def moe_forward(x, w_router, bias, w_up, w_down, k: int, *, out=None, topk_idx_out=None,
+                gates_out=None, workspace=None, stream=None):
+    bf = torch.bfloat16
+    _cuda_tensor(x, bf, "x", 2)
+    _cuda_tensor(w_router, bf, "w_router", 2)
+    _cuda_tensor(bias, torch.float32, "bias", 1)
+    _cuda_tensor(w_up, bf, "w_up", 3)
+    _cuda_tensor(w_down, bf, "w_down", 3)
+    T, H = x.shape
+    E, F, _ = w_up.shape
+    y = out if out is not None else torch.empty((T, H), dtype=bf, device=x.device)
+    L = lib()
+    ws = _workspace(L.moe_forward_workspace_size(T, H, E, k, F), x.device, workspace)
+    _check(L.moe_forward(_ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_up), _ptr(w_down), T, H, E,
+                         k, F, _ptr(y), _ptr(topk_idx_out), _ptr(gates_out), _ptr(ws),
+                         ws.numel(), _stream(stream)), "moe_forward")
+    return y
+
+
+def latent_moe_workspace_size(T, H, L_, Ep, kp, F, router_on_latent=True) -> int:
+    return int(lib().latent_moe_workspace_size(T, H, L_, Ep, kp, F, int(router_on_latent)))
+
+
+def latent_moe(x, w_in, w_out, w_router, bias, w_up, w_down, kp: int, *,
+               router_on_latent: bool = True, out=None, topk_idx_out=None, gates_out=None,
+               workspace=None, stream=None):
+    bf = torch.bfloat16
+    for t, n, d in ((x, "x", 2), (w_in, "w_in", 2), (w_out, "w_out", 2),
+                    (w_router, "w_router", 2), (w_up, "w_up", 3), (w_down, "w_down", 3)):
+        _cuda_tensor(t, bf, n, d)
+    _cuda_tensor(bias, torch.float32, "bias", 1)
+    T, H = x.shape
+    Lat = w_in.shape[0]
+    Ep, F, _ = w_up.shape
+    y = out if out is not None else torch.empty((T, H), dtype=bf, device=x.device)
+    L = lib()
+    ws = _workspace(L.latent_moe_workspace_size(T, H, Lat, Ep, kp, F, int(router_on_latent)),
+                    x.device, workspace)
+    _check(L.latent_moe(_ptr(x), _ptr(w_in), _ptr(w_out), _ptr(w_router), _ptr(bias),
+                        int(router_on_latent), _ptr(w_up), _ptr(w_down), T, H, Lat, Ep, kp, F,
+                        _ptr(y), _ptr(topk_idx_out), _ptr(gates_out), _ptr(ws), ws.numel(),
+                        _stream(stream)), "latent_moe")
+    return y

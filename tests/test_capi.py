@@ -1,0 +1,74 @@
+"""The C ABI library builds, loads and exports every symbol that include/moe.h declares.
+
+CPU only: no compute call is made (there is no GPU here). Argument checks that return
+before any CUDA call are exercised too.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mixture_experts_57_b300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n.startswith(("moe_", "latent_"))))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for want in ["moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_forward",
+                 "latent_moe", "moe_linear", "moe_get_device_status", "moe_status_string"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = moe.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in moe.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings():
+    assert moe.status_string(0) == "ok"
+    assert "timed out" in moe.status_string(5)
+    assert moe.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes_are_monotone():
+    L = moe.lib()
+    a = L.moe_forward_workspace_size(64, 2688, 128, 6, 1856)
+    b = L.moe_forward_workspace_size(16384, 2688, 128, 6, 1856)
+    assert 0 < a < b
+    # x_perm + h + y_perm dominate: rows * (2H + F) * 2 bytes
+    assert b >= 16384 * 6 * (2 * 2688 + 1856) * 2
+    assert L.moe_forward_workspace_size(-1, 64, 4, 2, 64) == 0
+    assert L.latent_moe_workspace_size(8192, 4096, 1024, 512, 24, 1024, 1) > \
+        L.latent_moe_workspace_size(8192, 4096, 1024, 512, 24, 1024, 0)
+
+
+@pytest.mark.parametrize("args", [
+    (0, 0, 0, 4, 64, 8, 2, 0, 0, 0, 0, 0, 0),        # null pointers with T > 0
+    (1, 1, 1, 4, 64, 2000, 2, 1, 1, 1, 1, 1, 0),     # E > 1024
+    (1, 1, 1, 4, 64, 8, 9, 1, 1, 1, 1, 1, 0),        # k > E
+    (1, 1, 1, -3, 64, 8, 2, 1, 1, 1, 1, 1, 0),       # negative T
+])
+def test_route_rejects_bad_arguments_before_any_cuda_call(args):
+    L = moe.lib()
+    assert L.moe_route(*args) == 1   # MOE_ERR_INVALID_ARG
+
+
+def test_unaligned_sizes_are_unsupported():
+    L = moe.lib()
+    # H not a multiple of 64 (pointers are fake but never dereferenced)
+    r = L.moe_forward(16, 16, 16, 16, 16, 4, 100, 8, 2, 64, 16, None, None, 16, 1 << 20, None)
+    assert r == 2
+    r = L.moe_linear(16, 16, 4, 96, 64, 16, None)
+    assert r == 2

@@ -1,0 +1,251 @@
+"""GPU path vs the fp64 oracle, element by element, on seeded inputs (needs a B300).
+
+Small cases span several tiles and a ragged tail and are compared in full. The full-size
+layer workloads are compared on every routing integer and on sampled token outputs.
+"""
+import numpy as np
+import pytest
+
+import moe_synth
+from oracle import moe_oracle as O
+from helpers import (assert_close, bf16_out, check_selection, gates_by_expert, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import sparse_mixture_experts_57_b300 as m
+    m.lib()
+    m.get_device_status()   # clears the status word
+    return m
+
+
+def _status_ok(moe):
+    assert moe.get_device_status() == 0
+
+
+def _bf(seed, shape, std=1.0):
+    return moe_synth.normal_bf16(seed, 50, shape, std)
+
+
+# ------------------------------------------------------------------------------ GEMM ----
+
+@pytest.mark.parametrize("T,K,N", [(1, 64, 64), (37, 128, 64), (300, 256, 192), (513, 320, 448),
+                                   (1000, 512, 256), (2048, 1024, 1856)])
+def test_linear(moe, T, K, N):
+    x = _bf(T * 7 + 1, (T, K))
+    w = _bf(T * 7 + 2, (N, K), 1 / np.sqrt(K))
+    y = moe.moe_linear(to_dev(x), to_dev(w))
+    torch.cuda.synchronize()
+    assert_close(bf16_out(y), O.latent_project_in(x, w), f"linear {T}x{K}x{N}")
+    _status_ok(moe)
+
+
+# ---------------------------------------------------------------------------- router ----
+
+def _route_case(moe, T, D, E, k, seed, bias_kind="uniform"):
+    w = moe_synth.Workload("r", T=T, H=D, E=E, k=k, F=64, seed=seed, bias=bias_kind)
+    inp = moe_synth.layer_inputs(w, with_experts=False)
+    idx, gates, tie = moe.moe_route(to_dev(inp["x"]), to_dev(inp["w_router"]),
+                                    to_dev(inp["bias"]), k)
+    torch.cuda.synchronize()
+    ref = O.route(inp["x"], inp["w_router"], inp["bias"], k)
+    gi = idx.cpu().numpy()
+    same = check_selection(gi, ref, inp["bias"], k)
+    g = gates.cpu().numpy().astype(np.float64)
+    # Gates inherit the logits' error: fp32 tensor-core accumulation of D bf16 products
+    # leaves about 1e-5 absolute error in z at D = 2688, i.e. about 1e-5 relative in s.
+    np.testing.assert_allclose(gates_by_expert(gi, g)[same],
+                               gates_by_expert(ref["idx"], ref["gates"])[same],
+                               rtol=1e-4, atol=1e-6)
+    np.testing.assert_allclose(g.sum(axis=1), 1.0, atol=1e-6)
+    _status_ok(moe)
+    return int((ref["gap"] < 1e-5).sum())
+
+
+@pytest.mark.parametrize("T,D,E,k", [(1, 64, 16, 2), (256, 256, 16, 2), (77, 2688, 128, 6),
+                                     (600, 512, 128, 6), (1100, 1024, 512, 24), (513, 256, 64, 8),
+                                     (40, 128, 1000, 32)])
+def test_route(moe, T, D, E, k):
+    _route_case(moe, T, D, E, k, seed=T + E)
+
+
+def test_route_nano_prefill_full(moe):
+    w = moe_synth.WORKLOADS["nano_prefill"]
+    ties = _route_case(moe, w.T, w.H, w.E, w.k, w.seed, w.bias)
+    assert ties < 50
+
+
+# --------------------------------------------------------------------------- permute ----
+
+@pytest.mark.parametrize("T,E,k,skew", [(1, 4, 1, 0), (31, 16, 2, 0), (33, 16, 2, 1.0),
+                                        (1000, 128, 6, 1.2), (4099, 512, 24, 0.5),
+                                        (700, 1024, 3, 0)])
+def test_permute(moe, T, E, k, skew):
+    idx = moe_synth.random_topk(T + E, T, E, k, skew)
+    H = 64
+    x = _bf(T, (T, H))
+    p = moe.moe_permute(to_dev(idx), to_dev(x), E)
+    torch.cuda.synchronize()
+    ref = O.permute(idx, E)
+    for key in ("counts", "offsets", "row_token", "slot_row"):
+        np.testing.assert_array_equal(p[key].cpu().numpy(), ref[key], err_msg=key)
+    xp = moe_synth.from_torch_bf16(p["x_perm"])
+    np.testing.assert_array_equal(xp, x[ref["row_token"]])
+    _status_ok(moe)
+
+
+def test_permute_reports_bad_expert_index(moe):
+    idx = moe_synth.random_topk(5, 64, 8, 2)
+    idx[3, 1] = 9            # out of range
+    idx[7, 1] = idx[7, 0]    # duplicate
+    x = _bf(1, (64, 64))
+    p = moe.moe_permute(to_dev(idx), to_dev(x), 8)
+    assert moe.get_device_status() == 1
+    sr = p["slot_row"].cpu().numpy()
+    assert sr[3 * 2 + 1] == -1
+    _status_ok(moe)
+
+
+# --------------------------------------------------------------------------- combine ----
+
+@pytest.mark.parametrize("T,H,k", [(1, 64, 1), (100, 192, 6), (257, 2688, 6), (64, 1024, 24)])
+def test_combine(moe, T, H, k):
+    E = max(k, 8)
+    idx = moe_synth.random_topk(T, T, E, k)
+    p = O.permute(idx, E)
+    yp = _bf(T + 3, (T * k, H))
+    g = moe_synth.random_gates(T, T, k)
+    y = moe.moe_combine(to_dev(yp), to_dev(p["slot_row"]), to_dev(g.reshape(-1)), T, k)
+    torch.cuda.synchronize()
+    ref = O.combine(yp, p["slot_row"], g, T, k)
+    assert_close(bf16_out(y), ref, "combine", rel_frob=4e-3, maxabs_rms=2e-2)
+
+
+# ----------------------------------------------------------------------- grouped FFN ----
+
+@pytest.mark.parametrize("T,E,k,H,F,skew", [
+    (64, 16, 1, 128, 64, 0.0),        # ~4 rows per expert: weights-as-M, N=16
+    (120, 8, 2, 256, 128, 0.0),       # ~30 rows: weights-as-M, N=32
+    (200, 8, 2, 256, 192, 0.5),       # ~50 rows: rows-as-M
+    (700, 8, 3, 512, 448, 1.5),       # skewed, several row tiles, ragged tails
+    (300, 32, 4, 320, 1856, 1.0),     # many N tiles with a ragged last tile
+    (40, 128, 6, 2688, 1856, 0.0),    # decode-like: many experts with few rows
+])
+def test_grouped_ffn(moe, T, E, k, H, F, skew):
+    idx = moe_synth.random_topk(T * 3 + E, T, E, k, skew)
+    p = O.permute(idx, E)
+    rows = T * k
+    xp = _bf(rows, (rows, H))
+    wu = moe_synth.expert_stack(T, moe_synth.TAG_UP, E, F, H)
+    wd = moe_synth.expert_stack(T, moe_synth.TAG_DOWN, E, H, F)
+    y = moe.moe_grouped_ffn(to_dev(xp), to_dev(p["offsets"]), to_dev(wu), to_dev(wd))
+    torch.cuda.synchronize()
+    ref = O.grouped_ffn(xp, p["offsets"], wu, wd)
+    assert_close(bf16_out(y), ref, "grouped ffn")
+    _status_ok(moe)
+
+
+# --------------------------------------------------------------------- whole layer ----
+
+def _layer_full(moe, w):
+    inp = moe_synth.layer_inputs(w)
+    dev = {k: to_dev(v) for k, v in inp.items()}
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    y = moe.moe_forward(dev["x"], dev["w_router"], dev["bias"], dev["w_up"], dev["w_down"], w.k,
+                        topk_idx_out=idx, gates_out=gates)
+    torch.cuda.synchronize()
+    ref = O.moe_layer(inp["x"], inp["w_router"], inp["bias"], inp["w_up"], inp["w_down"], w.k)
+    same = check_selection(idx.cpu().numpy(), ref, inp["bias"], w.k)
+    assert_close(bf16_out(y)[same], ref["y"][same], f"{w.name} layer")
+    _status_ok(moe)
+    return ref, same
+
+
+def test_layer_tiny(moe):
+    _layer_full(moe, moe_synth.WORKLOADS["tiny"])
+
+
+@pytest.mark.parametrize("T,H,E,k,F", [(1, 64, 4, 1, 64), (33, 128, 8, 8, 64),
+                                       (513, 256, 32, 4, 192), (97, 512, 64, 6, 256)])
+def test_layer_shapes(moe, T, H, E, k, F):
+    _layer_full(moe, moe_synth.Workload("shape", T=T, H=H, E=E, k=k, F=F, seed=T + H))
+
+
+def test_layer_nano_decode_full(moe):
+    """The whole decode workload (64 tokens, 128 experts, top-6) against the oracle."""
+    _layer_full(moe, moe_synth.WORKLOADS["nano_decode"])
+
+
+def _sampled_layer(moe, w, n_sample=40):
+    inp = moe_synth.layer_inputs(w)
+    dev = {k: to_dev(v) for k, v in inp.items()}
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    y = moe.moe_forward(dev["x"], dev["w_router"], dev["bias"], dev["w_up"], dev["w_down"], w.k,
+                        topk_idx_out=idx, gates_out=gates)
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    ref = O.route(inp["x"], inp["w_router"], inp["bias"], w.k)
+    gi = idx.cpu().numpy()
+    same = check_selection(gi, ref, inp["bias"], w.k)
+    if same.all():
+        p = O.permute(ref["idx"], w.E)
+        assert (np.bincount(gi.reshape(-1), minlength=w.E) == p["counts"]).all()
+    rng = np.random.default_rng(w.seed)
+    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n_sample, replace=False)]))
+    toks = toks[same[toks]]
+    ref_y = O.moe_tokens(inp["x"][toks], ref["idx"][toks], ref["gates"][toks], inp["w_up"],
+                         inp["w_down"])
+    assert_close(bf16_out(y)[toks], ref_y, f"{w.name} sampled tokens")
+
+
+@pytest.mark.slow
+def test_layer_nano_prefill_sampled(moe):
+    _sampled_layer(moe, moe_synth.WORKLOADS["nano_prefill"])
+
+
+# ------------------------------------------------------------------------- LatentMoE ----
+
+def _latent_case(moe, w, full=True, n_sample=24):
+    inp = moe_synth.layer_inputs(w)
+    dev = {k: to_dev(v) for k, v in inp.items()}
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    y = moe.latent_moe(dev["x"], dev["w_in"], dev["w_out"], dev["w_router"], dev["bias"],
+                       dev["w_up"], dev["w_down"], w.k, router_on_latent=w.router_on_latent,
+                       topk_idx_out=idx, gates_out=gates)
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    x_lat = O.latent_project_in(inp["x"], inp["w_in"])
+    r_in = x_lat if w.router_on_latent else inp["x"]
+    ref = O.route(r_in, inp["w_router"], inp["bias"], w.k)
+    same = check_selection(idx.cpu().numpy(), ref, inp["bias"], w.k)
+    if full:
+        toks = np.arange(w.T)
+    else:
+        rng = np.random.default_rng(w.seed)
+        toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n_sample, replace=False)]))
+    toks = toks[same[toks]]
+    y_lat = O.moe_tokens(x_lat[toks], ref["idx"][toks], ref["gates"][toks], inp["w_up"],
+                         inp["w_down"])
+    ref_y = y_lat @ O.widen_bf16(inp["w_out"]).T
+    assert_close(bf16_out(y)[toks], ref_y, f"{w.name} latent")
+
+
+@pytest.mark.parametrize("router_on_latent", [True, False])
+def test_latent_small(moe, router_on_latent):
+    w = moe_synth.Workload("latent_small", T=300, H=512, E=32, k=8, F=128, seed=7, latent=128,
+                           router_on_latent=router_on_latent)
+    _latent_case(moe, w)
+
+
+@pytest.mark.slow
+def test_latent_full_sampled(moe):
+    _latent_case(moe, moe_synth.WORKLOADS["latent"], full=False)
