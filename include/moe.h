@@ -91,6 +91,30 @@ int moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int H, int E,
                 cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * moe_permute_noalloc: moe_permute for callers that cannot provide a workspace.
+ * The pages have no counterpart to this call; it exists for integration only. Some callers
+ * cannot hand the library device memory for scratch, for example a host runtime whose own
+ * pool owns all device memory and forbids other allocations, or a serving loop that runs
+ * on a fixed memory plan. This call takes the same inputs and outputs as moe_permute and
+ * gives the same results. Its scratch lives in a fixed array inside the library's device
+ * image: moe_permute_noalloc_max_scratch_bytes() bytes (2 MiB), held on every GPU that
+ * loads the library until the process exits. No call allocates or frees memory.
+ * Limits and rules:
+ *  - ceil(T/32) * E * 8 bytes (rounded up to 256-byte slices) must fit in that array, e.g.
+ *    T = 16384 with E = 512; larger problems return MOE_ERR_UNSUPPORTED (use moe_permute).
+ *  - All calls on one device share the array. Calls that overlap on the GPU (unordered
+ *    streams) race on it; calls ordered on one stream do not. Nothing in the array has to
+ *    start at zero: each call overwrites every word it reads.
+ *  - The first call on each device looks up the array's device address with that device
+ *    current. Make that first call before any stream capture.
+ * Arguments, layouts and device-side error reporting are those of moe_permute.
+ * ------------------------------------------------------------------------------------- */
+size_t moe_permute_noalloc_max_scratch_bytes(void);
+int moe_permute_noalloc(const int32_t* topk_idx, const uint16_t* x, int T, int H, int E, int k,
+                        int32_t* counts, int32_t* offsets, int32_t* row_token,
+                        int32_t* slot_row, uint16_t* x_perm, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * moe_grouped_ffn: every expert's FFN on its segment of permuted rows.
  *   for rows r in [offsets[e], offsets[e+1]):
  *     h[r,:]      = max(0, x_perm[r,:] . w_up[e]^T)^2     (squared ReLU, stored bf16)

@@ -27,6 +27,8 @@ SIGNATURES = {
     "moe_route": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_permute": (_I, [_VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_permute_noalloc_max_scratch_bytes": (_SZ, []),
+    "moe_permute_noalloc": (_I, [_VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_grouped_ffn_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "moe_grouped_ffn": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _SZ, _VP]),
     "moe_combine": (_I, [_VP, _I, _VP, _VP, _I, _I, _I, _VP, _VP]),
