@@ -3,7 +3,7 @@
 // "Nemotron 3 Nano" summary (shd-paper.top), 技术框架: a combination layer forms the
 // weighted combination of the chosen experts' outputs.
 //   y[t, :] = sum_j gates[t, j] * y_perm[slot_row[t, j], :]
-// Deterministic (no atomics): one warp per token, fp32 accumulation, 16-byte loads/stores.
+// Deterministic (no atomics), fp32 accumulation, 16-byte loads and stores.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -25,38 +25,32 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// One thread per (token, 8-element column block): every thread issues its k row loads
+// back to back, so even a 64-token decode batch keeps thousands of loads in flight.
 __global__ void k_combine(const uint16_t* __restrict__ y_perm, int rows,
                           const int32_t* __restrict__ slot_row, const float* __restrict__ gates,
                           int T, int H, int k, uint16_t* __restrict__ y) {
-  const int lane = threadIdx.x & 31;
-  const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
-  // lanes j < k hold slot j's row and gate
-  int my_row = -1;
-  float my_g = 0.f;
-  if (lane < k) {
-    my_row = slot_row[t * k + lane];
-    my_g = gates[t * k + lane];
-    if (my_row < 0 || my_row >= rows) my_row = -1;
-  }
+  griddep_wait();
+  griddep_launch_dependents();
   const int nvec = H / 8;
-  // The loop bound is warp-uniform so every lane takes part in the shuffles.
-  for (int base = 0; base < nvec; base += 32) {
-    const int v = base + lane;
-    const bool active = v < nvec;
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int r = __shfl_sync(0xffffffffu, my_row, j);
-      const float g = __shfl_sync(0xffffffffu, my_g, j);
-      if (r < 0 || !active) continue;
-      const uint4 yv =
-          __ldg(reinterpret_cast<const uint4*>(y_perm + static_cast<long long>(r) * H) + v);
-      acc8(a, yv, g);
-    }
-    if (active)
-      reinterpret_cast<uint4*>(y + t * H)[v] =
-          make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(T) * nvec) return;
+  const long long t = i / nvec;
+  const int v = static_cast<int>(i - t * nvec);
+  const int32_t* sr = slot_row + t * k;
+  const float* gg = gates + t * k;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int j = 0; j < k; ++j) {
+    const int r = __ldg(sr + j);
+    const float g = __ldg(gg + j);
+    if (r < 0 || r >= rows) continue;
+    const uint4 yv =
+        __ldg(reinterpret_cast<const uint4*>(y_perm + static_cast<long long>(r) * H) + v);
+    acc8(a, yv, g);
   }
+  reinterpret_cast<uint4*>(y + t * H)[v] =
+      make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
 }
 
 }  // namespace
@@ -65,11 +59,9 @@ int launch_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row, co
                    int T, int H, int k, uint16_t* y, cudaStream_t s) {
   if (T <= 0) return MOE_OK;
   const int threads = 256;
-  const long long blocks = (static_cast<long long>(T) * 32 + threads - 1) / threads;
-  k_combine<<<static_cast<unsigned>(blocks), threads, 0, s>>>(y_perm, rows, slot_row, gates, T, H,
-                                                              k, y);
-  MOE_LAUNCHED();
-  return MOE_OK;
+  const long long n = static_cast<long long>(T) * (H / 8);
+  return launch_pdl(k_combine, dim3(static_cast<unsigned>((n + threads - 1) / threads)),
+                    dim3(threads), 0, s, y_perm, rows, slot_row, gates, T, H, k, y);
 }
 
 }  // namespace moe

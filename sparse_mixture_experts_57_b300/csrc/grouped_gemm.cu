@@ -217,6 +217,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
+  // On-chip set-up above overlaps the previous kernel; global memory is touched only after
+  // it has completed.
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 2) {
     // Row segments of the groups and the exclusive prefix of their row-tile counts.
     const int per = (E + 31) / 32;
@@ -524,9 +528,7 @@ int launch_variant(const GroupedGemm& g, const KArgs& ka, cudaStream_t s) {
   const long long tiles = row_tiles * ((g.N + CT - 1) / CT);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   if (grid <= 0) return MOE_OK;
-  kern<<<grid, NUM_THREADS, smem, s>>>(tm_act, tm_w, ka);
-  MOE_LAUNCHED();
-  return MOE_OK;
+  return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), smem, s, tm_act, tm_w, ka);
 }
 
 int pick_bn_rows_as_m(int N) {

@@ -23,6 +23,39 @@ int cuda_status(cudaError_t e);
   } while (0)
 #define MOE_LAUNCHED() MOE_CUDA(cudaGetLastError())
 
+// Kernel launch with programmatic dependent launch: the kernel may be scheduled while its
+// predecessor on the stream is still running. Every kernel of this library calls
+// griddep_wait() before its first global-memory access, which waits for the predecessor
+// to complete and its writes to become visible, so stream order is kept. Only launch
+// latency and the kernels' set-up (barrier init, TMEM allocation) overlap.
+template <typename... Params, typename... Args>
+inline int launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+  return e == cudaSuccess ? 0 : cuda_status(e);
+}
+
+#ifdef __CUDACC__
+// Wait until the preceding kernel of the stream has completed and its memory is visible.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next kernel of the stream to be scheduled (it still waits in griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -12,6 +12,7 @@
 //   offsets : exclusive scan of counts
 //   gather  : rank of (t, e) = wpref[t/32][e] + popc(bits[t/32][e] below t's bit);
 //             row = offsets[e] + rank; copy the token row into x_perm with 16-byte moves.
+// Small problems run mark, count and offsets as one single-block kernel (k_perm_small).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -23,6 +24,8 @@ constexpr int kMarkWarps = 4;
 
 __global__ void k_perm_mark(const int32_t* __restrict__ idx, int T, int E, int k,
                             uint32_t* __restrict__ bits, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ uint32_t smask[];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
@@ -54,6 +57,8 @@ __global__ void k_perm_mark(const int32_t* __restrict__ idx, int T, int E, int k
 // Block (32 x 32): 32 experts per block along x, 32 chunks of token words along y.
 __global__ void k_perm_count(const uint32_t* __restrict__ bits, int W, int E,
                              int32_t* __restrict__ wpref, int32_t* __restrict__ counts) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ int part[32][33];
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int e = blockIdx.x * 32 + tx;
@@ -77,12 +82,11 @@ __global__ void k_perm_count(const uint32_t* __restrict__ bits, int W, int E,
   }
 }
 
-// Single block, 1024 threads: offsets = exclusive scan of counts (E <= 1024).
-__global__ void k_perm_offsets(const int32_t* __restrict__ counts, int E,
-                               int32_t* __restrict__ offsets) {
-  __shared__ int warp_sums[32];
+// Exclusive scan of one value per thread over a block of up to 1024 threads.
+// Returns this thread's exclusive prefix; *total receives the block sum.
+__device__ __forceinline__ int block_exclusive_scan(int c, int* warp_sums, int* total) {
   const int i = threadIdx.x, lane = i & 31, wid = i >> 5;
-  const int c = i < E ? counts[i] : 0;
+  const int nw = (blockDim.x + 31) >> 5;
   int incl = c;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -92,7 +96,7 @@ __global__ void k_perm_offsets(const int32_t* __restrict__ counts, int E,
   if (lane == 31) warp_sums[wid] = incl;
   __syncthreads();
   if (wid == 0) {
-    int ws = warp_sums[lane];
+    const int ws = lane < nw ? warp_sums[lane] : 0;
     int wincl = ws;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -100,11 +104,71 @@ __global__ void k_perm_offsets(const int32_t* __restrict__ counts, int E,
       if (lane >= d) wincl += v;
     }
     warp_sums[lane] = wincl - ws;
+    if (lane == 31) warp_sums[32] = wincl;
   }
   __syncthreads();
-  const int excl = warp_sums[wid] + incl - c;
+  *total = warp_sums[32];
+  return warp_sums[wid] + incl - c;
+}
+
+// Single block, 1024 threads: offsets = exclusive scan of counts (E <= 1024).
+__global__ void k_perm_offsets(const int32_t* __restrict__ counts, int E,
+                               int32_t* __restrict__ offsets) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int warp_sums[33];
+  const int i = threadIdx.x;
+  const int c = i < E ? counts[i] : 0;
+  int total;
+  const int excl = block_exclusive_scan(c, warp_sums, &total);
   if (i < E) offsets[i] = excl;
-  if (i == E - 1) offsets[E] = excl + c;
+  if (i == 0) offsets[E] = total;
+}
+
+// Small problems (few token words): one 1024-thread block marks, counts and scans in
+// shared memory, replacing the mark, count and offsets kernels.
+constexpr int kSmallMaxWords = 8192;  // ceil(T/32) * E bit-matrix words held in shared memory
+constexpr int kSmallMaxTokenWords = 64;
+
+__global__ void __launch_bounds__(1024)
+    k_perm_small(const int32_t* __restrict__ idx, int T, int E, int k,
+                 uint32_t* __restrict__ bits_g, int32_t* __restrict__ wpref_g,
+                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ uint32_t bits[];  // [W][E]
+  __shared__ int warp_sums[33];
+  const int W = (T + 31) / 32;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < W * E; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  bool bad = false;
+  const long long n = static_cast<long long>(T) * k;
+  for (long long i = tid; i < n; i += blockDim.x) {
+    const int t = static_cast<int>(i / k);
+    const int e = idx[i];
+    if (e < 0 || e >= E) {
+      bad = true;
+      continue;
+    }
+    const uint32_t bit = 1u << (t & 31);
+    if (atomicOr(&bits[(t >> 5) * E + e], bit) & bit) bad = true;
+  }
+  if (__syncthreads_or(bad) && tid == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+  int c = 0;
+  if (tid < E) {
+    for (int w = 0; w < W; ++w) {
+      const uint32_t b = bits[w * E + tid];
+      wpref_g[w * E + tid] = c;
+      bits_g[w * E + tid] = b;
+      c += __popc(b);
+    }
+    counts[tid] = c;
+  }
+  int total;
+  const int excl = block_exclusive_scan(c, warp_sums, &total);
+  if (tid < E) offsets[tid] = excl;
+  if (tid == 0) offsets[E] = total;
 }
 
 // One warp per (token, slot).
@@ -115,6 +179,8 @@ __global__ void k_perm_gather(const int32_t* __restrict__ idx, const uint16_t* _
                               const int32_t* __restrict__ offsets,
                               int32_t* __restrict__ row_token, int32_t* __restrict__ slot_row,
                               uint16_t* __restrict__ x_perm) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long gid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (gid >= static_cast<long long>(T) * k) return;
@@ -158,19 +224,30 @@ int launch_permute(const int32_t* idx, const uint16_t* x, int64_t ldx, int T, in
   uint32_t* bits = static_cast<uint32_t*>(scratch);
   int32_t* wpref = reinterpret_cast<int32_t*>(static_cast<char*>(scratch) +
                                               align_up(static_cast<size_t>(W) * E * 4, 256));
-  const size_t mark_smem = static_cast<size_t>(kMarkWarps) * E * 4;
-  k_perm_mark<<<(W + kMarkWarps - 1) / kMarkWarps, kMarkWarps * 32, mark_smem, s>>>(idx, T, E, k,
-                                                                                   bits, status);
-  MOE_LAUNCHED();
-  k_perm_count<<<(E + 31) / 32, dim3(32, 32), 0, s>>>(bits, W, E, wpref, counts);
-  MOE_LAUNCHED();
-  k_perm_offsets<<<1, 1024, 0, s>>>(counts, E, offsets);
-  MOE_LAUNCHED();
+  int st;
+  if (W <= kSmallMaxTokenWords && static_cast<long long>(W) * E <= kSmallMaxWords) {
+    st = launch_pdl(k_perm_small, dim3(1), dim3(1024), static_cast<size_t>(W) * E * 4, s, idx, T,
+                    E, k, bits, wpref, counts, offsets, status);
+    if (st) return st;
+  } else {
+    const size_t mark_smem = static_cast<size_t>(kMarkWarps) * E * 4;
+    st = launch_pdl(k_perm_mark, dim3((W + kMarkWarps - 1) / kMarkWarps), dim3(kMarkWarps * 32),
+                    mark_smem, s, idx, T, E, k, bits, status);
+    if (st) return st;
+    st = launch_pdl(k_perm_count, dim3((E + 31) / 32), dim3(32, 32), 0, s,
+                    static_cast<const uint32_t*>(bits), W, E, wpref, counts);
+    if (st) return st;
+    st = launch_pdl(k_perm_offsets, dim3(1), dim3(1024), 0, s, static_cast<const int32_t*>(counts),
+                    E, offsets);
+    if (st) return st;
+  }
   const long long warps = static_cast<long long>(T) * k;
   const int threads = 256;
-  k_perm_gather<<<static_cast<unsigned>((warps * 32 + threads - 1) / threads), threads, 0, s>>>(
-      idx, x, ldx, T, H, E, k, bits, wpref, offsets, row_token, slot_row, x_perm);
-  MOE_LAUNCHED();
+  st = launch_pdl(k_perm_gather, dim3(static_cast<unsigned>((warps * 32 + threads - 1) / threads)),
+                  dim3(threads), 0, s, idx, x, static_cast<long long>(ldx), T, H, E, k,
+                  static_cast<const uint32_t*>(bits), static_cast<const int32_t*>(wpref),
+                  static_cast<const int32_t*>(offsets), row_token, slot_row, x_perm);
+  if (st) return st;
   return MOE_OK;
 }
 

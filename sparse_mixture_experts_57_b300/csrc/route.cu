@@ -15,7 +15,7 @@
 namespace moe {
 namespace {
 
-constexpr int kTokPerWarp = 8;
+constexpr int kTokPerWarp = 4;
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -34,10 +34,13 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
 
 // logits[t, e] = sum_p sum_d x[t, p*D + d] * w[e, d] over `parts` planes: with parts > 1
 // the input row holds bf16 planes (hi, mid, lo) whose sum is a wider-precision vector.
-// One warp per (expert, group of 8 tokens); lanes stride over D in 8-element vectors.
+// One warp per (expert, group of 4 tokens); lanes stride over D in 8-element vectors,
+// four strides unrolled so their loads are in flight together.
 __global__ void k_router_logits(const uint16_t* __restrict__ x, long long ldx,
                                 const uint16_t* __restrict__ w, int T, int D, int E, int parts,
                                 float* __restrict__ logits) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int groups = (T + kTokPerWarp - 1) / kTokPerWarp;
@@ -49,6 +52,7 @@ __global__ void k_router_logits(const uint16_t* __restrict__ x, long long ldx,
   for (int i = 0; i < kTokPerWarp; ++i) acc[i] = 0.f;
   const uint4* wrow = reinterpret_cast<const uint4*>(w + static_cast<long long>(e) * D);
   const int nvec = D / 8;
+#pragma unroll 4
   for (int v = lane; v < nvec; v += 32) {
     const uint4 wv = __ldg(wrow + v);
 #pragma unroll
@@ -77,6 +81,8 @@ template <int VPL>
 __global__ void k_topk(const float* __restrict__ logits, const float* __restrict__ bias, int T,
                        int E, int k, int32_t* __restrict__ idx, float* __restrict__ gates,
                        uint8_t* __restrict__ tie) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -154,10 +160,8 @@ int launch_router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_route
   const long long warps = static_cast<long long>((T + kTokPerWarp - 1) / kTokPerWarp) * E;
   const int threads = 256;
   const long long blocks = (warps * 32 + threads - 1) / threads;
-  k_router_logits<<<static_cast<unsigned>(blocks), threads, 0, s>>>(x, ldx, w_router, T, D, E,
-                                                                    parts, logits);
-  MOE_LAUNCHED();
-  return MOE_OK;
+  return launch_pdl(k_router_logits, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
+                    x, static_cast<long long>(ldx), w_router, T, D, E, parts, logits);
 }
 
 int launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx,
@@ -165,21 +169,13 @@ int launch_topk(const float* logits, const float* bias, int T, int E, int k, int
   if (T <= 0) return MOE_OK;
   const int threads = 256;
   const long long blocks = (static_cast<long long>(T) * 32 + threads - 1) / threads;
-  const unsigned b = static_cast<unsigned>(blocks);
-  if (E <= 32)
-    k_topk<1><<<b, threads, 0, s>>>(logits, bias, T, E, k, idx, gates, tie);
-  else if (E <= 64)
-    k_topk<2><<<b, threads, 0, s>>>(logits, bias, T, E, k, idx, gates, tie);
-  else if (E <= 128)
-    k_topk<4><<<b, threads, 0, s>>>(logits, bias, T, E, k, idx, gates, tie);
-  else if (E <= 256)
-    k_topk<8><<<b, threads, 0, s>>>(logits, bias, T, E, k, idx, gates, tie);
-  else if (E <= 512)
-    k_topk<16><<<b, threads, 0, s>>>(logits, bias, T, E, k, idx, gates, tie);
-  else
-    k_topk<32><<<b, threads, 0, s>>>(logits, bias, T, E, k, idx, gates, tie);
-  MOE_LAUNCHED();
-  return MOE_OK;
+  const dim3 b(static_cast<unsigned>(blocks)), th(threads);
+  if (E <= 32) return launch_pdl(k_topk<1>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
+  if (E <= 64) return launch_pdl(k_topk<2>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
+  if (E <= 128) return launch_pdl(k_topk<4>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
+  if (E <= 256) return launch_pdl(k_topk<8>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
+  if (E <= 512) return launch_pdl(k_topk<16>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
+  return launch_pdl(k_topk<32>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
 }
 
 }  // namespace moe
