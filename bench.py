@@ -334,7 +334,7 @@ def run_ours(args, w: moe_synth.Workload):
         unit = "GB/s"
     roof_ms = max(alg["flops"] / (peaks["bf16_tflops"] * 1e12),
                   alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
-    traffic = read_traffic(w.name)
+    traffic = read_traffic(w.name, alg["touched"])
     out = {
         "metric": METRIC,
         "value": world * T / (ms / 1e3),
@@ -375,9 +375,12 @@ def run_ours(args, w: moe_synth.Workload):
     return out
 
 
-def read_traffic(workload: str):
+def read_traffic(workload: str, units: int):
     """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it still
-    describes the current kernel source (else null)."""
+    describes the current kernel source (else null). The summary gives bytes per unit
+    (touched expert matrix) measured on a scaled case; a launch moves `units` of them."""
+    if "[" in workload:          # scaled cases have no committed counters
+        return None
     path = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}.md")
     try:
         with open(path) as f:
@@ -386,13 +389,13 @@ def read_traffic(workload: str):
         return None
     vals = {}
     for line in txt.splitlines():
-        if line.startswith("traffic_bytes_per_launch:"):
+        if line.startswith("traffic_bytes_per_unit:"):
             vals["t"] = float(line.split(":", 1)[1])
         if line.startswith("kernel_source_sha256:"):
             vals["h"] = line.split(":", 1)[1].strip()
     if "t" not in vals or vals.get("h") != kernel_source_hash():
         return None
-    return vals["t"]
+    return vals["t"] * units
 
 
 def kernel_source_hash() -> str:
@@ -500,10 +503,21 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="nano_decode",
                     choices=[k for k, v in moe_synth.WORKLOADS.items() if not v.nvfp4])
+    ap.add_argument("--T", type=int, default=None,
+                    help="override the token count (a scaled case, e.g. for profiling)")
+    ap.add_argument("--E", type=int, default=None,
+                    help="override the expert count of a standard layer (scaled case)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = moe_synth.WORKLOADS[args.workload]
+    if args.T is not None or args.E is not None:
+        import dataclasses
+        if w.latent and args.E is not None:
+            ap.error("--E applies to the standard layer only")
+        T = args.T if args.T is not None else w.T
+        E = args.E if args.E is not None else w.E
+        w = dataclasses.replace(w, T=T, E=E, name=f"{w.name}[T={T},E={E}]")
     if args.steps is None:
         # enough steps for about two seconds of timed work (clock samples land inside it)
         args.steps = {"nano_decode": 2000, "tiny": 2000}.get(w.name, 500) \
