@@ -373,3 +373,38 @@ def moe_tokens_nvfp4(x_all, x_rows, idx_rows, gates_rows, w_up, w_down, h_amax=N
         hq = nvfp4_dequantize(h.astype(np.float32), gh)
         out[i] += float(gates_rows[i][j]) * (hq @ wd_cache[e].T)[0]
     return out
+
+
+def grouped_ffn_nvfp4(x_perm, offsets, w_up, w_down) -> np.ndarray:
+    """The expert FFNs with NVFP4 operands ([N3] §2.4).
+
+    Each expert matrix is quantised with its own global scale. The permuted activations are
+    quantised with one global scale over the whole x_perm tensor, and the hidden activations
+    with one over the whole h tensor (all experts). Products and sums are exact in fp64 on
+    the dequantised values.
+    """
+    xp = _f64(x_perm).astype(np.float32)
+    E = len(offsets) - 1
+    xq = nvfp4_dequantize(xp)
+    hs = {}
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            hs[e] = np.maximum(xq[a:b] @ nvfp4_dequantize(w_up[e]).T, 0.0) ** 2
+    h_amax = max((float(np.max(np.abs(h))) for h in hs.values()), default=0.0)
+    gh = nvfp4_global_scale(np.float32(h_amax))
+    out = np.zeros((xp.shape[0], np.asarray(w_down).shape[1]))
+    for e, h in hs.items():
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        out[a:b] = nvfp4_dequantize(h.astype(np.float32), gh) @ nvfp4_dequantize(w_down[e]).T
+    return out
+
+
+def moe_layer_nvfp4(x, w_router, bias, w_up, w_down, k: int) -> dict:
+    """Routed MoE layer with NVFP4 experts: bf16 routing, NVFP4 expert FFNs, fp64 combine."""
+    r = route(x, w_router, bias, k)
+    E = np.asarray(w_router).shape[0]
+    p = permute(r["idx"], E)
+    y_perm = grouped_ffn_nvfp4(gather_rows(x, p["row_token"]), p["offsets"], w_up, w_down)
+    T = np.asarray(x).shape[0]
+    return {"y": combine(y_perm, p["slot_row"], r["gates"], T, k), **r, **p}

@@ -310,11 +310,80 @@ def check_nvfp4_bounds(o):
     np.testing.assert_array_equal(q2["deq"], blk.astype(np.float64))
 
 
+def _nearest_even(v, table_vals, table_codes):
+    """Brute-force round-to-nearest over a decoded value table, ties to the even code."""
+    d = np.abs(np.asarray(table_vals) - v)
+    best = d.min()
+    cands = [i for i in range(len(d)) if d[i] == best]
+    if len(cands) > 1:
+        cands = [i for i in cands if table_codes[i] % 2 == 0]
+    return table_vals[cands[0]]
+
+
+def _brute_nvfp4(mat, g):
+    """NVFP4 quantise-dequantise by table search (no rint-based rounding)."""
+    e2 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    e4_vals, e4_codes = [], []
+    for code in range(127):            # non-negative finite E4M3 values (0x7F is NaN)
+        ex, m = code >> 3, code & 7
+        e4_vals.append(m * 2.0 ** -9 if ex == 0 else (1 + m / 8) * 2.0 ** (ex - 7))
+        e4_codes.append(code)
+    a = np.asarray(mat, np.float32)
+    out = np.zeros(a.shape)
+    g = np.float32(g)
+    for r in range(a.shape[0]):
+        for b in range(a.shape[1] // 16):
+            blk = a[r, 16 * b:16 * b + 16]
+            ratio = np.float32(np.max(np.abs(blk)) / np.float32(np.float32(6) * g))
+            sb = min(_nearest_even(float(ratio), e4_vals, e4_codes), 448.0) if g > 0 else 0.0
+            den = np.float32(np.float32(sb) * g)
+            for i in range(16):
+                if den > 0:
+                    s = float(np.float32(blk[i] / den))
+                    q = 6.0 if abs(s) > 6 else _nearest_even(abs(s), e2, list(range(8)))
+                    out[r, 16 * b + i] = np.copysign(q, s) * float(den)
+    return out
+
+
+def check_nvfp4_brute_force(o):
+    rng = np.random.default_rng(21)
+    a = (rng.standard_normal((5, 64)) * np.exp(rng.uniform(-6, 3, (5, 1)))).astype(np.float32)
+    g = o.nvfp4_global_scale(np.max(np.abs(a)))
+    np.testing.assert_array_equal(o.nvfp4_quantize(a)["deq"], _brute_nvfp4(a, g))
+
+
+def check_grouped_ffn_nvfp4(o):
+    """NVFP4 expert FFNs by brute force: table-search quantiser, scalar-loop products."""
+    rng = np.random.default_rng(22)
+    E, D, F = 2, 32, 16
+    x = rng.standard_normal((5, D)).astype(np.float32)
+    offsets = np.array([0, 2, 5])
+    wu = rng.standard_normal((E, F, D)).astype(np.float32)
+    wd = rng.standard_normal((E, D, F)).astype(np.float32)
+    got = o.grouped_ffn_nvfp4(x, offsets, wu, wd)
+    xq = _brute_nvfp4(x, o.nvfp4_global_scale(np.max(np.abs(x))))
+    hs = []
+    for e in range(E):
+        wq = _brute_nvfp4(wu[e], o.nvfp4_global_scale(np.max(np.abs(wu[e]))))
+        for r in range(offsets[e], offsets[e + 1]):
+            hs.append([max(math.fsum(xq[r, i] * wq[f, i] for i in range(D)), 0.0) ** 2
+                       for f in range(F)])
+    hs = np.array(hs)
+    hq = _brute_nvfp4(hs, o.nvfp4_global_scale(np.float32(np.max(np.abs(hs)))))
+    ref = np.zeros((5, D))
+    for e in range(E):
+        wq = _brute_nvfp4(wd[e], o.nvfp4_global_scale(np.max(np.abs(wd[e]))))
+        for r in range(offsets[e], offsets[e + 1]):
+            ref[r] = [math.fsum(hq[r, f] * wq[i, f] for f in range(F)) for i in range(D)]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = [check_route_closed_form, check_topk_brute_force, check_layer_brute_force,
               check_ffn_closed_form, check_single_expert_is_dense_ffn, check_identical_experts,
               check_k_equals_E, check_forced_expert, check_gate_and_count_invariants,
               check_latent_identity, check_latent_brute_force, check_combine_weights,
-              check_e2m1_table, check_e4m3_table, check_nvfp4_block, check_nvfp4_bounds]
+              check_e2m1_table, check_e4m3_table, check_nvfp4_block, check_nvfp4_bounds,
+              check_nvfp4_brute_force, check_grouped_ffn_nvfp4]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
