@@ -185,6 +185,63 @@ int latent_moe(const uint16_t* x, const uint16_t* w_in, const uint16_t* w_out,
                int32_t* topk_idx_out, float* gates_out,
                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * NVFP4 expert FFNs (NVIDIA Nemotron 3 notes §2.4: E2M1 elements in 16-element micro-blocks,
+ * an E4M3 scale per block, a second-level FP32 scale per tensor). For a tensor with
+ * amax A the global scale is g = A / (6 * 448); each block of 16 consecutive K elements gets
+ * sb = E4M3(amax(block) / (6 g)) and each element q = E2M1(v / (sb g)), both rounded to
+ * nearest with ties to even and saturating; the value is q * sb * g. Decisions are taken in
+ * fp32 with correctly rounded division. Routing, dispatch and the combine stay bf16/fp32.
+ *
+ * NVFP4 matrix formats used by these calls, for G matrices of [N, K] (K a multiple of 64):
+ *  - codes  [G, N, K/2] bytes: E2M1 codes (sign in bit 3), element 2i in the low nibble.
+ *  - scales E4M3 bytes in the tensor cores' tile order: per matrix, one 512-byte atom per
+ *    (128-row block rb, 64-element K step j), atoms ordered by rb then j
+ *    (ceil(N/128) * K/64 atoms per matrix); inside an atom, row 128 rb + 32 r1 + r0 and
+ *    K block kb (0..3 within the step) sit at byte r0 * 16 + r1 * 4 + kb. Rows past N in
+ *    the last block hold zero scales.
+ *  - global_scale [G] fp32: g of each matrix (each expert matrix is its own tensor).
+ * ------------------------------------------------------------------------------------- */
+size_t moe_nvfp4_codes_bytes(int G, int N, int K);
+size_t moe_nvfp4_scales_bytes(int G, int N, int K);
+
+/* moe_quantize_nvfp4_weights: quantise G bf16 weight matrices w [G, N, K] into the formats
+ * above (a set-up step, done once per weight set). K must be a multiple of 64; w, codes
+ * and scales 16-byte aligned; G <= 1024. (The NVFP4 FFN calls need N a multiple of 64.) No workspace: global_scale doubles as the
+ * per-matrix amax accumulator. Asynchronous on `stream`. */
+int moe_quantize_nvfp4_weights(const uint16_t* w, int G, int N, int K, uint8_t* codes,
+                               uint8_t* scales, float* global_scale, cudaStream_t stream);
+
+/* moe_grouped_ffn_nvfp4: moe_grouped_ffn with NVFP4 operands.
+ *   x_perm rows are quantised in the call with one global scale over the whole x_perm
+ *   tensor; h = max(0, x_q . w_up_q[e]^T)^2 (fp32 accumulation, then bf16) is quantised with
+ *   one global scale over all of h; y_perm = h_q . w_down_q[e]^T, stored bf16.
+ * Each expert's row segment is padded internally to whole 128-row tiles (at most 127 extra
+ * rows per expert). Layout: x_perm [rows, H] bf16, offsets [E+1] int32, y_perm [rows, H] bf16;
+ * up weights quantised from [E, F, H], down weights from [E, H, F].
+ * Workspace: moe_grouped_ffn_nvfp4_workspace_size(). */
+size_t moe_grouped_ffn_nvfp4_workspace_size(int rows, int H, int F, int E);
+int moe_grouped_ffn_nvfp4(const uint16_t* x_perm, const int32_t* offsets,
+                          const uint8_t* up_codes, const uint8_t* up_scales,
+                          const float* up_gscale, const uint8_t* down_codes,
+                          const uint8_t* down_scales, const float* down_gscale, int rows, int H,
+                          int F, int E, uint16_t* y_perm, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/* moe_forward_nvfp4: the routed MoE layer with NVFP4 expert FFNs: moe_route (bf16 inputs,
+ * fp32 scores), the permutation, moe_grouped_ffn_nvfp4 on the routed tokens (the tokens are
+ * quantised straight from x, with the global scale of the whole x, and gathered into the
+ * padded expert order in one pass; no bf16 x_perm is written) and moe_combine.
+ * Layout: as moe_forward, with the NVFP4 weights above. Workspace:
+ * moe_forward_nvfp4_workspace_size(). */
+size_t moe_forward_nvfp4_workspace_size(int T, int H, int E, int k, int F);
+int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                      const uint8_t* up_codes, const uint8_t* up_scales, const float* up_gscale,
+                      const uint8_t* down_codes, const uint8_t* down_scales,
+                      const float* down_gscale, int T, int H, int E, int k, int F, uint16_t* y,
+                      int32_t* topk_idx_out, float* gates_out, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

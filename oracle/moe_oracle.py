@@ -358,10 +358,13 @@ def moe_tokens_nvfp4(x_all, x_rows, idx_rows, gates_rows, w_up, w_down, h_amax=N
     n, k = np.asarray(idx_rows).shape
     out = np.zeros((n, np.asarray(w_down).shape[1]))
     hs = []
+    wu_cache: dict[int, np.ndarray] = {}
     for i in range(n):
         for j in range(k):
             e = int(idx_rows[i][j])
-            a = xr[i:i + 1] @ nvfp4_dequantize(w_up[e]).T
+            if e not in wu_cache:
+                wu_cache[e] = nvfp4_dequantize(w_up[e])
+            a = xr[i:i + 1] @ wu_cache[e].T
             hs.append((i, j, e, np.maximum(a, 0.0) ** 2))
     if h_amax is None:
         h_amax = max(float(np.max(np.abs(h[3]))) for h in hs) if hs else 0.0
@@ -373,6 +376,21 @@ def moe_tokens_nvfp4(x_all, x_rows, idx_rows, gates_rows, w_up, w_down, h_amax=N
         hq = nvfp4_dequantize(h.astype(np.float32), gh)
         out[i] += float(gates_rows[i][j]) * (hq @ wd_cache[e].T)[0]
     return out
+
+
+def nvfp4_hidden_amax(x, idx, w_up) -> float:
+    """amax of the hidden activations h over every routed (token, expert) pair, with the
+    tokens and the up-projection weights in NVFP4 as in grouped_ffn_nvfp4. This is the
+    tensor-wide amax that sets the global scale of h; moe_tokens_nvfp4 takes it as h_amax
+    when only a sample of tokens is evaluated."""
+    xq = nvfp4_dequantize(_f64(x).astype(np.float32))
+    idx = np.asarray(idx)
+    amax = 0.0
+    for e in np.unique(idx):
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        a = xq[toks] @ nvfp4_dequantize(w_up[int(e)]).T
+        amax = max(amax, float(np.max(np.maximum(a, 0.0) ** 2)))
+    return amax
 
 
 def grouped_ffn_nvfp4(x_perm, offsets, w_up, w_down) -> np.ndarray:

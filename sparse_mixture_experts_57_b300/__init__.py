@@ -6,6 +6,7 @@ thin Python binding of its C ABI (include/moe.h). Torch supplies device memory a
 """
 from ._binding import (  # noqa: F401
     MoeError,
+    Nvfp4Weights,
     SIGNATURES,
     get_device_status,
     latent_moe,
@@ -13,10 +14,14 @@ from ._binding import (  # noqa: F401
     lib,
     moe_combine,
     moe_forward,
+    moe_forward_nvfp4,
+    moe_forward_nvfp4_workspace_size,
     moe_forward_workspace_size,
     moe_grouped_ffn,
+    moe_grouped_ffn_nvfp4,
     moe_linear,
     moe_permute,
+    moe_quantize_nvfp4_weights,
     moe_route,
     status_string,
 )

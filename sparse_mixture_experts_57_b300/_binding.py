@@ -36,6 +36,15 @@ SIGNATURES = {
     "moe_forward_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ,
                          _VP]),
+    "moe_nvfp4_codes_bytes": (_SZ, [_I, _I, _I]),
+    "moe_nvfp4_scales_bytes": (_SZ, [_I, _I, _I]),
+    "moe_quantize_nvfp4_weights": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _VP]),
+    "moe_grouped_ffn_nvfp4_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "moe_grouped_ffn_nvfp4": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP,
+                                   _VP, _SZ, _VP]),
+    "moe_forward_nvfp4_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward_nvfp4": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
+                               _VP, _VP, _VP, _VP, _SZ, _VP]),
     "latent_moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "latent_moe": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP,
                         _VP, _VP, _SZ, _VP]),
@@ -233,4 +242,77 @@ def latent_moe(x, w_in, w_out, w_router, bias, w_up, w_down, kp: int, *,
                         int(router_on_latent), _ptr(w_up), _ptr(w_down), T, H, Lat, Ep, kp, F,
                         _ptr(y), _ptr(topk_idx_out), _ptr(gates_out), _ptr(ws), ws.numel(),
                         _stream(stream)), "latent_moe")
+    return y
+
+
+# ------------------------------------------------------------------------------ NVFP4 ----
+
+class Nvfp4Weights:
+    """G expert matrices [N, K] quantised to NVFP4 on the device (formats of include/moe.h):
+    codes [G, N, K/2] uint8, scales (tile-ordered E4M3 atoms) uint8, gscale [G] fp32."""
+
+    def __init__(self, codes, scales, gscale, G, N, K):
+        self.codes, self.scales, self.gscale = codes, scales, gscale
+        self.G, self.N, self.K = G, N, K
+
+    def ptrs(self):
+        return _ptr(self.codes), _ptr(self.scales), _ptr(self.gscale)
+
+
+def moe_quantize_nvfp4_weights(w, *, stream=None) -> Nvfp4Weights:
+    _cuda_tensor(w, torch.bfloat16, "w", 3)
+    G, N, K = w.shape
+    L = lib()
+    nc, ns = int(L.moe_nvfp4_codes_bytes(G, N, K)), int(L.moe_nvfp4_scales_bytes(G, N, K))
+    if nc == 0 or ns == 0:
+        raise MoeError(1, "moe_quantize_nvfp4_weights")
+    codes = torch.empty((G, N, K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((ns,), dtype=torch.uint8, device=w.device)
+    gscale = torch.empty((G,), dtype=torch.float32, device=w.device)
+    _check(L.moe_quantize_nvfp4_weights(_ptr(w), G, N, K, _ptr(codes), _ptr(scales),
+                                        _ptr(gscale), _stream(stream)),
+           "moe_quantize_nvfp4_weights")
+    return Nvfp4Weights(codes, scales, gscale, G, N, K)
+
+
+def moe_grouped_ffn_nvfp4(x_perm, offsets, w_up: Nvfp4Weights, w_down: Nvfp4Weights, *,
+                          out=None, workspace=None, stream=None):
+    _cuda_tensor(x_perm, torch.bfloat16, "x_perm", 2)
+    _cuda_tensor(offsets, torch.int32, "offsets", 1)
+    rows, H = x_perm.shape
+    E, F = w_up.G, w_up.N
+    if (w_up.K, w_down.G, w_down.N, w_down.K) != (H, E, H, F):
+        raise ValueError("NVFP4 weight shapes do not match x_perm")
+    y = out if out is not None else torch.empty((rows, H), dtype=torch.bfloat16,
+                                                device=x_perm.device)
+    L = lib()
+    ws = _workspace(L.moe_grouped_ffn_nvfp4_workspace_size(rows, H, F, E), x_perm.device,
+                    workspace)
+    _check(L.moe_grouped_ffn_nvfp4(_ptr(x_perm), _ptr(offsets), *w_up.ptrs(), *w_down.ptrs(),
+                                   rows, H, F, E, _ptr(y), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "moe_grouped_ffn_nvfp4")
+    return y
+
+
+def moe_forward_nvfp4_workspace_size(T, H, E, k, F) -> int:
+    return int(lib().moe_forward_nvfp4_workspace_size(T, H, E, k, F))
+
+
+def moe_forward_nvfp4(x, w_router, bias, w_up: Nvfp4Weights, w_down: Nvfp4Weights, k: int, *,
+                      out=None, topk_idx_out=None, gates_out=None, workspace=None, stream=None):
+    bf = torch.bfloat16
+    _cuda_tensor(x, bf, "x", 2)
+    _cuda_tensor(w_router, bf, "w_router", 2)
+    _cuda_tensor(bias, torch.float32, "bias", 1)
+    T, H = x.shape
+    E, F = w_up.G, w_up.N
+    if (w_up.K, w_down.G, w_down.N, w_down.K) != (H, E, H, F):
+        raise ValueError("NVFP4 weight shapes do not match x")
+    y = out if out is not None else torch.empty((T, H), dtype=bf, device=x.device)
+    L = lib()
+    ws = _workspace(L.moe_forward_nvfp4_workspace_size(T, H, E, k, F), x.device, workspace)
+    _check(L.moe_forward_nvfp4(_ptr(x), _ptr(w_router), _ptr(bias), *w_up.ptrs(),
+                               *w_down.ptrs(), T, H, E, k, F, _ptr(y), _ptr(topk_idx_out),
+                               _ptr(gates_out), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_forward_nvfp4")
     return y

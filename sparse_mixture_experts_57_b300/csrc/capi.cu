@@ -171,6 +171,105 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
   return launch_combine(w.y_perm, rows, w.slot_row, gates, T, D, k, y, s);
 }
 
+// NVFP4 expert FFN buffers. P bounds the padded rows: every group rounded up to whole
+// 128-row tiles adds at most 127 rows.
+struct Fp4Ws {
+  int P;
+  int32_t* poff;
+  uint32_t* amax;  // [0] activations entering the up-projection, [1] hidden activations
+  uint8_t* xq;
+  uint8_t* xsf;
+  uint16_t* h;
+  uint8_t* hq;
+  uint8_t* hsf;
+};
+
+int fp4_rows_bound(int rows, int E) {
+  const long long p = static_cast<long long>(rows) + 127LL * E;
+  return static_cast<int>(align_up(static_cast<size_t>(p), 128));
+}
+
+Fp4Ws carve_fp4(Carver& c, int rows, int H, int F, int E) {
+  Fp4Ws w;
+  w.P = fp4_rows_bound(rows, E);
+  const size_t P = static_cast<size_t>(w.P);
+  w.poff = c.take<int32_t>(E + 1);
+  w.amax = c.take<uint32_t>(2);
+  w.xq = c.take<uint8_t>(P * H / 2);
+  w.xsf = c.take<uint8_t>(nvfp4_sf_bytes(w.P, H));
+  w.h = c.take<uint16_t>(P * F);
+  w.hq = c.take<uint8_t>(P * F / 2);
+  w.hsf = c.take<uint8_t>(nvfp4_sf_bytes(w.P, F));
+  return w;
+}
+
+struct Nvfp4Weights {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* gscale;
+};
+
+// NVFP4 expert FFNs. The rows entering the experts are gathered from `src` (row stride ld):
+// token row_token[offsets[e] + r] when row_token is given, else row offsets[e] + r. amax_rows
+// rows of src make up the activation tensor whose amax sets its global scale.
+int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const int32_t* row_token,
+              const int32_t* offsets, const Nvfp4Weights& up, const Nvfp4Weights& down, int rows,
+              int H, int F, int E, uint16_t* y_perm, const Fp4Ws& w, cudaStream_t s) {
+  MOE_CUDA(cudaMemsetAsync(w.amax, 0, 2 * sizeof(uint32_t), s));
+  int st = launch_amax_bf16(src, amax_rows * ld, 1, w.amax, s);
+  if (st) return st;
+  st = launch_pad_offsets(offsets, E, w.poff, s);
+  if (st) return st;
+  st = launch_quant_act(src, ld, amax_rows, row_token, offsets, w.poff, E, H, w.P, w.amax, w.xq,
+                        w.xsf, s);
+  if (st) return st;
+  Fp4Gemm g{};
+  g.a_codes = w.xq;
+  g.a_sf = w.xsf;
+  g.a_amax = w.amax;
+  g.P = w.P;
+  g.poff = w.poff;
+  g.w_codes = up.codes;
+  g.w_sf = up.scales;
+  g.w_gscale = up.gscale;
+  g.E = E;
+  g.N = F;
+  g.K = H;
+  g.out_off = nullptr;
+  g.out_rows = w.P;
+  g.out = w.h;
+  g.ldo = F;
+  g.epi = EPI_SQRELU_BF16;
+  g.out_amax = w.amax + 1;
+  st = launch_fp4_gemm(g, s);
+  if (st) return st;
+  st = launch_quant_act(w.h, F, w.P, nullptr, nullptr, w.poff, E, F, w.P, w.amax + 1, w.hq,
+                        w.hsf, s);
+  if (st) return st;
+  Fp4Gemm d{};
+  d.a_codes = w.hq;
+  d.a_sf = w.hsf;
+  d.a_amax = w.amax + 1;
+  d.P = w.P;
+  d.poff = w.poff;
+  d.w_codes = down.codes;
+  d.w_sf = down.scales;
+  d.w_gscale = down.gscale;
+  d.E = E;
+  d.N = H;
+  d.K = F;
+  d.out_off = offsets;
+  d.out_rows = rows;
+  d.out = y_perm;
+  d.ldo = H;
+  d.epi = EPI_BF16;
+  return launch_fp4_gemm(d, s);
+}
+
+bool nvfp4_weights_ok(const uint8_t* codes, const uint8_t* scales, const float* g) {
+  return codes && scales && g && aligned16(codes) && aligned16(scales);
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -391,6 +490,124 @@ int latent_moe(const uint16_t* x, const uint16_t* w_in, const uint16_t* w_out,
   o.ldo = H;
   o.epi = EPI_BF16;
   return launch_grouped_gemm(o, stream);
+}
+
+size_t moe_nvfp4_codes_bytes(int G, int N, int K) {
+  if (G < 1 || N < 1 || K < 64 || K % 64) return 0;
+  return static_cast<size_t>(G) * N * (K / 2);
+}
+
+size_t moe_nvfp4_scales_bytes(int G, int N, int K) {
+  if (G < 1 || N < 1 || K < 64 || K % 64) return 0;
+  return static_cast<size_t>(G) * nvfp4_sf_bytes(N, K);
+}
+
+int moe_quantize_nvfp4_weights(const uint16_t* w, int G, int N, int K, uint8_t* codes,
+                               uint8_t* scales, float* global_scale, cudaStream_t stream) {
+  if (G < 1 || G > 1024 || N < 1 || K < 64) return MOE_ERR_INVALID_ARG;
+  if (!w || !codes || !scales || !global_scale) return MOE_ERR_INVALID_ARG;
+  if (K % 64 || !aligned16(w) || !aligned16(codes) || !aligned16(scales))
+    return MOE_ERR_UNSUPPORTED;
+  // global_scale first accumulates each matrix's amax (as fp32 bits), then holds amax / 2688.
+  MOE_CUDA(cudaMemsetAsync(global_scale, 0, sizeof(float) * G, stream));
+  uint32_t* amax = reinterpret_cast<uint32_t*>(global_scale);
+  int st = launch_amax_bf16(w, static_cast<long long>(N) * K, G, amax, stream);
+  if (st) return st;
+  st = launch_quant_weights(w, G, N, K, amax, codes, scales, stream);
+  if (st) return st;
+  return launch_finalize_gscale(global_scale, G, stream);
+}
+
+size_t moe_grouped_ffn_nvfp4_workspace_size(int rows, int H, int F, int E) {
+  if (rows < 0 || H <= 0 || F <= 0 || E < 1 || E > 1024) return 0;
+  Carver c(nullptr, 0);
+  carve_fp4(c, rows, H, F, E);
+  return c.used + 256;
+}
+
+int moe_grouped_ffn_nvfp4(const uint16_t* x_perm, const int32_t* offsets,
+                          const uint8_t* up_codes, const uint8_t* up_scales,
+                          const float* up_gscale, const uint8_t* down_codes,
+                          const uint8_t* down_scales, const float* down_gscale, int rows, int H,
+                          int F, int E, uint16_t* y_perm, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  if (rows < 0 || H <= 0 || F <= 0 || E < 1 || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(rows) + 127LL * E + 127 > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x_perm || !offsets || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!nvfp4_weights_ok(up_codes, up_scales, up_gscale) ||
+      !nvfp4_weights_ok(down_codes, down_scales, down_gscale))
+    return MOE_ERR_INVALID_ARG;
+  if (H % 64 || F % 64 || !aligned16(x_perm) || !aligned16(y_perm)) return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  const Fp4Ws w = carve_fp4(c, rows, H, F, E);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  return ffn_nvfp4(x_perm, H, rows, nullptr, offsets, {up_codes, up_scales, up_gscale},
+                   {down_codes, down_scales, down_gscale}, rows, H, F, E, y_perm, w, stream);
+}
+
+size_t moe_forward_nvfp4_workspace_size(int T, int H, int E, int k, int F) {
+  if (!dims_ok(T, H, E, k) || F <= 0) return 0;
+  Carver c(nullptr, 0);
+  const size_t rows = static_cast<size_t>(T) * k;
+  c.take<float>(static_cast<size_t>(T) * E);                     // logits
+  c.take<int32_t>(rows);                                        // idx
+  c.take<float>(rows);                                          // gates
+  c.take<uint8_t>(T > 0 ? T : 1);                               // tie
+  c.take<int32_t>(E);                                           // counts
+  c.take<int32_t>(E + 1);                                       // offsets
+  c.take<int32_t>(rows);                                        // row_token
+  c.take<int32_t>(rows);                                        // slot_row
+  c.take<char>(permute_scratch_bytes(T, E));
+  c.take<uint16_t>(rows * H);                                   // y_perm
+  carve_fp4(c, static_cast<int>(rows), H, F, E);
+  return c.used + 256;
+}
+
+int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                      const uint8_t* up_codes, const uint8_t* up_scales, const float* up_gscale,
+                      const uint8_t* down_codes, const uint8_t* down_scales,
+                      const float* down_gscale, int T, int H, int E, int k, int F, uint16_t* y,
+                      int32_t* topk_idx_out, float* gates_out, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(T, H, E, k) || F <= 0) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * k + 127LL * E + 127 > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !bias || !y) return MOE_ERR_INVALID_ARG;
+  if (!nvfp4_weights_ok(up_codes, up_scales, up_gscale) ||
+      !nvfp4_weights_ok(down_codes, down_scales, down_gscale))
+    return MOE_ERR_INVALID_ARG;
+  if (H % 64 || F % 64 || !aligned16(x) || !aligned16(w_router) || !aligned16(y))
+    return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  const size_t rows = static_cast<size_t>(T) * k;
+  float* logits = c.take<float>(static_cast<size_t>(T) * E);
+  int32_t* idx = c.take<int32_t>(rows);
+  float* gates = c.take<float>(rows);
+  uint8_t* tie = c.take<uint8_t>(T);
+  int32_t* counts = c.take<int32_t>(E);
+  int32_t* offsets = c.take<int32_t>(E + 1);
+  int32_t* row_token = c.take<int32_t>(rows);
+  int32_t* slot_row = c.take<int32_t>(rows);
+  void* perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
+  uint16_t* y_perm = c.take<uint16_t>(rows * H);
+  const Fp4Ws w = carve_fp4(c, static_cast<int>(rows), H, F, E);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  if (topk_idx_out) idx = topk_idx_out;
+  if (gates_out) gates = gates_out;
+  // routing and dispatch stay in bf16/fp32; the expert FFNs run in NVFP4
+  int st = router_logits(x, H, w_router, T, H, E, 1, logits, stream);
+  if (st) return st;
+  st = launch_topk(logits, bias, T, E, k, idx, gates, tie, stream);
+  if (st) return st;
+  st = launch_permute(idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, nullptr,
+                      perm_scratch, stream);
+  if (st) return st;
+  st = ffn_nvfp4(x, H, T, row_token, offsets, {up_codes, up_scales, up_gscale},
+                 {down_codes, down_scales, down_gscale}, static_cast<int>(rows), H, F, E, y_perm,
+                 w, stream);
+  if (st) return st;
+  return launch_combine(y_perm, static_cast<int>(rows), slot_row, gates, T, H, k, y, stream);
 }
 
 }  // extern "C"

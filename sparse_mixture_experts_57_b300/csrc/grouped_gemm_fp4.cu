@@ -1,0 +1,425 @@
+// grouped_gemm_fp4.cu: block-scaled NVFP4 grouped GEMM on tcgen05 tensor cores.
+//
+// The expert FFN contraction of the routed MoE layer ("NVIDIA Nemotron 3: Efficient and
+// Open Intelligence" notes, §2.2) with both operands in NVFP4 (§2.4: E2M1 elements, an E4M3
+// scale per 16 elements, an FP32 scale per tensor):
+//
+//   out[r, n] = epi( g_a * g_w[e] * sum_k (qa[r,k] sa[r,k/16]) (qw[e,n,k] sw[e,n,k/16]) )
+//
+// for the rows r of group e. Activation rows are laid out with every group padded to whole
+// 128-row tiles, so each row tile starts on a scale-atom boundary.
+//
+// One CTA per SM, 192 threads, as the bf16 kernel:
+//   warp 0 lane 0  TMA producer: per stage 256 K-elements (128 bytes) of 128 activation rows
+//                  and 128 weight rows (128-byte swizzle), plus the matching scale atoms
+//                  (2 KB each, untiled bulk copies).
+//   warp 1 lane 0  MMA issuer: tcgen05.cp moves the stage's scale atoms into TMEM (a ring of
+//                  scale columns tied to the smem stages), then tcgen05.mma kind::mxf4nvf4
+//                  (M=128, N=128, K=64) with block scales into a double-buffered fp32
+//                  accumulator.
+//   warps 2..5     epilogue: tcgen05.ld, global scales, squared ReLU or plain, bf16 stores.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "tc.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BKB = 128;        // K bytes per stage and row: 256 E2M1 elements
+constexpr int KSTEP = 64;       // K elements per MMA
+constexpr int STEPS_PER_STAGE = 4;
+constexpr int STAGES = 5;
+constexpr int MAXG = 1024;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t A_BYTES = BM * BKB;
+constexpr uint32_t B_BYTES = BN * BKB;
+constexpr uint32_t ATOM = 512;
+constexpr uint32_t SF_STAGE = STEPS_PER_STAGE * ATOM;  // one 128-row block, 4 K steps
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_STRIDE = BN;                     // accumulators at columns 0 and 128
+constexpr uint32_t SF_COL0 = 2 * BN;                    // then per stage 16 A + 16 B columns
+constexpr uint32_t SF_COLS_PER_STAGE = 2 * 4 * STEPS_PER_STAGE;
+static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+constexpr uint32_t IDESC = idesc_nvfp4_f32(BM, BN);
+
+struct KArgs {
+  const int* poff;
+  const int* out_off;
+  int E, N, K, P;
+  const uint8_t* a_sf;
+  const uint8_t* w_sf;
+  const uint32_t* a_amax;
+  const float* w_gscale;
+  void* out;
+  long long ldo;
+  int out_rows;
+  int epi;
+  uint32_t* out_amax;
+  int* status;
+};
+
+constexpr size_t smem_bytes() {
+  return 1024 + size_t(STAGES) * (A_BYTES + B_BYTES + 2 * SF_STAGE) + (2 * STAGES + 4) * 8 + 16 +
+         4 * (MAXG + 1) * 4;
+}
+
+__device__ __forceinline__ void record(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_fp4_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+               const KArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + STAGES * A_BYTES;
+  uint8_t* sSFA = sB + STAGES * B_BYTES;
+  uint8_t* sSFB = sSFA + STAGES * SF_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * SF_STAGE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_pref = reinterpret_cast<int*>(tmem_slot + 4);  // row-tile prefix per group
+  int* s_aoff = s_pref + (MAXG + 1);                     // padded row offset
+  int* s_ooff = s_aoff + (MAXG + 1);                     // output row offset
+  int* s_ocnt = s_ooff + (MAXG + 1);                     // rows to store
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = a.E;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  if (warp == 2) {
+    // Group table: padded segments (whole 128-row tiles) and where their outputs go.
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int local = 0;
+    bool bad = false;
+    for (int e = e0; e < e1; ++e) {
+      const int lo = a.poff[e], hi = a.poff[e + 1];
+      int tiles = (hi - lo) / BM;
+      if (lo < 0 || hi < lo || hi > a.P || ((lo | hi) & (BM - 1))) {
+        bad = true;
+        tiles = 0;
+      }
+      int olo = lo, ocnt = hi - lo;
+      if (a.out_off) {
+        olo = a.out_off[e];
+        ocnt = a.out_off[e + 1] - olo;
+        if (olo < 0 || ocnt < 0 || olo + ocnt > a.out_rows || ocnt > hi - lo) {
+          bad = true;
+          tiles = 0;
+          ocnt = 0;
+        }
+      } else if (hi > a.out_rows) {
+        bad = true;
+        tiles = 0;
+      }
+      s_aoff[e] = lo;
+      s_ooff[e] = olo;
+      s_ocnt[e] = ocnt;
+      s_pref[e] = tiles;  // temporarily the tile count
+      local += tiles;
+    }
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e1; ++e) {
+      const int t = s_pref[e];
+      s_pref[e] = run;
+      run += t;
+    }
+    if (lane == 31) s_pref[E] = incl;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record(a.status, MOE_ERR_INVALID_ARG);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_ct = (a.N + BN - 1) / BN;
+  const int total = s_pref[E] * n_ct;
+  const int KS = a.K / KSTEP;                                      // MMA steps along K
+  const int NST = (KS + STEPS_PER_STAGE - 1) / STEPS_PER_STAGE;    // pipeline stages along K
+
+  auto decode = [&](int tile, int& e, int& rt, int& ct) {
+    const int rtg = tile / n_ct;
+    ct = tile - rtg * n_ct;
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pref[mid + 1] > rtg)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    e = lo;
+    rt = rtg - s_pref[lo];
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ TMA producer
+      const uint64_t pol_w = policy_evict_last();
+      const uint64_t pol_a = policy_evict_last();
+      const int nbw = n_ct;  // weight scale row blocks per expert
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int e, rt, ct;
+        decode(tile, e, rt, ct);
+        const int row0 = s_aoff[e] + rt * BM;
+        const int col0 = ct * BN;
+        const uint8_t* sfa = a.a_sf + (static_cast<long long>(row0 / BM) * KS) * ATOM;
+        const uint8_t* sfw =
+            a.w_sf + ((static_cast<long long>(e) * nbw + ct) * KS) * ATOM;
+        for (int kb = 0; kb < NST; ++kb) {
+          const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + 2u * nsteps * ATOM);
+          tma_load_2d(sA + stage * A_BYTES, &tm_a, &full[stage], kb * BKB, row0, pol_a);
+          tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kb * BKB, col0, e, pol_w);
+          const long long so = static_cast<long long>(kb) * STEPS_PER_STAGE * ATOM;
+          bulk_load(sSFA + stage * SF_STAGE, sfa + so, nsteps * ATOM, &full[stage], pol_a);
+          bulk_load(sSFB + stage * SF_STAGE, sfw + so, nsteps * ATOM, &full[stage], pol_w);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record(a.status, MOE_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
+        for (int kb = 0; kb < NST; ++kb) {
+          const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // Scale atoms -> TMEM. The column ring is tied to the smem stages: this stage's
+          // columns were last read by MMAs that completed before its smem slot was refilled.
+          const uint32_t sfa_col = SF_COL0 + stage * SF_COLS_PER_STAGE;
+          const uint32_t sfb_col = sfa_col + 4 * STEPS_PER_STAGE;
+          for (int j = 0; j < nsteps; ++j) {
+            tmem_cp_sf_atom(tmem_base + sfa_col + 4 * j,
+                            sdesc_k_none(smem_u32(sSFA + stage * SF_STAGE + j * ATOM), 2048, 128));
+            tmem_cp_sf_atom(tmem_base + sfb_col + 4 * j,
+                            sdesc_k_none(smem_u32(sSFB + stage * SF_STAGE + j * ATOM), 2048, 128));
+          }
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(sA + stage * A_BYTES));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(sB + stage * B_BYTES));
+          for (int j = 0; j < nsteps; ++j)
+            umma_nvfp4(d_tmem, adesc + 2u * j, bdesc + 2u * j, IDESC,
+                       tmem_base + sfa_col + 4 * j, tmem_base + sfb_col + 4 * j, (kb | j) != 0);
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record(a.status, MOE_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const float ga = __fdiv_rn(__uint_as_float(*a.a_amax), kNvfp4GlobalDiv);
+    float vmax = 0.f;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, rt, ct;
+      decode(tile, e, rt, ct);
+      const int local = rt * BM + m;
+      const bool valid = local < s_ocnt[e];
+      const long long row = static_cast<long long>(s_ooff[e]) + local;
+      const int col0 = ct * BN;
+      const int ncols = min(BN, a.N - col0);
+      const float scale = ga * a.w_gscale[e];
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
+        *abort_flag = 1;
+        record(a.status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_STRIDE;
+      for (int n0 = 0; n0 < ncols; n0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tb + n0, r);
+        tmem_ld_wait();
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * scale;
+        if (a.epi == EPI_SQRELU_BF16) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float t = fmaxf(v[i], 0.f);
+            v[i] = t * t;
+          }
+        }
+        if (valid) {
+          if (a.epi == EPI_SQRELU_BF16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) vmax = fmaxf(vmax, v[i]);
+          }
+          uint32_t p[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) p[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                                row * a.ldo + col0 + n0);
+          dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+          dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (a.out_amax) {
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, d));
+      // squared ReLU outputs are >= 0: their fp32 bit patterns order like their values
+      if (lane == 0 && vmax > 0.f) atomicMax(a.out_amax, __float_as_uint(vmax));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
+  if (g.P <= 0) return MOE_OK;
+  if (g.K % KSTEP || g.N % 16 || g.E < 1 || g.E > MAXG || g.P % BM) return MOE_ERR_UNSUPPORTED;
+  if (g.epi != EPI_BF16 && g.epi != EPI_SQRELU_BF16) return MOE_ERR_UNSUPPORTED;
+  KArgs ka;
+  ka.poff = g.poff;
+  ka.out_off = g.out_off;
+  ka.E = g.E;
+  ka.N = g.N;
+  ka.K = g.K;
+  ka.P = g.P;
+  ka.a_sf = g.a_sf;
+  ka.w_sf = g.w_sf;
+  ka.a_amax = g.a_amax;
+  ka.w_gscale = g.w_gscale;
+  ka.out = g.out;
+  ka.ldo = g.ldo;
+  ka.out_rows = g.out_rows;
+  ka.epi = g.epi;
+  ka.out_amax = g.epi == EPI_SQRELU_BF16 ? g.out_amax : nullptr;
+  ka.status = status_word();
+  if (!ka.status) return MOE_ERR_CUDA;
+
+  CUtensorMap tm_a, tm_w;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(g.K / 2), static_cast<uint64_t>(g.P)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(g.K / 2)};
+    const uint32_t box[2] = {BKB, BM};
+    if (!encode_tmap(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box))
+      return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(g.K / 2), static_cast<uint64_t>(g.N),
+                              static_cast<uint64_t>(g.E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(g.K / 2),
+                                 static_cast<uint64_t>(g.N) * (g.K / 2)};
+    const uint32_t box[3] = {BKB, BN, 1};
+    if (!encode_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_codes, dims, strides, box))
+      return MOE_ERR_CUDA;
+  }
+  constexpr size_t smem = smem_bytes();
+  static_assert(smem <= 232448, "shared memory per CTA");
+  static int configured_device = -1;
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (configured_device != dev) {
+    MOE_CUDA(cudaFuncSetAttribute(k_fp4_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(smem)));
+    configured_device = dev;
+  }
+  const long long tiles = static_cast<long long>(g.P / BM) * ((g.N + BN - 1) / BN);
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  if (grid <= 0) return MOE_OK;
+  return launch_pdl(k_fp4_gemm, dim3(grid), dim3(NUM_THREADS), smem, s, tm_a, tm_w, ka);
+}
+
+}  // namespace moe

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "moe.h"
@@ -108,6 +109,63 @@ struct GroupedGemm {
   int precise;           // 1: fp32 partial sums every 256 of K (for routing inputs)
 };
 int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s);
+
+// Tiled TMA descriptor (rank 2 or 3) with 128-byte swizzle, zero fill out of bounds.
+// dims and box are innermost first; strides_bytes holds the rank - 1 outer strides.
+bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+
+// ------------------------------------------------------------------------------ NVFP4 ----
+// NVFP4 matrix [R, K]: E2M1 codes, two per byte (element 2i in bits 0-3), [R, K/2]; one
+// E4M3 scale per 16 elements of K stored as 512-byte atoms, atom (R/128 block rb, K/64
+// step j) at (rb * (K/64) + j) * 512 with row 128 rb + 32 r1 + r0, block kb at byte
+// r0 * 16 + r1 * 4 + kb; and an fp32 global scale g = amax / (6 * 448).
+constexpr float kNvfp4GlobalDiv = 2688.0f;  // 6 (E2M1 max) * 448 (E4M3 max)
+
+inline size_t nvfp4_sf_bytes(long long rows, int K) {
+  return static_cast<size_t>((rows + 127) / 128) * (K / 64) * 512;
+}
+
+// amax[g] = max |src| over matrix g (bf16 bits; amax kept as fp32 bits). amax must be zeroed.
+int launch_amax_bf16(const uint16_t* src, long long elems_per_matrix, int G, uint32_t* amax,
+                     cudaStream_t s);
+// Quantise G weight matrices [N, K] with per-matrix global scales from amax[g].
+int launch_quant_weights(const uint16_t* w, int G, int N, int K, const uint32_t* amax,
+                         uint8_t* codes, uint8_t* sf, cudaStream_t s);
+// g[i] = amax[i] / 2688 in place (amax held as fp32 bits in the same words).
+int launch_finalize_gscale(float* g, int G, cudaStream_t s);
+// poff = exclusive scan of round_up(offsets[e+1] - offsets[e], 128): expert segments padded
+// to whole 128-row tiles.
+int launch_pad_offsets(const int32_t* offsets, int E, int32_t* poff, cudaStream_t s);
+// Quantise activation rows into the padded layout. Row p of expert e (local = p - poff[e]):
+// gather mode (offsets != null): source row row_token[offsets[e] + local] (or
+// offsets[e] + local when row_token is null) if local < count[e], else a zero row;
+// identity mode (offsets == null): source row p. Global scale from *amax. A source row at or
+// past src_rows is read as zeros and reported on the status word.
+int launch_quant_act(const uint16_t* src, long long ld, long long src_rows,
+                     const int32_t* row_token, const int32_t* offsets, const int32_t* poff,
+                     int E, int K, int P_max, const uint32_t* amax, uint8_t* codes, uint8_t* sf,
+                     cudaStream_t s);
+
+struct Fp4Gemm {
+  const uint8_t* a_codes;  // [P, K/2], rows padded per group (poff)
+  const uint8_t* a_sf;     // atoms of the padded rows
+  const uint32_t* a_amax;  // activation amax (fp32 bits); g_a = amax / 2688
+  int P;                   // allocated padded rows (bound for poff[E])
+  const int32_t* poff;     // [E+1] padded group offsets (multiples of 128)
+  const uint8_t* w_codes;  // [E, N, K/2]
+  const uint8_t* w_sf;     // [E][ceil(N/128)][K/64] atoms
+  const float* w_gscale;   // [E]
+  int E, N, K;
+  const int32_t* out_off;  // [E+1] output row offsets (store only local < count), or null:
+                           // output row = padded row (every row stored)
+  int out_rows;            // rows of `out`
+  void* out;               // bf16 [out_rows, ldo]
+  long long ldo;
+  int epi;                 // EPI_SQRELU_BF16 or EPI_BF16
+  uint32_t* out_amax;      // EPI_SQRELU_BF16: max of the stored values (fp32 bits), or null
+};
+int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s);
 
 // Router pieces.
 int launch_router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_router, int T,

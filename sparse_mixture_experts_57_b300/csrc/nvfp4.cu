@@ -1,0 +1,269 @@
+// nvfp4.cu: NVFP4 quantisation of expert weights and routed activations.
+//
+// "NVIDIA Nemotron 3: Efficient and Open Intelligence" notes, §2.4: NVFP4 holds E2M1
+// elements in 16-element micro-blocks, each block with an E4M3 scale, plus a second-level
+// FP32 scale per tensor. For one tensor with global scale g = amax / (6 * 448):
+//   block scale  sb = E4M3(amax(block) / (6 g))            (nearest, ties to even, saturating)
+//   element code q  = E2M1(v / (sb g))                      (nearest, ties to the even code,
+//                                                            saturating at 6)
+//   value           = q * sb * g
+// Blocks run along the contraction axis K. Every decision is taken in fp32 with correctly
+// rounded division, so the codes and scales depend only on the input bits.
+//
+// Layouts (shared with the block-scaled grouped GEMM): codes [rows, K/2], element 2i in the
+// low nibble; scales as 512-byte atoms, one per (128-row block, 64-element K step): row
+// 128 rb + 32 r1 + r0, block kb of the step at byte r0 * 16 + r1 * 4 + kb. One thread
+// quantises one row's 64-element K step: 128 bytes in, 32 code bytes and one 32-bit word of
+// four scales out.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+#include "scan.cuh"
+
+namespace moe {
+namespace {
+
+// E2M1 code (sign in bit 3) of s rounded to the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+// a value exactly between two neighbours takes the one with the even code; |s| > 6 gives 6.
+__device__ __forceinline__ uint32_t e2m1_code(float s) {
+  const float m = fabsf(s);
+  const uint32_t c = (m > 0.25f) + (m >= 0.75f) + (m > 1.25f) + (m >= 1.75f) + (m > 2.5f) +
+                     (m >= 3.5f) + (m > 5.0f);
+  return (c != 0u && s < 0.f) ? (c | 8u) : c;
+}
+
+// Value of a non-negative E4M3 byte: exponent bias 7, 3 mantissa bits, subnormals below 2^-6.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  if (e == 0u) return static_cast<float>(m) * (1.0f / 512.0f);
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+__device__ __forceinline__ float global_scale(const uint32_t* amax) {
+  return __fdiv_rn(__uint_as_float(*amax), kNvfp4GlobalDiv);
+}
+
+// Quantise 64 consecutive bf16 values (src 16-byte aligned). Writes 32 code bytes and
+// returns the four block-scale bytes packed little-endian (block 0 in the low byte).
+__device__ __forceinline__ uint32_t quant64(const uint4* __restrict__ src, float g, uint4* dst) {
+  uint32_t sf = 0u;
+  uint32_t q[8];
+  const float six_g = __fmul_rn(6.0f, g);
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk) {
+    const uint4 a = __ldg(src + 2 * blk), b = __ldg(src + 2 * blk + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+    float bmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+    uint32_t sb = 0u;
+    float denom = 0.f;
+    if (g > 0.f) {
+      sb = static_cast<uint32_t>(
+          __nv_cvt_float_to_fp8(__fdiv_rn(bmax, six_g), __NV_SATFINITE, __NV_E4M3));
+      denom = __fmul_rn(e4m3_value(sb), g);
+    }
+    q[2 * blk] = 0u;
+    q[2 * blk + 1] = 0u;
+    if (denom > 0.f) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        q[2 * blk + (i >> 3)] |= e2m1_code(__fdiv_rn(v[i], denom)) << (4 * (i & 7));
+    }
+    sf |= sb << (8 * blk);
+  }
+  dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+  dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  return sf;
+}
+
+__device__ __forceinline__ uint32_t* sf_word(uint8_t* sf, long long row, int j, int KS) {
+  const long long rb = row >> 7;
+  const int r = static_cast<int>(row & 127);
+  return reinterpret_cast<uint32_t*>(sf + (rb * KS + j) * 512 + (r & 31) * 16 + (r >> 5) * 4);
+}
+
+__global__ void k_amax_bf16(const uint16_t* __restrict__ src, long long per_matrix,
+                            uint32_t* __restrict__ amax) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int g = blockIdx.y;
+  const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<long long>(g) * per_matrix);
+  const long long nvec = per_matrix / 8;
+  uint32_t m = 0u;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(p + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      m = max(m, w[k] & 0x7fffu);
+      m = max(m, (w[k] >> 16) & 0x7fffu);
+    }
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+  // |bf16| bit patterns order like their values; as fp32 bits they keep that order.
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(amax + g, m << 16);
+}
+
+__global__ void k_quant_weights(const uint16_t* __restrict__ w, int G, int N, int K,
+                                const uint32_t* __restrict__ amax, uint8_t* __restrict__ codes,
+                                uint8_t* __restrict__ sf) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int KS = K / 64;
+  const long long rows_pad = static_cast<long long>((N + 127) / 128) * 128;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= G * rows_pad * KS) return;
+  const long long ar = i / KS;  // row in the padded stack of G matrices
+  const int j = static_cast<int>(i - ar * KS);
+  const int g = static_cast<int>(ar / rows_pad);
+  const int n = static_cast<int>(ar - g * rows_pad);
+  uint32_t* word = sf_word(sf, ar, j, KS);
+  if (n >= N) {  // rows past N in the last 128-row block: zero scales
+    *word = 0u;
+    return;
+  }
+  const long long row = static_cast<long long>(g) * N + n;
+  uint4 out[2];
+  *word = quant64(reinterpret_cast<const uint4*>(w + row * K + j * 64), global_scale(amax + g),
+                  out);
+  uint4* dst = reinterpret_cast<uint4*>(codes + row * (K / 2) + j * 32);
+  dst[0] = out[0];
+  dst[1] = out[1];
+}
+
+__global__ void k_finalize_gscale(float* g, int G) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < G) g[i] = __fdiv_rn(g[i], kNvfp4GlobalDiv);  // g[i] holds amax as fp32 bits
+}
+
+__global__ void k_pad_offsets(const int32_t* __restrict__ offsets, int E,
+                              int32_t* __restrict__ poff, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int warp_sums[33];
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E) {
+    c = offsets[e + 1] - offsets[e];
+    if (c < 0) {
+      atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+      c = 0;
+    }
+    c = (c + 127) & ~127;
+  }
+  int total;
+  const int excl = block_exclusive_scan(c, warp_sums, &total);
+  if (e < E) poff[e] = excl;
+  if (e == 0) poff[E] = total;
+}
+
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads)
+    k_quant_act(const uint16_t* __restrict__ src, long long ld, long long src_rows,
+                const int32_t* __restrict__ row_token, const int32_t* __restrict__ offsets,
+                const int32_t* __restrict__ poff, int E, int K, int P_max,
+                const uint32_t* __restrict__ amax, uint8_t* __restrict__ codes,
+                uint8_t* __restrict__ sf, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ int s_poff[];
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_poff[i] = poff[i];
+  __syncthreads();
+  const int KS = K / 64;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long p = i / KS;
+  const int j = static_cast<int>(i - p * KS);
+  if (p >= s_poff[E] || p >= P_max) return;
+  long long srow = p;
+  if (offsets) {
+    int lo = 0, hi = E - 1;  // expert e with s_poff[e] <= p < s_poff[e+1]
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_poff[mid + 1] > p)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    const int local = static_cast<int>(p - s_poff[lo]);
+    const int base = offsets[lo];
+    srow = local < offsets[lo + 1] - base ? (row_token ? row_token[base + local] : base + local)
+                                          : -1;
+  }
+  if (srow >= src_rows) {  // offsets or row_token outside the source tensor
+    if (j == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+    srow = -1;
+  }
+  uint32_t* word = sf_word(sf, p, j, KS);
+  uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + j * 32);
+  if (srow < 0) {  // padding row of a segment
+    *word = 0u;
+    dst[0] = make_uint4(0u, 0u, 0u, 0u);
+    dst[1] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  uint4 out[2];
+  *word = quant64(reinterpret_cast<const uint4*>(src + srow * ld + j * 64), global_scale(amax),
+                  out);
+  dst[0] = out[0];
+  dst[1] = out[1];
+}
+
+}  // namespace
+
+int launch_amax_bf16(const uint16_t* src, long long elems_per_matrix, int G, uint32_t* amax,
+                     cudaStream_t s) {
+  if (G <= 0 || elems_per_matrix <= 0) return MOE_OK;
+  const long long nvec = elems_per_matrix / 8;
+  long long blocks = (nvec + 255) / 256;
+  const long long cap = 4LL * sm_count();  // with grid.y matrices, enough to fill the GPU
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(k_amax_bf16, dim3(static_cast<unsigned>(blocks), G), dim3(256), 0, s, src,
+                    elems_per_matrix, amax);
+}
+
+int launch_quant_weights(const uint16_t* w, int G, int N, int K, const uint32_t* amax,
+                         uint8_t* codes, uint8_t* sf, cudaStream_t s) {
+  const long long n = static_cast<long long>(G) * ((N + 127) / 128) * 128 * (K / 64);
+  if (n <= 0) return MOE_OK;
+  return launch_pdl(k_quant_weights, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
+                    s, w, G, N, K, amax, codes, sf);
+}
+
+int launch_finalize_gscale(float* g, int G, cudaStream_t s) {
+  return launch_pdl(k_finalize_gscale, dim3((G + 255) / 256), dim3(256), 0, s, g, G);
+}
+
+int launch_pad_offsets(const int32_t* offsets, int E, int32_t* poff, cudaStream_t s) {
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  return launch_pdl(k_pad_offsets, dim3(1), dim3(1024), 0, s, offsets, E, poff, status);
+}
+
+int launch_quant_act(const uint16_t* src, long long ld, long long src_rows,
+                     const int32_t* row_token, const int32_t* offsets, const int32_t* poff,
+                     int E, int K, int P_max, const uint32_t* amax, uint8_t* codes, uint8_t* sf,
+                     cudaStream_t s) {
+  const long long n = static_cast<long long>(P_max) * (K / 64);
+  if (n <= 0) return MOE_OK;
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  return launch_pdl(k_quant_act, dim3(static_cast<unsigned>((n + kQuantThreads - 1) / kQuantThreads)),
+                    dim3(kQuantThreads), static_cast<size_t>(E + 1) * 4, s, src, ld, src_rows,
+                    row_token, offsets, poff, E, K, P_max, amax, codes, sf, status);
+}
+
+}  // namespace moe

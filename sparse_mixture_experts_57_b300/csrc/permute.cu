@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "scan.cuh"
 
 namespace moe {
 namespace {
@@ -80,35 +81,6 @@ __global__ void k_perm_count(const uint32_t* __restrict__ bits, int W, int E,
     }
     if (ty == 31) counts[e] = run;
   }
-}
-
-// Exclusive scan of one value per thread over a block of up to 1024 threads.
-// Returns this thread's exclusive prefix; *total receives the block sum.
-__device__ __forceinline__ int block_exclusive_scan(int c, int* warp_sums, int* total) {
-  const int i = threadIdx.x, lane = i & 31, wid = i >> 5;
-  const int nw = (blockDim.x + 31) >> 5;
-  int incl = c;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += v;
-  }
-  if (lane == 31) warp_sums[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const int ws = lane < nw ? warp_sums[lane] : 0;
-    int wincl = ws;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, wincl, d);
-      if (lane >= d) wincl += v;
-    }
-    warp_sums[lane] = wincl - ws;
-    if (lane == 31) warp_sums[32] = wincl;
-  }
-  __syncthreads();
-  *total = warp_sums[32];
-  return warp_sums[wid] + incl - c;
 }
 
 // Single block, 1024 threads: offsets = exclusive scan of counts (E <= 1024).
@@ -197,6 +169,7 @@ __global__ void k_perm_gather(const int32_t* __restrict__ idx, const uint16_t* _
     row_token[row] = t;
     slot_row[gid] = row;
   }
+  if (x_perm == nullptr) return;  // index-only permutation (the NVFP4 path gathers itself)
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * ldx);
   uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<long long>(row) * H);
   const int nvec = H / 8;

@@ -169,4 +169,56 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ------------------------------------------------------------------- NVFP4 (block scaled)
+// Untiled bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Shared-memory descriptor, no swizzle, K-major: core matrices of 8 rows x 16 bytes with
+// rows 16 bytes apart; sbo = byte distance between 8-row groups, lbo = between core
+// matrices along K.
+__device__ __forceinline__ uint64_t sdesc_k_none(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>(lbo >> 4) << 16) | (static_cast<uint64_t>(sbo >> 4) << 32) |
+         (static_cast<uint64_t>(1) << 46);
+}
+
+// Copy one 512-byte scale-factor atom (32 rows x 16 bytes in shared memory) into 4 TMEM
+// columns, replicated over the four 32-lane quadrants: TMEM lane 32q + r0, column c + r1
+// receives the 4 bytes that the atom holds at r0 * 16 + r1 * 4. This is the layout the
+// block-scaled MMA reads: the scales of A row m at lane m, column c + m / 32; those of B
+// row n at lane n % 32, column c + n / 32.
+__device__ __forceinline__ void tmem_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// D[tmem] (+)= (A * SFA) * (B * SFB)^T with A, B in E2M1 (two per byte, K-major) and one
+// E4M3 scale per 16 elements of K (kind::mxf4nvf4, scale_vec::4X). K = 64 per instruction.
+__device__ __forceinline__ void umma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (bits 7-9 and 10-12 = 1), both
+// K-major, N >> 3 at bit 17, scale type UE4M3 (bit 23 = 0), M >> 4 at bit 24, K = 64.
+__host__ __device__ constexpr uint32_t idesc_nvfp4_f32(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 }  // namespace moe

@@ -378,12 +378,47 @@ def check_grouped_ffn_nvfp4(o):
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
 
 
+def check_nvfp4_layer_paths(o):
+    """The NVFP4 layer, the tensor-wide hidden amax and the sampled per-token evaluation
+    against brute force: table-search quantiser, scalar-loop products, explicit combine."""
+    rng = np.random.default_rng(23)
+    T, D, F, E, k = 6, 32, 16, 3, 2
+    x = moe_synth.bf16_bits(rng.standard_normal((T, D)).astype(np.float32))
+    wr = moe_synth.bf16_bits(rng.standard_normal((E, D)).astype(np.float32))
+    bias = np.zeros(E, np.float32)
+    wu = moe_synth.bf16_bits(rng.standard_normal((E, F, D)).astype(np.float32))
+    wd = moe_synth.bf16_bits(rng.standard_normal((E, D, F)).astype(np.float32))
+    r = o.route(x, wr, bias, k)
+    xf = o.widen_bf16(x).astype(np.float32)
+    xq = _brute_nvfp4(xf, o.nvfp4_global_scale(np.max(np.abs(xf))))
+    wuq = [_brute_nvfp4(o.widen_bf16(wu[e]), o.nvfp4_global_scale(np.max(np.abs(
+        o.widen_bf16(wu[e]).astype(np.float32))))) for e in range(E)]
+    wdq = [_brute_nvfp4(o.widen_bf16(wd[e]), o.nvfp4_global_scale(np.max(np.abs(
+        o.widen_bf16(wd[e]).astype(np.float32))))) for e in range(E)]
+    pairs = [(t, j, int(r["idx"][t, j])) for t in range(T) for j in range(k)]
+    hs = np.array([[max(math.fsum(xq[t, i] * wuq[e][f, i] for i in range(D)), 0.0) ** 2
+                    for f in range(F)] for t, j, e in pairs])
+    h_amax = float(np.max(hs))
+    assert o.nvfp4_hidden_amax(x, r["idx"], wu) == pytest.approx(h_amax, rel=1e-12)
+    hq = _brute_nvfp4(hs.astype(np.float32), o.nvfp4_global_scale(np.float32(h_amax)))
+    ref = np.zeros((T, D))
+    for n, (t, j, e) in enumerate(pairs):
+        ref[t] += r["gates"][t, j] * np.array(
+            [math.fsum(hq[n, f] * wdq[e][i, f] for f in range(F)) for i in range(D)])
+    got = o.moe_layer_nvfp4(x, wr, bias, wu, wd, k)["y"]
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-10)
+    toks = np.array([1, 4])
+    sampled = o.moe_tokens_nvfp4(x, x[toks], r["idx"][toks], r["gates"][toks], wu, wd,
+                                 h_amax=h_amax)
+    np.testing.assert_allclose(sampled, ref[toks], rtol=1e-10, atol=1e-10)
+
+
 ALL_CHECKS = [check_route_closed_form, check_topk_brute_force, check_layer_brute_force,
               check_ffn_closed_form, check_single_expert_is_dense_ffn, check_identical_experts,
               check_k_equals_E, check_forced_expert, check_gate_and_count_invariants,
               check_latent_identity, check_latent_brute_force, check_combine_weights,
               check_e2m1_table, check_e4m3_table, check_nvfp4_block, check_nvfp4_bounds,
-              check_nvfp4_brute_force, check_grouped_ffn_nvfp4]
+              check_nvfp4_brute_force, check_grouped_ffn_nvfp4, check_nvfp4_layer_paths]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
