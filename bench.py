@@ -1,14 +1,16 @@
 """Benchmark of the routed MoE layer forward pass on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload nano_decode|nano_prefill|latent|tiny]
+                    [--workload nano_decode|nano_prefill|latent|nvfp4_prefill|tiny]
 
 One step = one whole layer forward (route, permute, grouped expert FFN, combine; the
 LatentMoE workload adds its two projections) over one batch of seeded synthetic tokens,
 through the library's C ABI. Prints one JSON line.
 
 The default workload is the Nano-shaped decode layer: 64 tokens, H=2688, 128 experts,
-top-6, F=1856. Inputs and weights are resident in HBM before the timed region starts. L2 is
+top-6, F=1856. The NVFP4 prefill workload quantises the expert weights once, untimed, and
+runs moe_forward_nvfp4 (activation quantisation included in every step). Inputs and
+weights are resident in HBM before the timed region starts. L2 is
 flushed (a 512 MiB write) before every timed step. Each step is timed with CUDA events on
 the launching stream; the grouped expert FFN, the dominant kernel, is timed the same way.
 
@@ -40,6 +42,9 @@ import moe_synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and % of roofline (128 experts top-6, bf16) on 1 B300"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# Dense FP4 tensor rate relative to BF16 on B300 (nominal 13.5 vs 2.25 PFLOP/s): the FP4
+# peak is the measured BF16 peak times this ratio.
+FP4_OVER_BF16 = 13.5 / 2.25
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -71,7 +76,10 @@ def layer_algorithmic(w: moe_synth.Workload, counts: np.ndarray) -> dict:
     f_router = 2.0 * w.T * (w.latent if (w.latent and w.router_on_latent) else w.H) * w.E
     f_experts = 4.0 * rows * D * w.F
     f_proj = 4.0 * w.T * w.H * w.latent if w.latent else 0.0
-    b_weights = touched * 2.0 * D * w.F * 2
+    # bf16 weights: 2 bytes per element; NVFP4: half a byte of code plus one E4M3 scale per
+    # 16 elements
+    w_bytes = (0.5 + 1.0 / 16) if w.nvfp4 else 2.0
+    b_weights = touched * 2.0 * D * w.F * w_bytes
     b_router = w.E * (D if (w.latent and w.router_on_latent) else w.H) * 2.0
     b_proj = 2.0 * w.H * w.latent * 2 if w.latent else 0.0
     b_io = 2.0 * w.T * w.H * 2
@@ -79,6 +87,7 @@ def layer_algorithmic(w: moe_synth.Workload, counts: np.ndarray) -> dict:
     # plus the permuted activations read and written
     ffn_bytes_per_launch = touched * D * w.F * 2.0 + rows * (D + w.F) * 2.0
     return {"flops": f_router + f_experts + f_proj, "bytes": b_weights + b_router + b_proj + b_io,
+            "flops_router": f_router, "flops_experts": f_experts, "flops_proj": f_proj,
             "touched": touched, "ffn_flops_per_launch": 2.0 * rows * D * w.F,
             "ffn_bytes_per_launch": ffn_bytes_per_launch}
 
@@ -188,6 +197,13 @@ def run_ours(args, w: moe_synth.Workload):
         ws_lat = torch.empty(L.latent_moe_workspace_size(T, H, w.latent, E, k, F,
                                                          int(w.router_on_latent)),
                              dtype=torch.uint8, device=dev)
+    elif w.nvfp4:
+        # weight quantisation is a set-up step, outside the timed region
+        nv_up = moe.moe_quantize_nvfp4_weights(d["w_up"])
+        nv_down = moe.moe_quantize_nvfp4_weights(d["w_down"])
+        del d["w_up"], d["w_down"]
+        ws_fp4 = torch.empty(L.moe_forward_nvfp4_workspace_size(T, H, E, k, F),
+                             dtype=torch.uint8, device=dev)
     else:
         ws_fwd = torch.empty(L.moe_forward_workspace_size(T, H, E, k, F), dtype=torch.uint8,
                              device=dev)
@@ -200,7 +216,19 @@ def run_ours(args, w: moe_synth.Workload):
 
     # one step; for the standard layer the four calls are issued one by one so the grouped
     # FFN can be bracketed by events on the launching stream
+    def nvfp4_call(x_ptr, idx_ptr, gates_ptr):
+        chk(L.moe_forward_nvfp4(x_ptr, P(d["w_router"]), P(d["bias"]), *nv_up.ptrs(),
+                                *nv_down.ptrs(), T, H, E, k, F, P(y), idx_ptr, gates_ptr,
+                                P(ws_fp4), ws_fp4.numel(), sp), "moe_forward_nvfp4")
+
     def step(e_ffn0=None, e_ffn1=None):
+        if w.nvfp4:
+            if e_ffn0 is not None:
+                e_ffn0.record(stream)
+            nvfp4_call(P(d["x"]), P(idx), P(gates))
+            if e_ffn1 is not None:
+                e_ffn1.record(stream)
+            return
         if w.latent:
             if e_ffn0 is not None:
                 e_ffn0.record(stream)
@@ -224,7 +252,10 @@ def run_ours(args, w: moe_synth.Workload):
         chk(L.moe_combine(P(y_perm), rows, P(slot_row), P(gates), T, H, k, P(y), sp),
             "moe_combine")
 
-    launches_per_step = (11 if w.latent else 9)
+    # kernels per step: route 2, permutation 2-4, FFN 2, combine 1 (bf16); the latent layer
+    # adds its two projections; the NVFP4 layer replaces the gather by amax, padding,
+    # two quantisations and the two block-scaled GEMMs
+    launches_per_step = 11 if w.latent else (12 if w.nvfp4 else 9)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -285,7 +316,9 @@ def run_ours(args, w: moe_synth.Workload):
         a, b = ev(), ev()
         a.record(stream)
         x_dev.copy_(x_host, non_blocking=True)
-        if w.latent:
+        if w.nvfp4:
+            nvfp4_call(P(x_dev), None, None)
+        elif w.latent:
             chk(L.latent_moe(P(x_dev), P(d["w_in"]), P(d["w_out"]), P(d["w_router"]),
                              P(d["bias"]), int(w.router_on_latent), P(d["w_up"]), P(d["w_down"]),
                              T, H, w.latent, E, k, F, P(y), None, None, P(ws_lat),
@@ -314,8 +347,15 @@ def run_ours(args, w: moe_synth.Workload):
 
     peaks, peak_src = load_peaks()
     alg = layer_algorithmic(w, counts_from_routing(routing, E))
-    launches = 1 if w.latent else 2   # grouped GEMM launches inside the FFN bracket
-    if w.latent:
+    launches = 1 if (w.latent or w.nvfp4) else 2   # calls inside the FFN bracket
+    p_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
+    if w.nvfp4:
+        # the whole NVFP4 layer call is bracketed; its block-scaled GEMMs dominate
+        bound = "tensor"
+        achieved = alg["flops_experts"] / (ffn / 1e3) / 1e12
+        peak = p_fp4
+        unit = "TFLOP/s"
+    elif w.latent:
         bound = "tensor"
         dom_units = alg["flops"]
         achieved = dom_units / (ffn / 1e3) / 1e12
@@ -332,8 +372,12 @@ def run_ours(args, w: moe_synth.Workload):
         achieved = alg["ffn_bytes_per_launch"] * launches / (ffn / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
-    roof_ms = max(alg["flops"] / (peaks["bf16_tflops"] * 1e12),
-                  alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    if w.nvfp4:
+        t_flops = (alg["flops_experts"] / p_fp4 +
+                   (alg["flops_router"] + alg["flops_proj"]) / peaks["bf16_tflops"]) / 1e12
+    else:
+        t_flops = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
+    roof_ms = max(t_flops, alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
     traffic = read_traffic(w.name, alg["touched"])
     out = {
         "metric": METRIC,
@@ -346,7 +390,7 @@ def run_ours(args, w: moe_synth.Workload):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "nvfp4 experts, bf16 router" if w.nvfp4 else "bf16",
         "data": "synthetic (seeded, random-init weights of the named shape)",
         "config": {"workload": w.name, "T": T, "H": H, "E": E, "k": k, "F": F,
                    "latent": w.latent or None, "bias": w.bias, "l2": "flushed before every step",
@@ -354,8 +398,11 @@ def run_ours(args, w: moe_synth.Workload):
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": ("whole latent layer (tcgen05 GEMMs dominate)" if w.latent
+                                else "whole NVFP4 layer (block-scaled tcgen05 GEMMs dominate)"
+                                if w.nvfp4
                                 else "grouped expert GEMM (tcgen05), up + down launches"),
-                     "peak_source": peak_src,
+                     "peak_source": (f"{peak_src} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16)"
+                                     if w.nvfp4 else peak_src),
                      "ffn_ms": ffn, "launches_timed": launches},
         "layer_roofline": {"time_ms": roof_ms, "frac": roof_ms / ms,
                            "tflops": alg["flops"] / (ms / 1e3) / 1e12,
@@ -429,6 +476,9 @@ def _oracle_sample(w, inp, toks):
         y_lat = O.moe_tokens(x_lat, r["idx"], r["gates"], inp["w_up"], inp["w_down"])
         return y_lat @ O.widen_bf16(inp["w_out"]).T
     r = O.route(x, inp["w_router"], inp["bias"], w.k)
+    if w.nvfp4:
+        # the sample's own hidden amax stands in for the tensor-wide one: same per-token work
+        return O.moe_tokens_nvfp4(inp["x"], x, r["idx"], r["gates"], inp["w_up"], inp["w_down"])
     return O.moe_tokens(x, r["idx"], r["gates"], inp["w_up"], inp["w_down"])
 
 
@@ -502,7 +552,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="nano_decode",
-                    choices=[k for k, v in moe_synth.WORKLOADS.items() if not v.nvfp4])
+                    choices=list(moe_synth.WORKLOADS))
     ap.add_argument("--T", type=int, default=None,
                     help="override the token count (a scaled case, e.g. for profiling)")
     ap.add_argument("--E", type=int, default=None,

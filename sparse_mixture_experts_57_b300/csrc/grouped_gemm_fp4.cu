@@ -9,15 +9,24 @@
 // for the rows r of group e. Activation rows are laid out with every group padded to whole
 // 128-row tiles, so each row tile starts on a scale-atom boundary.
 //
-// One CTA per SM, 192 threads, as the bf16 kernel:
+// One CTA per SM, 320 threads:
 //   warp 0 lane 0  TMA producer: per stage 256 K-elements (128 bytes) of 128 activation rows
 //                  and 128 weight rows (128-byte swizzle), plus the matching scale atoms
 //                  (2 KB each, untiled bulk copies).
-//   warp 1 lane 0  MMA issuer: tcgen05.cp moves the stage's scale atoms into TMEM (a ring of
-//                  scale columns tied to the smem stages), then tcgen05.mma kind::mxf4nvf4
-//                  (M=128, N=128, K=64) with block scales into a double-buffered fp32
-//                  accumulator.
+//   warps 6..9     scale writers, one per TMEM lane quadrant: read the stage's scale atoms
+//                  from shared memory and write them into a ring of TMEM scale columns
+//                  (tcgen05.st), in the layout the block-scaled MMA reads (see below).
+//   warp 1 lane 0  MMA issuer: tcgen05.mma kind::mxf4nvf4 (M=128, N=128, K=64) with block
+//                  scales into a double-buffered fp32 accumulator.
 //   warps 2..5     epilogue: tcgen05.ld, global scales, squared ReLU or plain, bf16 stores.
+//
+// Scale columns read by one MMA with scale addresses (a, b): A row m at lane m, column
+// a + m / 32; B row n at lane 32 q + n % 32, column b + n / 32, for the lane quadrant q
+// of every output row block (so the B scales are written to all four quadrants). MMA j of
+// a stage uses a = A0 + 4 j and b = B0 + 4 j (addresses on 4-column boundaries), so a stage
+// takes 16 A columns (each lane writes the one column of its quadrant per MMA) and 16 B
+// columns. Writing the scales with warp stores keeps the tensor pipe's own queue free of
+// copies.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -34,7 +43,7 @@ constexpr int KSTEP = 64;       // K elements per MMA
 constexpr int STEPS_PER_STAGE = 4;
 constexpr int STAGES = 5;
 constexpr int MAXG = 1024;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;
 constexpr uint32_t A_BYTES = BM * BKB;
 constexpr uint32_t B_BYTES = BN * BKB;
 constexpr uint32_t ATOM = 512;
@@ -42,7 +51,8 @@ constexpr uint32_t SF_STAGE = STEPS_PER_STAGE * ATOM;  // one 128-row block, 4 K
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = BN;                     // accumulators at columns 0 and 128
 constexpr uint32_t SF_COL0 = 2 * BN;                    // then per stage 16 A + 16 B columns
-constexpr uint32_t SF_COLS_PER_STAGE = 2 * 4 * STEPS_PER_STAGE;
+constexpr uint32_t SF_A_COLS = 16;
+constexpr uint32_t SF_COLS_PER_STAGE = 32;
 static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
 constexpr uint32_t IDESC = idesc_nvfp4_f32(BM, BN);
 
@@ -63,7 +73,7 @@ struct KArgs {
 };
 
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(STAGES) * (A_BYTES + B_BYTES + 2 * SF_STAGE) + (2 * STAGES + 4) * 8 + 16 +
+  return 1024 + size_t(STAGES) * (A_BYTES + B_BYTES + 2 * SF_STAGE) + (3 * STAGES + 4) * 8 + 16 +
          4 * (MAXG + 1) * 4;
 }
 
@@ -86,7 +96,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sSFB = sSFA + STAGES * SF_STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * SF_STAGE);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* sfull = empty + STAGES;  // the stage's scales are in TMEM
+  uint64_t* tfull = sfull + STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -103,6 +114,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
+      mbar_init(&sfull[i], 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -250,21 +262,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
         for (int kb = 0; kb < NST; ++kb) {
           const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          // the scale writers arrive only after the stage's operands have landed
+          if (!mbar_wait(&sfull[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // Scale atoms -> TMEM. The column ring is tied to the smem stages: this stage's
-          // columns were last read by MMAs that completed before its smem slot was refilled.
           const uint32_t sfa_col = SF_COL0 + stage * SF_COLS_PER_STAGE;
-          const uint32_t sfb_col = sfa_col + 4 * STEPS_PER_STAGE;
-          for (int j = 0; j < nsteps; ++j) {
-            tmem_cp_sf_atom(tmem_base + sfa_col + 4 * j,
-                            sdesc_k_none(smem_u32(sSFA + stage * SF_STAGE + j * ATOM), 2048, 128));
-            tmem_cp_sf_atom(tmem_base + sfb_col + 4 * j,
-                            sdesc_k_none(smem_u32(sSFB + stage * SF_STAGE + j * ATOM), 2048, 128));
-          }
+          const uint32_t sfb_col = sfa_col + SF_A_COLS;
           const uint64_t adesc = sdesc_k_sw128(smem_u32(sA + stage * A_BYTES));
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(sB + stage * B_BYTES));
           for (int j = 0; j < nsteps; ++j)
@@ -287,6 +292,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 1;
         record(a.status, MOE_ERR_TIMEOUT);
       }
+    }
+  } else if (warp >= 6) {
+    // -------------------------------------------------------------------- scale writers
+    // Quadrant q of TMEM, lane r0 = this lane. The smem atoms hold row 32 r1 + r0 of step j
+    // at byte j * 512 + r0 * 16 + r1 * 4 (four E4M3 scales, one per 16 K elements).
+    const int q = warp & 3;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int kb = 0; kb < NST; ++kb) {
+        const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
+        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sa = sSFA + stage * SF_STAGE;
+        const uint8_t* sb = sSFB + stage * SF_STAGE;
+        uint32_t wa[4];
+        uint32_t wb[16];
+#pragma unroll
+        for (int j = 0; j < STEPS_PER_STAGE; ++j) {
+          if (j < nsteps) {
+            wa[j] = *reinterpret_cast<const uint32_t*>(sa + j * ATOM + lane * 16 + q * 4);
+            const uint4 v = *reinterpret_cast<const uint4*>(sb + j * ATOM + lane * 16);
+            wb[4 * j] = v.x;
+            wb[4 * j + 1] = v.y;
+            wb[4 * j + 2] = v.z;
+            wb[4 * j + 3] = v.w;
+          } else {
+            wa[j] = 0u;
+            wb[4 * j] = wb[4 * j + 1] = wb[4 * j + 2] = wb[4 * j + 3] = 0u;
+          }
+        }
+        // The ring slot of this stage was last read by MMAs that completed before the
+        // stage's smem was refilled, i.e. before full[stage] fired for this phase.
+        const uint32_t sfa_col = SF_COL0 + stage * SF_COLS_PER_STAGE;  // 32-column aligned
+#pragma unroll
+        for (int j = 0; j < STEPS_PER_STAGE; ++j) tmem_st1(lane_base + sfa_col + 4 * j + q, wa[j]);
+        tmem_st16(lane_base + sfa_col + SF_A_COLS, wb);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (lane == 0) record(a.status, MOE_ERR_TIMEOUT);
     }
   } else {
     // ------------------------------------------------------------------------ epilogue
