@@ -9,24 +9,30 @@
 // for the rows r of group e. Activation rows are laid out with every group padded to whole
 // 128-row tiles, so each row tile starts on a scale-atom boundary.
 //
-// One CTA per SM, 320 threads:
+// One CTA per SM, 448 threads:
 //   warp 0 lane 0  TMA producer: per stage 256 K-elements (128 bytes) of 128 activation rows
-//                  and 128 weight rows (128-byte swizzle), plus the matching scale atoms
-//                  (2 KB each, untiled bulk copies).
-//   warps 6..9     scale writers, one per TMEM lane quadrant: read the stage's scale atoms
+//                  and 256 weight rows (128-byte swizzle), plus the matching scale atoms
+//                  (untiled bulk copies).
+//   warps 10..13   scale writers, one per TMEM lane quadrant: read the stage's scale atoms
 //                  from shared memory and write them into a ring of TMEM scale columns
 //                  (tcgen05.st), in the layout the block-scaled MMA reads (see below).
-//   warp 1 lane 0  MMA issuer: tcgen05.mma kind::mxf4nvf4 (M=128, N=128, K=64) with block
-//                  scales into a double-buffered fp32 accumulator.
-//   warps 2..5     epilogue: tcgen05.ld, global scales, squared ReLU or plain, bf16 stores.
+//   warp 1 lane 0  MMA issuer: tcgen05.mma kind::mxf4nvf4 (M=128, N=256, K=64) with block
+//                  scales into one fp32 accumulator of 256 TMEM columns.
+//   warps 2..9     epilogue, two warps per lane quadrant (128 columns each): tcgen05.ld of
+//                  the accumulator into registers (global scales, activation, packed to
+//                  bf16), then the accumulator is released to the next tile's MMAs before
+//                  the stores go out.
+//
+// Why N = 256: with block-scaled FP4 MMAs the tensor cores consume operand bytes from shared
+// memory 4x faster than with bf16, and the TMA must write the same bytes into shared memory.
+// An M=128, N=256 tile moves 12 KB per 2M MACs where N = 128 moves 8 KB per 1M.
 //
 // Scale columns read by one MMA with scale addresses (a, b): A row m at lane m, column
 // a + m / 32; B row n at lane 32 q + n % 32, column b + n / 32, for the lane quadrant q
 // of every output row block (so the B scales are written to all four quadrants). MMA j of
-// a stage uses a = A0 + 4 j and b = B0 + 4 j (addresses on 4-column boundaries), so a stage
-// takes 16 A columns (each lane writes the one column of its quadrant per MMA) and 16 B
-// columns. Writing the scales with warp stores keeps the tensor pipe's own queue free of
-// copies.
+// a stage uses a = A0 + 4 j and b = B0 + 8 j (addresses on 4-column boundaries): per stage
+// 16 A columns (each lane writes the one column of its quadrant per MMA) and 32 B columns.
+// Writing the scales with warp stores keeps the tensor pipe's own queue free of copies.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -37,22 +43,23 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 256;
 constexpr int BKB = 128;        // K bytes per stage and row: 256 E2M1 elements
 constexpr int KSTEP = 64;       // K elements per MMA
 constexpr int STEPS_PER_STAGE = 4;
-constexpr int STAGES = 5;
+constexpr int STAGES = 4;
 constexpr int MAXG = 1024;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 448;
+constexpr int EPI_WARP0 = 2, SFW_WARP0 = 10;
 constexpr uint32_t A_BYTES = BM * BKB;
 constexpr uint32_t B_BYTES = BN * BKB;
 constexpr uint32_t ATOM = 512;
-constexpr uint32_t SF_STAGE = STEPS_PER_STAGE * ATOM;  // one 128-row block, 4 K steps
+constexpr uint32_t SFA_STAGE = STEPS_PER_STAGE * ATOM;      // one 128-row block, 4 K steps
+constexpr uint32_t SFB_STAGE = 2 * STEPS_PER_STAGE * ATOM;  // two 128-row blocks
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_STRIDE = BN;                     // accumulators at columns 0 and 128
-constexpr uint32_t SF_COL0 = 2 * BN;                    // then per stage 16 A + 16 B columns
-constexpr uint32_t SF_A_COLS = 16;
-constexpr uint32_t SF_COLS_PER_STAGE = 32;
+constexpr uint32_t SF_COL0 = BN;                 // accumulator in columns [0, 256)
+constexpr uint32_t SF_COLS_PER_STAGE = 64;       // A at +0 (16 columns), B at +32 (32)
+constexpr uint32_t SF_B_OFF = 32;
 static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
 constexpr uint32_t IDESC = idesc_nvfp4_f32(BM, BN);
 
@@ -73,8 +80,8 @@ struct KArgs {
 };
 
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(STAGES) * (A_BYTES + B_BYTES + 2 * SF_STAGE) + (3 * STAGES + 4) * 8 + 16 +
-         4 * (MAXG + 1) * 4;
+  return 1024 + size_t(STAGES) * (A_BYTES + B_BYTES + SFA_STAGE + SFB_STAGE) +
+         (3 * STAGES + 2) * 8 + 16 + (MAXG + 1) * 4;
 }
 
 __device__ __forceinline__ void record(int* status, int code) { atomicCAS(status, 0, code); }
@@ -93,18 +100,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + STAGES * A_BYTES;
   uint8_t* sSFA = sB + STAGES * B_BYTES;
-  uint8_t* sSFB = sSFA + STAGES * SF_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * SF_STAGE);
+  uint8_t* sSFB = sSFA + STAGES * SFA_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * SFB_STAGE);
   uint64_t* empty = full + STAGES;
   uint64_t* sfull = empty + STAGES;  // the stage's scales are in TMEM
-  uint64_t* tfull = sfull + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tfull = sfull + STAGES;  // the accumulator holds a finished tile
+  uint64_t* tempty = tfull + 1;      // the epilogue has read the accumulator
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_pref = reinterpret_cast<int*>(tmem_slot + 4);  // row-tile prefix per group
-  int* s_aoff = s_pref + (MAXG + 1);                     // padded row offset
-  int* s_ooff = s_aoff + (MAXG + 1);                     // output row offset
-  int* s_ocnt = s_ooff + (MAXG + 1);                     // rows to store
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -116,10 +120,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&empty[i], 1);
       mbar_init(&sfull[i], 4);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
-    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 32 * (SFW_WARP0 - EPI_WARP0));
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -134,7 +136,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   griddep_wait();
   griddep_launch_dependents();
   if (warp == 2) {
-    // Group table: padded segments (whole 128-row tiles) and where their outputs go.
+    // Row-tile prefix over the groups' padded segments (whole 128-row tiles). A group whose
+    // offsets are inconsistent is reported and gets no tiles, so no role ever reads it.
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
     int local = 0;
@@ -145,23 +148,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lo < 0 || hi < lo || hi > a.P || ((lo | hi) & (BM - 1))) {
         bad = true;
         tiles = 0;
-      }
-      int olo = lo, ocnt = hi - lo;
-      if (a.out_off) {
-        olo = a.out_off[e];
-        ocnt = a.out_off[e + 1] - olo;
+      } else if (a.out_off) {
+        const int olo = a.out_off[e], ocnt = a.out_off[e + 1] - olo;
         if (olo < 0 || ocnt < 0 || olo + ocnt > a.out_rows || ocnt > hi - lo) {
           bad = true;
           tiles = 0;
-          ocnt = 0;
         }
       } else if (hi > a.out_rows) {
         bad = true;
         tiles = 0;
       }
-      s_aoff[e] = lo;
-      s_ooff[e] = olo;
-      s_ocnt[e] = ocnt;
       s_pref[e] = tiles;  // temporarily the tile count
       local += tiles;
     }
@@ -186,6 +182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const uint32_t tmem_base = *tmem_slot;
   const int n_ct = (a.N + BN - 1) / BN;
+  const int nbw = (a.N + 127) / 128;                               // weight scale row blocks
   const int total = s_pref[E] * n_ct;
   const int KS = a.K / KSTEP;                                      // MMA steps along K
   const int NST = (KS + STEPS_PER_STAGE - 1) / STEPS_PER_STAGE;    // pipeline stages along K
@@ -208,32 +205,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
-      const uint64_t pol_w = policy_evict_last();
-      const uint64_t pol_a = policy_evict_last();
-      const int nbw = n_ct;  // weight scale row blocks per expert
+      const uint64_t pol = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, rt, ct;
         decode(tile, e, rt, ct);
-        const int row0 = s_aoff[e] + rt * BM;
+        const int row0 = __ldg(a.poff + e) + rt * BM;
         const int col0 = ct * BN;
+        const bool two = 2 * ct + 1 < nbw;  // the tile's second 128-row weight block exists
         const uint8_t* sfa = a.a_sf + (static_cast<long long>(row0 / BM) * KS) * ATOM;
         const uint8_t* sfw =
-            a.w_sf + ((static_cast<long long>(e) * nbw + ct) * KS) * ATOM;
+            a.w_sf + ((static_cast<long long>(e) * nbw + 2 * ct) * KS) * ATOM;
         for (int kb = 0; kb < NST; ++kb) {
           const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + 2u * nsteps * ATOM);
-          tma_load_2d(sA + stage * A_BYTES, &tm_a, &full[stage], kb * BKB, row0, pol_a);
-          tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kb * BKB, col0, e, pol_w);
+          const uint32_t sf_bytes = nsteps * ATOM;
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + (two ? 3u : 2u) * sf_bytes);
+          tma_load_2d(sA + stage * A_BYTES, &tm_a, &full[stage], kb * BKB, row0, pol);
+          tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kb * BKB, col0, e, pol);
           const long long so = static_cast<long long>(kb) * STEPS_PER_STAGE * ATOM;
-          bulk_load(sSFA + stage * SF_STAGE, sfa + so, nsteps * ATOM, &full[stage], pol_a);
-          bulk_load(sSFB + stage * SF_STAGE, sfw + so, nsteps * ATOM, &full[stage], pol_w);
+          bulk_load(sSFA + stage * SFA_STAGE, sfa + so, sf_bytes, &full[stage], pol);
+          bulk_load(sSFB + stage * SFB_STAGE, sfw + so, sf_bytes, &full[stage], pol);
+          if (two)
+            bulk_load(sSFB + stage * SFB_STAGE + SFA_STAGE, sfw + static_cast<long long>(KS) * ATOM + so,
+                      sf_bytes, &full[stage], pol);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -250,16 +250,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // -------------------------------------------------------------------- MMA issuer
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
         for (int kb = 0; kb < NST; ++kb) {
           const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
           // the scale writers arrive only after the stage's operands have landed
@@ -269,12 +267,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sfa_col = SF_COL0 + stage * SF_COLS_PER_STAGE;
-          const uint32_t sfb_col = sfa_col + SF_A_COLS;
+          const uint32_t sfb_col = sfa_col + SF_B_OFF;
           const uint64_t adesc = sdesc_k_sw128(smem_u32(sA + stage * A_BYTES));
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(sB + stage * B_BYTES));
           for (int j = 0; j < nsteps; ++j)
-            umma_nvfp4(d_tmem, adesc + 2u * j, bdesc + 2u * j, IDESC,
-                       tmem_base + sfa_col + 4 * j, tmem_base + sfb_col + 4 * j, (kb | j) != 0);
+            umma_nvfp4(tmem_base, adesc + 2u * j, bdesc + 2u * j, IDESC,
+                       tmem_base + sfa_col + 4 * j, tmem_base + sfb_col + 8 * j, (kb | j) != 0);
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -282,57 +280,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
+        umma_commit(tfull);
+        acc_phase ^= 1u;
       }
       if (!ok) {
         *abort_flag = 1;
         record(a.status, MOE_ERR_TIMEOUT);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= SFW_WARP0) {
     // -------------------------------------------------------------------- scale writers
     // Quadrant q of TMEM, lane r0 = this lane. The smem atoms hold row 32 r1 + r0 of step j
-    // at byte j * 512 + r0 * 16 + r1 * 4 (four E4M3 scales, one per 16 K elements).
+    // at byte j * 512 + r0 * 16 + r1 * 4 (four E4M3 scales, one per 16 K elements); the B
+    // stage holds the tile's first 128 weight rows, then the second.
     const int q = warp & 3;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      int e, rt, ct;
+      decode(tile, e, rt, ct);
+      const bool two = 2 * ct + 1 < nbw;
       for (int kb = 0; kb < NST; ++kb) {
         const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
         if (!mbar_wait(&full[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
-        const uint8_t* sa = sSFA + stage * SF_STAGE;
-        const uint8_t* sb = sSFB + stage * SF_STAGE;
-        uint32_t wa[4];
-        uint32_t wb[16];
+        const uint8_t* sa = sSFA + stage * SFA_STAGE;
+        const uint8_t* sb = sSFB + stage * SFB_STAGE;
+        uint32_t wa[STEPS_PER_STAGE];
+        uint32_t wb[2][16];
 #pragma unroll
         for (int j = 0; j < STEPS_PER_STAGE; ++j) {
+          uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+          wa[j] = 0u;
           if (j < nsteps) {
             wa[j] = *reinterpret_cast<const uint32_t*>(sa + j * ATOM + lane * 16 + q * 4);
-            const uint4 v = *reinterpret_cast<const uint4*>(sb + j * ATOM + lane * 16);
-            wb[4 * j] = v.x;
-            wb[4 * j + 1] = v.y;
-            wb[4 * j + 2] = v.z;
-            wb[4 * j + 3] = v.w;
-          } else {
-            wa[j] = 0u;
-            wb[4 * j] = wb[4 * j + 1] = wb[4 * j + 2] = wb[4 * j + 3] = 0u;
+            v0 = *reinterpret_cast<const uint4*>(sb + j * ATOM + lane * 16);
+            if (two) v1 = *reinterpret_cast<const uint4*>(sb + SFA_STAGE + j * ATOM + lane * 16);
           }
+          uint32_t* w = wb[j >> 1] + 8 * (j & 1);
+          w[0] = v0.x;
+          w[1] = v0.y;
+          w[2] = v0.z;
+          w[3] = v0.w;
+          w[4] = v1.x;
+          w[5] = v1.y;
+          w[6] = v1.z;
+          w[7] = v1.w;
         }
         // The ring slot of this stage was last read by MMAs that completed before the
         // stage's smem was refilled, i.e. before full[stage] fired for this phase.
-        const uint32_t sfa_col = SF_COL0 + stage * SF_COLS_PER_STAGE;  // 32-column aligned
+        const uint32_t sfa_col = SF_COL0 + stage * SF_COLS_PER_STAGE;  // 64-column aligned
 #pragma unroll
         for (int j = 0; j < STEPS_PER_STAGE; ++j) tmem_st1(lane_base + sfa_col + 4 * j + q, wa[j]);
-        tmem_st16(lane_base + sfa_col + SF_A_COLS, wb);
+        tmem_st16(lane_base + sfa_col + SF_B_OFF, wb[0]);
+        tmem_st16(lane_base + sfa_col + SF_B_OFF + 16, wb[1]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -350,60 +355,79 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    const int half = (warp - EPI_WARP0) >> 2;  // columns [128 half, 128 half + 128)
     const int m = q * 32 + lane;
     const float ga = __fdiv_rn(__uint_as_float(*a.a_amax), kNvfp4GlobalDiv);
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + 128 * half;
     float vmax = 0.f;
-    int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, rt, ct;
       decode(tile, e, rt, ct);
       const int local = rt * BM + m;
-      const bool valid = local < s_ocnt[e];
-      const long long row = static_cast<long long>(s_ooff[e]) + local;
-      const int col0 = ct * BN;
-      const int ncols = min(BN, a.N - col0);
-      const float scale = ga * a.w_gscale[e];
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
+      int ocnt, obase;
+      if (a.out_off) {
+        obase = __ldg(a.out_off + e);
+        ocnt = __ldg(a.out_off + e + 1) - obase;
+      } else {
+        obase = __ldg(a.poff + e);
+        ocnt = __ldg(a.poff + e + 1) - obase;
+      }
+      const bool valid = local < ocnt;
+      const long long row = static_cast<long long>(obase) + local;
+      const int c0 = ct * BN + 128 * half;           // first column of this warp
+      const int ncols = max(0, min(128, a.N - c0));  // warp-uniform, a multiple of 16
+      const float scale = ga * __ldg(a.w_gscale + e);
+      if (!mbar_wait(tfull, acc_phase, abort_flag)) {
         *abort_flag = 1;
         record(a.status, MOE_ERR_TIMEOUT);
         break;
       }
       tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_STRIDE;
-      for (int n0 = 0; n0 < ncols; n0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tb + n0, r);
-        tmem_ld_wait();
-        float v[16];
+      uint32_t p[64];  // this row's 128 outputs, packed bf16 pairs
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * scale;
-        if (a.epi == EPI_SQRELU_BF16) {
+      for (int c = 0; c < 4; ++c) {
+        if (32 * c < ncols) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(tb + 32 * c, r0);
+          tmem_ld16(tb + 32 * c + 16, r1);
+          tmem_ld_wait();
+          float v[32];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float t = fmaxf(v[i], 0.f);
-            v[i] = t * t;
+            v[i] = __uint_as_float(r0[i]) * scale;
+            v[16 + i] = __uint_as_float(r1[i]) * scale;
           }
-        }
-        if (valid) {
           if (a.epi == EPI_SQRELU_BF16) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) vmax = fmaxf(vmax, v[i]);
-          }
-          uint32_t p[8];
+            for (int i = 0; i < 32; ++i) {
+              const float t = fmaxf(v[i], 0.f);
+              v[i] = t * t;
+            }
+            if (valid) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) p[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                                                row * a.ldo + col0 + n0);
-          dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-          dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+              for (int i = 0; i < 32; ++i) vmax = fmaxf(vmax, v[i]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) p[16 * c + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
         }
       }
+      // The accumulator is in registers: let the next tile's MMAs start.
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
+      mbar_arrive(tempty);
+      acc_phase ^= 1u;
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * a.ldo + c0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (32 * c < ncols) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[4 * c + i] = make_uint4(p[16 * c + 4 * i], p[16 * c + 4 * i + 1],
+                                          p[16 * c + 4 * i + 2], p[16 * c + 4 * i + 3]);
+          }
+        }
       }
     }
     if (a.out_amax) {
@@ -427,7 +451,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   if (g.P <= 0) return MOE_OK;
-  if (g.K % KSTEP || g.N % 16 || g.E < 1 || g.E > MAXG || g.P % BM) return MOE_ERR_UNSUPPORTED;
+  if (g.K % KSTEP || g.N % 32 || g.E < 1 || g.E > MAXG || g.P % BM) return MOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_BF16 && g.epi != EPI_SQRELU_BF16) return MOE_ERR_UNSUPPORTED;
   KArgs ka;
   ka.poff = g.poff;

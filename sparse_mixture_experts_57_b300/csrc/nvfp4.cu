@@ -8,7 +8,8 @@
 //                                                            saturating at 6)
 //   value           = q * sb * g
 // Blocks run along the contraction axis K. Every decision is taken in fp32 with correctly
-// rounded division, so the codes and scales depend only on the input bits.
+// rounded division, so the codes and scales depend only on the input bits (and match an
+// fp32 evaluation of the same formulas exactly).
 //
 // Layouts (shared with the block-scaled grouped GEMM): codes [rows, K/2], element 2i in the
 // low nibble; scales as 512-byte atoms, one per (128-row block, 64-element K step): row
@@ -24,13 +25,32 @@
 namespace moe {
 namespace {
 
-// E2M1 code (sign in bit 3) of s rounded to the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6;
-// a value exactly between two neighbours takes the one with the even code; |s| > 6 gives 6.
-__device__ __forceinline__ uint32_t e2m1_code(float s) {
-  const float m = fabsf(s);
-  const uint32_t c = (m > 0.25f) + (m >= 0.75f) + (m > 1.25f) + (m >= 1.75f) + (m > 2.5f) +
-                     (m >= 3.5f) + (m > 5.0f);
-  return (c != 0u && s < 0.f) ? (c | 8u) : c;
+// Eight values rounded to E2M1 (nearest, ties to the even code, saturating at +-6) and
+// packed two per byte, element 2i in the low nibble: the hardware's round-to-nearest-even
+// conversion of fp32 to E2M1 pairs (the first source operand goes to the high nibble).
+__device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]),
+        "f"(q[7]));
+  return r;
+}
+
+// v / d correctly rounded, for a divisor d with 2^-100 < d < 2^100 and |v / d| < 2^100:
+// Markstein's division by fused multiply-add (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// y = RN(1/d) and q = RN(v y), the remainder r = v - q d is exact in one fma, and
+// RN(q + r y) = RN(v / d).
+__device__ __forceinline__ float div_markstein(float v, float d, float y) {
+  const float q = __fmul_rn(v, y);
+  const float r = fmaf(-q, d, v);
+  return fmaf(r, y, q);
 }
 
 // Value of a non-negative E4M3 byte: exponent bias 7, 3 mantissa bits, subnormals below 2^-6.
@@ -70,13 +90,22 @@ __device__ __forceinline__ uint32_t quant64(const uint4* __restrict__ src, float
           __nv_cvt_float_to_fp8(__fdiv_rn(bmax, six_g), __NV_SATFINITE, __NV_E4M3));
       denom = __fmul_rn(e4m3_value(sb), g);
     }
-    q[2 * blk] = 0u;
-    q[2 * blk + 1] = 0u;
-    if (denom > 0.f) {
+    float s[16];
+    if (denom > 0x1p-100f && denom < 0x1p100f) {
+      const float y = __frcp_rn(denom);
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        q[2 * blk + (i >> 3)] |= e2m1_code(__fdiv_rn(v[i], denom)) << (4 * (i & 7));
+      for (int i = 0; i < 16; ++i) s[i] = div_markstein(v[i], denom, y);
+    } else if (denom > 0.f) {  // outside the range of the fast division
+#pragma unroll
+      for (int i = 0; i < 16; ++i) s[i] = __fdiv_rn(v[i], denom);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) s[i] = 0.f;
     }
+    const float lo[8] = {s[0], s[1], s[2], s[3], s[4], s[5], s[6], s[7]};
+    const float hi[8] = {s[8], s[9], s[10], s[11], s[12], s[13], s[14], s[15]};
+    q[2 * blk] = e2m1x8(lo);
+    q[2 * blk + 1] = e2m1x8(hi);
     sf |= sb << (8 * blk);
   }
   dst[0] = make_uint4(q[0], q[1], q[2], q[3]);

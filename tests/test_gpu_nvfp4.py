@@ -80,15 +80,45 @@ def _rel_checks(got, ref, what):
 
 # --------------------------------------------------------------------- quantiser ----
 
+def _tie_matrix(N, K):
+    """Values exactly on every E2M1 rounding boundary of their block, and one bf16 step to
+    either side. The matrix amax is 168 = 2688 / 16, so g = 1/16 exactly; every other block
+    has amax 6 g s for a block scale s with few mantissa bits, so its divisor is s g exactly
+    and the boundaries t s g are exact bf16 values."""
+    g = 1.0 / 16
+    scales = [1.0, 1.25, 1.5, 1.75, 0.5625, 3.0, 0.75, 2.5]
+    bounds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    w = np.zeros((N, K), np.float32)
+    for r in range(N):
+        for b in range(K // 16):
+            sc = scales[(r + b) % len(scales)]
+            d = sc * g
+            blk = [6 * g * sc]
+            for i in range(15):
+                t = bounds[(r * 3 + b + i) % len(bounds)]
+                v = np.float32(t * d)
+                side = (i + r) % 3                  # on, below, above the boundary
+                if side:
+                    bits = moe_synth.bf16_bits(np.array([v], np.float32)).astype(np.int32)
+                    bits += 1 if side == 2 else -1
+                    v = O.widen_bf16(bits.astype(np.uint16))[0]
+                blk.append(v if (i + b) % 2 else -v)
+            w[r, 16 * b:16 * b + 16] = blk
+    w[0, 0] = 2688 * g                             # the matrix amax
+    return w
+
+
 def test_quantize_weights_bit_exact(moe):
-    G, N, K = 4, 200, 320                  # ragged last 128-row block, 5 K steps
+    G, N, K = 5, 200, 320                  # ragged last 128-row block, 5 K steps
     rng = np.random.default_rng(31)
     w = rng.standard_normal((G, N, K)).astype(np.float32) / np.sqrt(K)
     # matrix 1: rows spanning 24 binades, so small blocks get subnormal E4M3 scales
     w[1] *= np.exp2(-(np.arange(N) % 24))[:, None].astype(np.float32)
     w[2] = 0.0                             # all-zero matrix: g = 0, every scale 0
     w[3, :, :16] = 0.0                     # all-zero blocks inside a live matrix
+    w[4] = _tie_matrix(N, K)               # rounding ties and their neighbours
     wb = moe_synth.bf16_bits(w)
+    assert (O.widen_bf16(wb[4]) == w[4]).all()     # the tie values are exact in bf16
     nv = moe.moe_quantize_nvfp4_weights(to_dev(wb))
     torch.cuda.synchronize()
     _status_ok(moe)
