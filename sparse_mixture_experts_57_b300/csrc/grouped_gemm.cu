@@ -548,7 +548,8 @@ int pick_bn_rows_as_m(int N) {
 }  // namespace
 
 bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base,
-                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn || rank < 2 || rank > 3) return false;
   cuuint64_t d[3], st[2];
@@ -559,7 +560,7 @@ bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void
   }
   for (int i = 0; i < rank - 1; ++i) st[i] = strides_bytes[i];
   return fn(m, dtype, rank, const_cast<void*>(base), d, st, b, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

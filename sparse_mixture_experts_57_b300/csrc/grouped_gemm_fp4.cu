@@ -21,7 +21,9 @@
 //   warps 2..9     epilogue, two warps per lane quadrant (128 columns each): tcgen05.ld of
 //                  the accumulator into registers (global scales, activation, packed to
 //                  bf16), then the accumulator is released to the next tile's MMAs before
-//                  the stores go out.
+//                  the stores go out. A warp's 32-row band goes out as 32x32 pieces staged in
+//                  swizzled shared memory and written by TMA stores; only the partial last
+//                  band of an expert is stored row by row.
 //
 // Why N = 256: with block-scaled FP4 MMAs the tensor cores consume operand bytes from shared
 // memory 4x faster than with bf16, and the TMA must write the same bytes into shared memory.
@@ -47,7 +49,7 @@ constexpr int BN = 256;
 constexpr int BKB = 128;        // K bytes per stage and row: 256 E2M1 elements
 constexpr int KSTEP = 64;       // K elements per MMA
 constexpr int STEPS_PER_STAGE = 4;
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int MAXG = 1024;
 constexpr int NUM_THREADS = 448;
 constexpr int EPI_WARP0 = 2, SFW_WARP0 = 10;
@@ -59,6 +61,8 @@ constexpr uint32_t SFB_STAGE = 2 * STEPS_PER_STAGE * ATOM;  // two 128-row block
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = BN;                 // accumulator in columns [0, 256)
 constexpr uint32_t SF_COLS_PER_STAGE = 64;       // A at +0 (16 columns), B at +32 (32)
+constexpr uint32_t STG_BYTES = 2048;             // one 32 x 32 bf16 output piece
+constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t SF_B_OFF = 32;
 static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
 constexpr uint32_t IDESC = idesc_nvfp4_f32(BM, BN);
@@ -81,7 +85,7 @@ struct KArgs {
 
 constexpr size_t smem_bytes() {
   return 1024 + size_t(STAGES) * (A_BYTES + B_BYTES + SFA_STAGE + SFB_STAGE) +
-         (3 * STAGES + 2) * 8 + 16 + (MAXG + 1) * 4;
+         size_t(NUM_EPI_WARPS) * 2 * STG_BYTES + (3 * STAGES + 2) * 8 + 16 + (MAXG + 1) * 4;
 }
 
 __device__ __forceinline__ void record(int* status, int code) { atomicCAS(status, 0, code); }
@@ -93,7 +97,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_fp4_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
-               const KArgs a) {
+               const __grid_constant__ CUtensorMap tm_out, const KArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -101,7 +105,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sB = sA + STAGES * A_BYTES;
   uint8_t* sSFA = sB + STAGES * B_BYTES;
   uint8_t* sSFB = sSFA + STAGES * SFA_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * SFB_STAGE);
+  uint8_t* sStage = sSFB + STAGES * SFB_STAGE;  // per epilogue warp: two 2 KB pieces
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + NUM_EPI_WARPS * 2 * STG_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* sfull = empty + STAGES;  // the stage's scales are in TMEM
   uint64_t* tfull = sfull + STAGES;  // the accumulator holds a finished tile
@@ -359,6 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int m = q * 32 + lane;
     const float ga = __fdiv_rn(__uint_as_float(*a.a_amax), kNvfp4GlobalDiv);
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + 128 * half;
+    uint8_t* stg = sStage + (warp - EPI_WARP0) * 2 * STG_BYTES;
     float vmax = 0.f;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -417,7 +423,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       mbar_arrive(tempty);
       acc_phase ^= 1u;
-      if (valid) {
+      const int band0 = rt * BM + q * 32;  // first local row of this warp's band
+      if (band0 + 32 <= ocnt) {
+        // Whole band valid: 32 x 32 pieces through shared memory (64-byte swizzle: 16-byte
+        // chunk c of row r at chunk c ^ ((r >> 1) & 3)), written by TMA.
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (32 * c < ncols) {
+            uint8_t* buf = stg + (c & 1) * STG_BYTES;
+            if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf is done
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(p[16 * c + 4 * i], p[16 * c + 4 * i + 1], p[16 * c + 4 * i + 2],
+                             p[16 * c + 4 * i + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_out, buf, c0 + 32 * c, obase + band0);
+              bulk_commit_group();
+            }
+          }
+        }
+      } else if (valid) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * a.ldo + c0);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -430,6 +459,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    if (lane == 0) bulk_wait_group_all();  // the staged pieces are written out
     if (a.out_amax) {
 #pragma unroll
       for (int d = 16; d > 0; d >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, d));
@@ -451,7 +481,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   if (g.P <= 0) return MOE_OK;
-  if (g.K % KSTEP || g.N % 32 || g.E < 1 || g.E > MAXG || g.P % BM) return MOE_ERR_UNSUPPORTED;
+  if (g.K % KSTEP || g.N % 32 || g.E < 1 || g.E > MAXG || g.P % BM || g.ldo % 8 ||
+      (reinterpret_cast<uintptr_t>(g.out) & 15))
+    return MOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_BF16 && g.epi != EPI_SQRELU_BF16) return MOE_ERR_UNSUPPORTED;
   KArgs ka;
   ka.poff = g.poff;
@@ -489,6 +521,15 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
     if (!encode_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_codes, dims, strides, box))
       return MOE_ERR_CUDA;
   }
+  CUtensorMap tm_out;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.out_rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(g.ldo) * 2};
+    const uint32_t box[2] = {32, 32};
+    if (!encode_tmap(&tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.out, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_64B))
+      return MOE_ERR_CUDA;
+  }
   constexpr size_t smem = smem_bytes();
   static_assert(smem <= 232448, "shared memory per CTA");
   static int configured_device = -1;
@@ -502,7 +543,7 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   const long long tiles = static_cast<long long>(g.P / BM) * ((g.N + BN - 1) / BN);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   if (grid <= 0) return MOE_OK;
-  return launch_pdl(k_fp4_gemm, dim3(grid), dim3(NUM_THREADS), smem, s, tm_a, tm_w, ka);
+  return launch_pdl(k_fp4_gemm, dim3(grid), dim3(NUM_THREADS), smem, s, tm_a, tm_w, tm_out, ka);
 }
 
 }  // namespace moe

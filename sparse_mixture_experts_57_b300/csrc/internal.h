@@ -110,10 +110,12 @@ struct GroupedGemm {
 };
 int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s);
 
-// Tiled TMA descriptor (rank 2 or 3) with 128-byte swizzle, zero fill out of bounds.
-// dims and box are innermost first; strides_bytes holds the rank - 1 outer strides.
+// Tiled TMA descriptor (rank 2 or 3), zero fill out of bounds, 128-byte swizzle unless
+// another is given. dims and box are innermost first; strides_bytes holds the rank - 1 outer
+// strides.
 bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base,
-                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 // ------------------------------------------------------------------------------ NVFP4 ----
 // NVFP4 matrix [R, K]: E2M1 codes, two per byte (element 2i in bits 0-3), [R, K/2]; one
