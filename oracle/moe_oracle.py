@@ -30,8 +30,8 @@ Readings where the pages are silent (each is listed in the design doc):
 
 Parity status: the routing, permutation, FFN, combine and LatentMoE functions are pinned
 by the CPU tests in tests/test_oracle_pins.py (brute force, closed forms, invariants,
-special cases). The NVFP4 functions are pinned by exhaustive format tables and error
-bounds.
+special cases). The NVFP4 and FP8 functions are pinned by exhaustive format tables, error
+bounds and brute force.
 """
 from __future__ import annotations
 
@@ -426,3 +426,101 @@ def moe_layer_nvfp4(x, w_router, bias, w_up, w_down, k: int) -> dict:
     y_perm = grouped_ffn_nvfp4(gather_rows(x, p["row_token"]), p["offsets"], w_up, w_down)
     T = np.asarray(x).shape[0]
     return {"y": combine(y_perm, p["slot_row"], r["gates"], T, k), **r, **p}
+
+
+# ----------------------------------------------------------------------------------------
+# FP8 experts ("Nemotron 3 Nano" summary, §4: FP8 post-training quantisation with selective
+# precision; BF16 and FP8 weights are released). The pages give no scaling granularity;
+# the reading here is per-tensor E4M3: one FP32 scale s = amax / 448 per expert matrix, one
+# over the whole routed-token tensor and one over the whole h. Elements q = E4M3(v / s),
+# nearest with ties to even, saturating at +-448; value q * s. Decisions in float32.
+# ----------------------------------------------------------------------------------------
+
+
+def fp8_scale(amax) -> np.float32:
+    """Per-tensor FP32 scale s = amax / 448, so the largest magnitude maps to E4M3's max."""
+    return np.float32(np.float32(amax) / np.float32(E4M3_MAX))
+
+
+def fp8_quantize(mat, s: np.float32 | None = None) -> dict:
+    """Quantise a matrix to E4M3 with one FP32 scale. Returns the E4M3 values q, s and the
+    dequantised matrix q*s. A zero scale gives zero codes."""
+    a32 = np.asarray(_f64(mat), dtype=np.float32)
+    if s is None:
+        s = fp8_scale(np.max(np.abs(a32)) if a32.size else 0.0)
+    s = np.float32(s)
+    if s > 0:
+        with np.errstate(over="ignore"):
+            q = e4m3_round((a32 / s).astype(np.float64))     # float32 division, then rounding
+    else:
+        q = np.zeros(a32.shape)
+    return {"q": q, "s": s, "deq": q * np.float64(s)}
+
+
+def fp8_dequantize(mat, s: np.float32 | None = None) -> np.ndarray:
+    return fp8_quantize(mat, s)["deq"]
+
+
+def grouped_ffn_fp8(x_perm, offsets, w_up, w_down) -> np.ndarray:
+    """The expert FFNs with FP8 operands: per-tensor scales for every expert matrix, for the
+    whole x_perm and for the whole h (all experts); fp64 products of the dequantised values."""
+    xp = _f64(x_perm).astype(np.float32)
+    E = len(offsets) - 1
+    xq = fp8_dequantize(xp)
+    hs = {}
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            hs[e] = np.maximum(xq[a:b] @ fp8_dequantize(w_up[e]).T, 0.0) ** 2
+    h_amax = max((float(np.max(h)) for h in hs.values()), default=0.0)
+    sh = fp8_scale(np.float32(h_amax))
+    out = np.zeros((xp.shape[0], np.asarray(w_down).shape[1]))
+    for e, h in hs.items():
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        out[a:b] = fp8_dequantize(h.astype(np.float32), sh) @ fp8_dequantize(w_down[e]).T
+    return out
+
+
+def moe_layer_fp8(x, w_router, bias, w_up, w_down, k: int) -> dict:
+    """Routed MoE layer with FP8 experts: bf16 routing, FP8 expert FFNs, fp64 combine."""
+    r = route(x, w_router, bias, k)
+    E = np.asarray(w_router).shape[0]
+    p = permute(r["idx"], E)
+    y_perm = grouped_ffn_fp8(gather_rows(x, p["row_token"]), p["offsets"], w_up, w_down)
+    T = np.asarray(x).shape[0]
+    return {"y": combine(y_perm, p["slot_row"], r["gates"], T, k), **r, **p}
+
+
+def fp8_hidden_amax(x, idx, w_up) -> float:
+    """amax of h over every routed (token, expert) pair with FP8 tokens and weights."""
+    xq = fp8_dequantize(_f64(x).astype(np.float32))
+    idx = np.asarray(idx)
+    amax = 0.0
+    for e in np.unique(idx):
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        a = xq[toks] @ fp8_dequantize(w_up[int(e)]).T
+        amax = max(amax, float(np.max(np.maximum(a, 0.0) ** 2)))
+    return amax
+
+
+def moe_tokens_fp8(x_all, x_rows, idx_rows, gates_rows, w_up, w_down, h_amax):
+    """FP8 layer output for a subset of tokens, given the tensor-wide amax of h."""
+    sx = fp8_scale(np.max(np.abs(_f64(x_all).astype(np.float32))))
+    xr = fp8_dequantize(_f64(x_rows).astype(np.float32), sx)
+    sh = fp8_scale(np.float32(h_amax))
+    n, k = np.asarray(idx_rows).shape
+    out = np.zeros((n, np.asarray(w_down).shape[1]))
+    cache: dict[tuple[int, int], np.ndarray] = {}
+
+    def wq(tag, e, w):
+        if (tag, e) not in cache:
+            cache[(tag, e)] = fp8_dequantize(w[e])
+        return cache[(tag, e)]
+
+    for i in range(n):
+        for j in range(k):
+            e = int(idx_rows[i][j])
+            h = np.maximum(xr[i:i + 1] @ wq(0, e, w_up).T, 0.0) ** 2
+            hq = fp8_dequantize(h.astype(np.float32), sh)
+            out[i] += float(gates_rows[i][j]) * (hq @ wq(1, e, w_down).T)[0]
+    return out

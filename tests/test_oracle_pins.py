@@ -413,12 +413,77 @@ def check_nvfp4_layer_paths(o):
     np.testing.assert_allclose(sampled, ref[toks], rtol=1e-10, atol=1e-10)
 
 
+def _brute_fp8(mat, s):
+    """Per-tensor E4M3 quantise-dequantise by table search."""
+    e4_vals = [(m * 2.0 ** -9 if ex == 0 else (1 + m / 8) * 2.0 ** (ex - 7))
+               for code in range(127) for ex, m in [(code >> 3, code & 7)]]
+    a = np.asarray(mat, np.float32)
+    out = np.zeros(a.shape)
+    s = np.float32(s)
+    for idx in np.ndindex(a.shape):
+        if s > 0:
+            v = float(np.float32(a[idx] / s))
+            q = 448.0 if abs(v) > 448 else _nearest_even(abs(v), e4_vals, list(range(127)))
+            out[idx] = np.copysign(q, v) * float(s)
+    return out
+
+
+def check_fp8_quantize(o):
+    rng = np.random.default_rng(24)
+    a = (rng.standard_normal((6, 48)) * np.exp(rng.uniform(-9, 4, (6, 1)))).astype(np.float32)
+    s = o.fp8_scale(np.max(np.abs(a)))
+    assert float(s) == pytest.approx(float(np.abs(a).max()) / 448.0, rel=1e-6)
+    q = o.fp8_quantize(a)
+    np.testing.assert_array_equal(q["deq"], _brute_fp8(a, s))
+    assert np.max(np.abs(q["q"])) == 448.0                # the amax maps to E4M3's maximum
+    # error bound: half an E4M3 step (2^(e-3) in binade e, 2^-9 subnormal spacing) times s
+    v = np.abs(a.astype(np.float64) / float(s))
+    step = np.exp2(np.maximum(np.floor(np.log2(np.maximum(v, 2.0 ** -9))), -6) - 3)
+    assert (np.abs(q["deq"] - a) <= 0.5 * step * float(s) * (1 + 1e-6) + 1e-30).all()
+    assert (o.fp8_quantize(np.zeros((2, 16), np.float32))["deq"] == 0).all()
+
+
+def check_fp8_layer_paths(o):
+    """FP8 grouped FFN, layer, hidden amax and sampled tokens against brute force."""
+    rng = np.random.default_rng(25)
+    T, D, F, E, k = 6, 32, 16, 3, 2
+    x = moe_synth.bf16_bits(rng.standard_normal((T, D)).astype(np.float32))
+    wr = moe_synth.bf16_bits(rng.standard_normal((E, D)).astype(np.float32))
+    bias = np.zeros(E, np.float32)
+    wu = moe_synth.bf16_bits(rng.standard_normal((E, F, D)).astype(np.float32))
+    wd = moe_synth.bf16_bits(rng.standard_normal((E, D, F)).astype(np.float32))
+    r = o.route(x, wr, bias, k)
+    xf = o.widen_bf16(x).astype(np.float32)
+    xq = _brute_fp8(xf, o.fp8_scale(np.max(np.abs(xf))))
+    def wq(w):
+        wf = o.widen_bf16(w).astype(np.float32)
+        return _brute_fp8(wf, o.fp8_scale(np.max(np.abs(wf))))
+    wuq = [wq(wu[e]) for e in range(E)]
+    wdq = [wq(wd[e]) for e in range(E)]
+    pairs = [(t, j, int(r["idx"][t, j])) for t in range(T) for j in range(k)]
+    hs = np.array([[max(math.fsum(xq[t, i] * wuq[e][f, i] for i in range(D)), 0.0) ** 2
+                    for f in range(F)] for t, j, e in pairs])
+    h_amax = float(np.max(hs))
+    assert o.fp8_hidden_amax(x, r["idx"], wu) == pytest.approx(h_amax, rel=1e-12)
+    hq = _brute_fp8(hs.astype(np.float32), o.fp8_scale(np.float32(h_amax)))
+    ref = np.zeros((T, D))
+    for n, (t, j, e) in enumerate(pairs):
+        ref[t] += r["gates"][t, j] * np.array(
+            [math.fsum(hq[n, f] * wdq[e][i, f] for f in range(F)) for i in range(D)])
+    np.testing.assert_allclose(o.moe_layer_fp8(x, wr, bias, wu, wd, k)["y"], ref,
+                               rtol=1e-10, atol=1e-10)
+    toks = np.array([0, 5])
+    got = o.moe_tokens_fp8(x, x[toks], r["idx"][toks], r["gates"][toks], wu, wd, h_amax)
+    np.testing.assert_allclose(got, ref[toks], rtol=1e-10, atol=1e-10)
+
+
 ALL_CHECKS = [check_route_closed_form, check_topk_brute_force, check_layer_brute_force,
               check_ffn_closed_form, check_single_expert_is_dense_ffn, check_identical_experts,
               check_k_equals_E, check_forced_expert, check_gate_and_count_invariants,
               check_latent_identity, check_latent_brute_force, check_combine_weights,
               check_e2m1_table, check_e4m3_table, check_nvfp4_block, check_nvfp4_bounds,
-              check_nvfp4_brute_force, check_grouped_ffn_nvfp4, check_nvfp4_layer_paths]
+              check_nvfp4_brute_force, check_grouped_ffn_nvfp4, check_nvfp4_layer_paths,
+              check_fp8_quantize, check_fp8_layer_paths]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -502,6 +567,10 @@ def _e2m1_ties_away(v):                   # mistake: ties rounded away from zero
     return np.copysign(np.minimum(np.floor(m / q + 0.5) * q, 6.0), v)
 
 
+def _fp8_scale_e2m1_max(amax):            # mistake: NVFP4's element maximum in the FP8 scale
+    return np.float32(np.float32(amax) / np.float32(6.0))
+
+
 _f64 = moe_oracle._f64
 
 MUTANTS = {
@@ -514,6 +583,7 @@ MUTANTS = {
     "combine_unweighted_layer": ({"combine": _combine_no_gates}, check_layer_brute_force),
     "sigmoid_sign": ({"sigmoid": _sigmoid_sign}, check_route_closed_form),
     "e2m1_ties_away": ({"e2m1_round": _e2m1_ties_away}, check_e2m1_table),
+    "fp8_scale_wrong_max": ({"fp8_scale": _fp8_scale_e2m1_max}, check_fp8_quantize),
 }
 
 
