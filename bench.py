@@ -1,7 +1,8 @@
 """Benchmark of the routed MoE layer forward pass on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload nano_decode|nano_prefill|latent|nvfp4_prefill|tiny]
+                    [--workload nano_decode|nano_prefill|latent|nvfp4_prefill|
+                                nano_decode_fp8|nano_prefill_fp8|tiny]
 
 One step = one whole layer forward (route, permute, grouped expert FFN, combine; the
 LatentMoE workload adds its two projections) over one batch of seeded synthetic tokens,
@@ -9,7 +10,8 @@ through the library's C ABI. Prints one JSON line.
 
 The default workload is the Nano-shaped decode layer: 64 tokens, H=2688, 128 experts,
 top-6, F=1856. The NVFP4 prefill workload quantises the expert weights once, untimed, and
-runs moe_forward_nvfp4 (activation quantisation included in every step). Inputs and
+runs moe_forward_nvfp4 (activation quantisation included in every step); the *_fp8
+workloads do the same with per-tensor E4M3 experts (moe_forward_fp8). Inputs and
 weights are resident in HBM before the timed region starts. L2 is
 flushed (a 512 MiB write) before every timed step. Each step is timed with CUDA events on
 the launching stream; the grouped expert FFN, the dominant kernel, is timed the same way.
@@ -45,6 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # Dense FP4 tensor rate relative to BF16 on B300 (nominal 13.5 vs 2.25 PFLOP/s): the FP4
 # peak is the measured BF16 peak times this ratio.
 FP4_OVER_BF16 = 13.5 / 2.25
+FP8_OVER_BF16 = 4.5 / 2.25
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -78,7 +81,7 @@ def layer_algorithmic(w: moe_synth.Workload, counts: np.ndarray) -> dict:
     f_proj = 4.0 * w.T * w.H * w.latent if w.latent else 0.0
     # bf16 weights: 2 bytes per element; NVFP4: half a byte of code plus one E4M3 scale per
     # 16 elements
-    w_bytes = (0.5 + 1.0 / 16) if w.nvfp4 else 2.0
+    w_bytes = (0.5 + 1.0 / 16) if w.nvfp4 else (1.0 if w.fp8 else 2.0)
     b_weights = touched * 2.0 * D * w.F * w_bytes
     b_router = w.E * (D if (w.latent and w.router_on_latent) else w.H) * 2.0
     b_proj = 2.0 * w.H * w.latent * 2 if w.latent else 0.0
@@ -197,6 +200,13 @@ def run_ours(args, w: moe_synth.Workload):
         ws_lat = torch.empty(L.latent_moe_workspace_size(T, H, w.latent, E, k, F,
                                                          int(w.router_on_latent)),
                              dtype=torch.uint8, device=dev)
+    elif w.fp8:
+        # weight quantisation is a set-up step, outside the timed region
+        f8_up = moe.moe_quantize_fp8_weights(d["w_up"])
+        f8_down = moe.moe_quantize_fp8_weights(d["w_down"])
+        del d["w_up"], d["w_down"]
+        ws_fp8 = torch.empty(L.moe_forward_fp8_workspace_size(T, H, E, k, F),
+                             dtype=torch.uint8, device=dev)
     elif w.nvfp4:
         # weight quantisation is a set-up step, outside the timed region
         nv_up = moe.moe_quantize_nvfp4_weights(d["w_up"])
@@ -221,7 +231,19 @@ def run_ours(args, w: moe_synth.Workload):
                                 *nv_down.ptrs(), T, H, E, k, F, P(y), idx_ptr, gates_ptr,
                                 P(ws_fp4), ws_fp4.numel(), sp), "moe_forward_nvfp4")
 
+    def fp8_call(x_ptr, idx_ptr, gates_ptr):
+        chk(L.moe_forward_fp8(x_ptr, P(d["w_router"]), P(d["bias"]), *f8_up.ptrs(),
+                              *f8_down.ptrs(), T, H, E, k, F, P(y), idx_ptr, gates_ptr,
+                              P(ws_fp8), ws_fp8.numel(), sp), "moe_forward_fp8")
+
     def step(e_ffn0=None, e_ffn1=None):
+        if w.fp8:
+            if e_ffn0 is not None:
+                e_ffn0.record(stream)
+            fp8_call(P(d["x"]), P(idx), P(gates))
+            if e_ffn1 is not None:
+                e_ffn1.record(stream)
+            return
         if w.nvfp4:
             if e_ffn0 is not None:
                 e_ffn0.record(stream)
@@ -255,7 +277,7 @@ def run_ours(args, w: moe_synth.Workload):
     # kernels per step: route 2, permutation 2-4, FFN 2, combine 1 (bf16); the latent layer
     # adds its two projections; the NVFP4 layer replaces the gather by amax, padding,
     # two quantisations and the two block-scaled GEMMs
-    launches_per_step = 11 if w.latent else (12 if w.nvfp4 else 9)
+    launches_per_step = 11 if w.latent else (12 if w.nvfp4 else (11 if w.fp8 else 9))
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -316,7 +338,9 @@ def run_ours(args, w: moe_synth.Workload):
         a, b = ev(), ev()
         a.record(stream)
         x_dev.copy_(x_host, non_blocking=True)
-        if w.nvfp4:
+        if w.fp8:
+            fp8_call(P(x_dev), None, None)
+        elif w.nvfp4:
             nvfp4_call(P(x_dev), None, None)
         elif w.latent:
             chk(L.latent_moe(P(x_dev), P(d["w_in"]), P(d["w_out"]), P(d["w_router"]),
@@ -347,9 +371,23 @@ def run_ours(args, w: moe_synth.Workload):
 
     peaks, peak_src = load_peaks()
     alg = layer_algorithmic(w, counts_from_routing(routing, E))
-    launches = 1 if (w.latent or w.nvfp4) else 2   # calls inside the FFN bracket
+    launches = 1 if (w.latent or w.nvfp4 or w.fp8) else 2   # calls inside the FFN bracket
     p_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
-    if w.nvfp4:
+    p_fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
+    t_fp8_flops = alg["flops_experts"] / p_fp8 / 1e12
+    t_fp8_bytes = alg["bytes"] / peaks["hbm_gbs"] / 1e9
+    if w.fp8 and t_fp8_bytes >= t_fp8_flops:
+        # the whole FP8 layer call is bracketed; streaming the E4M3 weights dominates
+        bound = "hbm"
+        achieved = alg["bytes"] / (ffn / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    elif w.fp8:
+        bound = "tensor"
+        achieved = alg["flops_experts"] / (ffn / 1e3) / 1e12
+        peak = p_fp8
+        unit = "TFLOP/s"
+    elif w.nvfp4:
         # the whole NVFP4 layer call is bracketed; its block-scaled GEMMs dominate
         bound = "tensor"
         achieved = alg["flops_experts"] / (ffn / 1e3) / 1e12
@@ -372,8 +410,8 @@ def run_ours(args, w: moe_synth.Workload):
         achieved = alg["ffn_bytes_per_launch"] * launches / (ffn / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
-    if w.nvfp4:
-        t_flops = (alg["flops_experts"] / p_fp4 +
+    if w.nvfp4 or w.fp8:
+        t_flops = (alg["flops_experts"] / (p_fp4 if w.nvfp4 else p_fp8) +
                    (alg["flops_router"] + alg["flops_proj"]) / peaks["bf16_tflops"]) / 1e12
     else:
         t_flops = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
@@ -390,7 +428,8 @@ def run_ours(args, w: moe_synth.Workload):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "nvfp4 experts, bf16 router" if w.nvfp4 else "bf16",
+        "dtype": ("nvfp4 experts, bf16 router" if w.nvfp4 else
+                  "e4m3 experts (per-tensor scales), bf16 router" if w.fp8 else "bf16"),
         "data": "synthetic (seeded, random-init weights of the named shape)",
         "config": {"workload": w.name, "T": T, "H": H, "E": E, "k": k, "F": F,
                    "latent": w.latent or None, "bias": w.bias, "l2": "flushed before every step",
@@ -400,9 +439,13 @@ def run_ours(args, w: moe_synth.Workload):
                      "kernel": ("whole latent layer (tcgen05 GEMMs dominate)" if w.latent
                                 else "whole NVFP4 layer (block-scaled tcgen05 GEMMs dominate)"
                                 if w.nvfp4
+                                else "whole FP8 layer (E4M3 tcgen05 grouped GEMMs dominate)"
+                                if w.fp8
                                 else "grouped expert GEMM (tcgen05), up + down launches"),
                      "peak_source": (f"{peak_src} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16)"
-                                     if w.nvfp4 else peak_src),
+                                     if w.nvfp4 else
+                                     f"{peak_src} bf16 x {FP8_OVER_BF16:g} (nominal FP8/BF16)"
+                                     if (w.fp8 and bound == "tensor") else peak_src),
                      "ffn_ms": ffn, "launches_timed": launches},
         "layer_roofline": {"time_ms": roof_ms, "frac": roof_ms / ms,
                            "tflops": alg["flops"] / (ms / 1e3) / 1e12,
@@ -479,6 +522,10 @@ def _oracle_sample(w, inp, toks):
     if w.nvfp4:
         # the sample's own hidden amax stands in for the tensor-wide one: same per-token work
         return O.moe_tokens_nvfp4(inp["x"], x, r["idx"], r["gates"], inp["w_up"], inp["w_down"])
+    if w.fp8:
+        h_amax = O.fp8_hidden_amax(x, r["idx"], inp["w_up"])     # over the sample
+        return O.moe_tokens_fp8(inp["x"], x, r["idx"], r["gates"], inp["w_up"], inp["w_down"],
+                                h_amax)
     return O.moe_tokens(x, r["idx"], r["gates"], inp["w_up"], inp["w_down"])
 
 
@@ -570,7 +617,7 @@ def main():
         w = dataclasses.replace(w, T=T, E=E, name=f"{w.name}[T={T},E={E}]")
     if args.steps is None:
         # enough steps for about two seconds of timed work (clock samples land inside it)
-        args.steps = {"nano_decode": 2000, "tiny": 2000}.get(w.name, 500) \
+        args.steps = {"nano_decode": 2000, "nano_decode_fp8": 2000, "tiny": 2000}.get(w.name, 500) \
             if args.impl == "ours" else 5
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     out = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)

@@ -242,6 +242,45 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
                       int32_t* topk_idx_out, float* gates_out, void* workspace,
                       size_t workspace_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * FP8 expert FFNs (Nemotron 3 Nano summary §4: FP8 post-training quantisation; BF16 and FP8
+ * weights are released). The pages give no scaling granularity; this library reads it as
+ * per-tensor E4M3: s = amax / 448 and q = E4M3(v / s), nearest with ties to even and
+ * saturating at +-448; the value is q * s. Tensors: each expert matrix, the whole routed
+ * token tensor, and the whole h. Decisions in fp32 with correctly rounded division. The GEMMs
+ * run on tcgen05 kind::f8f6f4 (E4M3 x E4M3, fp32 accumulation); routing, dispatch and the
+ * combine stay bf16/fp32.
+ * Formats: codes [G, N, K] bytes (E4M3), scale [G] fp32 (s of each matrix).
+ * ------------------------------------------------------------------------------------- */
+
+/* moe_quantize_fp8_weights: quantise G bf16 matrices w [G, N, K] (K a multiple of 16; w and
+ * codes 16-byte aligned) into codes and per-matrix scales. A set-up step; no workspace
+ * (scale doubles as the amax accumulator). Asynchronous on `stream`. */
+int moe_quantize_fp8_weights(const uint16_t* w, int G, int N, int K, uint8_t* codes,
+                             float* scale, cudaStream_t stream);
+
+/* moe_grouped_ffn_fp8: moe_grouped_ffn with E4M3 operands. x_perm rows are quantised in the
+ * call with the scale of the whole x_perm; h = max(0, x_q . w_up_q[e]^T)^2 is stored bf16 and
+ * quantised with the scale of the whole h; y_perm = h_q . w_down_q[e]^T (bf16).
+ * Layout: x_perm [rows, H] bf16, offsets [E+1], up codes from [E, F, H], down codes from
+ * [E, H, F], y_perm [rows, H] bf16. Workspace: moe_grouped_ffn_fp8_workspace_size(). */
+size_t moe_grouped_ffn_fp8_workspace_size(int rows, int H, int F, int E);
+int moe_grouped_ffn_fp8(const uint16_t* x_perm, const int32_t* offsets, const uint8_t* up_codes,
+                        const float* up_scale, const uint8_t* down_codes, const float* down_scale,
+                        int rows, int H, int F, int E, uint16_t* y_perm, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/* moe_forward_fp8: the routed MoE layer with FP8 expert FFNs: moe_route, the permutation,
+ * the FP8 FFNs on the routed tokens (quantised straight from x in expert order, with the
+ * scale of the whole x) and moe_combine. Layout as moe_forward. Workspace:
+ * moe_forward_fp8_workspace_size(). */
+size_t moe_forward_fp8_workspace_size(int T, int H, int E, int k, int F);
+int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                    const uint8_t* up_codes, const float* up_scale, const uint8_t* down_codes,
+                    const float* down_scale, int T, int H, int E, int k, int F, uint16_t* y,
+                    int32_t* topk_idx_out, float* gates_out, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,6 +42,7 @@ class Workload:
     latent: int = 0         # l > 0 marks a LatentMoE layer (experts live in R^l)
     router_on_latent: bool = True
     nvfp4: bool = False
+    fp8: bool = False       # per-tensor E4M3 experts
 
     @property
     def D(self) -> int:
@@ -71,6 +72,11 @@ WORKLOADS: dict[str, Workload] = {
     "latent": Workload("latent", T=8192, H=4096, E=_EP, k=_KP, F=1024, seed=3, latent=1024),
     "nvfp4_prefill": Workload("nvfp4_prefill", T=16384, H=2688, E=128, k=6, F=1856, seed=4,
                               bias="zipf", nvfp4=True),
+    # the decode and prefill layers with FP8 experts (same inputs as their bf16 versions)
+    "nano_decode_fp8": Workload("nano_decode_fp8", T=64, H=2688, E=128, k=6, F=1856, seed=1,
+                                fp8=True),
+    "nano_prefill_fp8": Workload("nano_prefill_fp8", T=16384, H=2688, E=128, k=6, F=1856,
+                                 seed=2, bias="zipf", fp8=True),
 }
 
 

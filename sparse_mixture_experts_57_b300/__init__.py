@@ -5,6 +5,7 @@ TMA, warp-level router top-k, deterministic permutation and combine). This packa
 thin Python binding of its C ABI (include/moe.h). Torch supplies device memory and streams.
 """
 from ._binding import (  # noqa: F401
+    Fp8Weights,
     MoeError,
     Nvfp4Weights,
     SIGNATURES,
@@ -14,13 +15,17 @@ from ._binding import (  # noqa: F401
     lib,
     moe_combine,
     moe_forward,
+    moe_forward_fp8,
+    moe_forward_fp8_workspace_size,
     moe_forward_nvfp4,
     moe_forward_nvfp4_workspace_size,
     moe_forward_workspace_size,
     moe_grouped_ffn,
+    moe_grouped_ffn_fp8,
     moe_grouped_ffn_nvfp4,
     moe_linear,
     moe_permute,
+    moe_quantize_fp8_weights,
     moe_quantize_nvfp4_weights,
     moe_route,
     status_string,

@@ -45,6 +45,13 @@ SIGNATURES = {
     "moe_forward_nvfp4_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward_nvfp4": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_quantize_fp8_weights": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP]),
+    "moe_grouped_ffn_fp8_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "moe_grouped_ffn_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _SZ,
+                                 _VP]),
+    "moe_forward_fp8_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP,
+                             _VP, _VP, _SZ, _VP]),
     "latent_moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "latent_moe": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP,
                         _VP, _VP, _SZ, _VP]),
@@ -315,4 +322,70 @@ def moe_forward_nvfp4(x, w_router, bias, w_up: Nvfp4Weights, w_down: Nvfp4Weight
                                *w_down.ptrs(), T, H, E, k, F, _ptr(y), _ptr(topk_idx_out),
                                _ptr(gates_out), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_forward_nvfp4")
+    return y
+
+
+# -------------------------------------------------------------------------------- FP8 ----
+
+class Fp8Weights:
+    """G expert matrices [N, K] quantised to per-tensor E4M3 on the device:
+    codes [G, N, K] uint8 and scale [G] fp32 (include/moe.h)."""
+
+    def __init__(self, codes, scale, G, N, K):
+        self.codes, self.scale = codes, scale
+        self.G, self.N, self.K = G, N, K
+
+    def ptrs(self):
+        return _ptr(self.codes), _ptr(self.scale)
+
+
+def moe_quantize_fp8_weights(w, *, stream=None) -> Fp8Weights:
+    _cuda_tensor(w, torch.bfloat16, "w", 3)
+    G, N, K = w.shape
+    codes = torch.empty((G, N, K), dtype=torch.uint8, device=w.device)
+    scale = torch.empty((G,), dtype=torch.float32, device=w.device)
+    _check(lib().moe_quantize_fp8_weights(_ptr(w), G, N, K, _ptr(codes), _ptr(scale),
+                                          _stream(stream)), "moe_quantize_fp8_weights")
+    return Fp8Weights(codes, scale, G, N, K)
+
+
+def moe_grouped_ffn_fp8(x_perm, offsets, w_up: Fp8Weights, w_down: Fp8Weights, *, out=None,
+                        workspace=None, stream=None):
+    _cuda_tensor(x_perm, torch.bfloat16, "x_perm", 2)
+    _cuda_tensor(offsets, torch.int32, "offsets", 1)
+    rows, H = x_perm.shape
+    E, F = w_up.G, w_up.N
+    if (w_up.K, w_down.G, w_down.N, w_down.K) != (H, E, H, F):
+        raise ValueError("FP8 weight shapes do not match x_perm")
+    y = out if out is not None else torch.empty((rows, H), dtype=torch.bfloat16,
+                                                device=x_perm.device)
+    L = lib()
+    ws = _workspace(L.moe_grouped_ffn_fp8_workspace_size(rows, H, F, E), x_perm.device,
+                    workspace)
+    _check(L.moe_grouped_ffn_fp8(_ptr(x_perm), _ptr(offsets), *w_up.ptrs(), *w_down.ptrs(),
+                                 rows, H, F, E, _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_ffn_fp8")
+    return y
+
+
+def moe_forward_fp8_workspace_size(T, H, E, k, F) -> int:
+    return int(lib().moe_forward_fp8_workspace_size(T, H, E, k, F))
+
+
+def moe_forward_fp8(x, w_router, bias, w_up: Fp8Weights, w_down: Fp8Weights, k: int, *,
+                    out=None, topk_idx_out=None, gates_out=None, workspace=None, stream=None):
+    bf = torch.bfloat16
+    _cuda_tensor(x, bf, "x", 2)
+    _cuda_tensor(w_router, bf, "w_router", 2)
+    _cuda_tensor(bias, torch.float32, "bias", 1)
+    T, H = x.shape
+    E, F = w_up.G, w_up.N
+    if (w_up.K, w_down.G, w_down.N, w_down.K) != (H, E, H, F):
+        raise ValueError("FP8 weight shapes do not match x")
+    y = out if out is not None else torch.empty((T, H), dtype=bf, device=x.device)
+    L = lib()
+    ws = _workspace(L.moe_forward_fp8_workspace_size(T, H, E, k, F), x.device, workspace)
+    _check(L.moe_forward_fp8(_ptr(x), _ptr(w_router), _ptr(bias), *w_up.ptrs(), *w_down.ptrs(),
+                             T, H, E, k, F, _ptr(y), _ptr(topk_idx_out), _ptr(gates_out),
+                             _ptr(ws), ws.numel(), _stream(stream)), "moe_forward_fp8")
     return y

@@ -266,6 +266,72 @@ int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const int3
   return launch_fp4_gemm(d, s);
 }
 
+// FP8 expert FFN buffers (unpadded: the E4M3 GEMM needs no scale atoms).
+struct Fp8Ws {
+  uint32_t* amax;  // [0] activations entering the up-projection, [1] hidden activations
+  uint8_t* xq;
+  uint16_t* h;
+  uint8_t* hq;
+};
+
+Fp8Ws carve_fp8(Carver& c, int rows, int H, int F) {
+  Fp8Ws w;
+  w.amax = c.take<uint32_t>(2);
+  w.xq = c.take<uint8_t>(static_cast<size_t>(rows) * H);
+  w.h = c.take<uint16_t>(static_cast<size_t>(rows) * F);
+  w.hq = c.take<uint8_t>(static_cast<size_t>(rows) * F);
+  return w;
+}
+
+// FP8 expert FFNs. The rows entering the experts are src rows row_token[r] (or r when
+// row_token is null); amax_rows rows of src make up the activation tensor of the scale.
+int ffn_fp8(const uint16_t* src, long long ld, long long amax_rows, const int32_t* row_token,
+            const int32_t* offsets, const uint8_t* up, const float* up_scale, const uint8_t* down,
+            const float* down_scale, int rows, int H, int F, int E, uint16_t* y_perm,
+            const Fp8Ws& w, cudaStream_t s) {
+  MOE_CUDA(cudaMemsetAsync(w.amax, 0, 2 * sizeof(uint32_t), s));
+  int st = launch_amax_bf16(src, amax_rows * ld, 1, w.amax, s);
+  if (st) return st;
+  st = launch_quant_fp8(src, ld, row_token, rows, H, 0, w.amax, w.xq, s);
+  if (st) return st;
+  GroupedGemm g{};
+  g.act = w.xq;
+  g.act_ld = H;
+  g.rows = rows;
+  g.w = up;
+  g.E = E;
+  g.N = F;
+  g.K = H;
+  g.offsets = offsets;
+  g.out = w.h;
+  g.ldo = F;
+  g.epi = EPI_SQRELU_BF16;
+  g.fp8 = 1;
+  g.a_amax = w.amax;
+  g.w_scale = up_scale;
+  g.out_amax = w.amax + 1;
+  st = launch_grouped_gemm(g, s);
+  if (st) return st;
+  st = launch_quant_fp8(w.h, F, nullptr, rows, F, 0, w.amax + 1, w.hq, s);
+  if (st) return st;
+  GroupedGemm d{};
+  d.act = w.hq;
+  d.act_ld = F;
+  d.rows = rows;
+  d.w = down;
+  d.E = E;
+  d.N = H;
+  d.K = F;
+  d.offsets = offsets;
+  d.out = y_perm;
+  d.ldo = H;
+  d.epi = EPI_BF16;
+  d.fp8 = 1;
+  d.a_amax = w.amax + 1;
+  d.w_scale = down_scale;
+  return launch_grouped_gemm(d, s);
+}
+
 bool nvfp4_weights_ok(const uint8_t* codes, const uint8_t* scales, const float* g) {
   return codes && scales && g && aligned16(codes) && aligned16(scales);
 }
@@ -606,6 +672,107 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
   st = ffn_nvfp4(x, H, T, row_token, offsets, {up_codes, up_scales, up_gscale},
                  {down_codes, down_scales, down_gscale}, static_cast<int>(rows), H, F, E, y_perm,
                  w, stream);
+  if (st) return st;
+  return launch_combine(y_perm, static_cast<int>(rows), slot_row, gates, T, H, k, y, stream);
+}
+
+int moe_quantize_fp8_weights(const uint16_t* w, int G, int N, int K, uint8_t* codes,
+                             float* scale, cudaStream_t stream) {
+  if (G < 1 || N < 1 || K < 16) return MOE_ERR_INVALID_ARG;
+  if (!w || !codes || !scale) return MOE_ERR_INVALID_ARG;
+  if (K % 16 || !aligned16(w) || !aligned16(codes)) return MOE_ERR_UNSUPPORTED;
+  // scale first accumulates each matrix's amax (as fp32 bits), then holds amax / 448.
+  MOE_CUDA(cudaMemsetAsync(scale, 0, sizeof(float) * G, stream));
+  uint32_t* amax = reinterpret_cast<uint32_t*>(scale);
+  int st = launch_amax_bf16(w, static_cast<long long>(N) * K, G, amax, stream);
+  if (st) return st;
+  st = launch_quant_fp8(w, K, nullptr, static_cast<long long>(G) * N, K, N, amax, codes, stream);
+  if (st) return st;
+  return launch_finalize_fp8_scale(scale, G, stream);
+}
+
+size_t moe_grouped_ffn_fp8_workspace_size(int rows, int H, int F, int E) {
+  (void)E;
+  if (rows < 0 || H <= 0 || F <= 0) return 0;
+  Carver c(nullptr, 0);
+  carve_fp8(c, rows, H, F);
+  return c.used + 256;
+}
+
+int moe_grouped_ffn_fp8(const uint16_t* x_perm, const int32_t* offsets, const uint8_t* up_codes,
+                        const float* up_scale, const uint8_t* down_codes, const float* down_scale,
+                        int rows, int H, int F, int E, uint16_t* y_perm, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  if (rows < 0 || H <= 0 || F <= 0 || E < 1 || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x_perm || !offsets || !up_codes || !up_scale || !down_codes || !down_scale || !y_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (H % 64 || F % 64 || !aligned16(x_perm) || !aligned16(y_perm) || !aligned16(up_codes) ||
+      !aligned16(down_codes))
+    return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  const Fp8Ws w = carve_fp8(c, rows, H, F);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  return ffn_fp8(x_perm, H, rows, nullptr, offsets, up_codes, up_scale, down_codes, down_scale,
+                 rows, H, F, E, y_perm, w, stream);
+}
+
+size_t moe_forward_fp8_workspace_size(int T, int H, int E, int k, int F) {
+  if (!dims_ok(T, H, E, k) || F <= 0) return 0;
+  Carver c(nullptr, 0);
+  const size_t rows = static_cast<size_t>(T) * k;
+  c.take<float>(static_cast<size_t>(T) * E);
+  c.take<int32_t>(rows);
+  c.take<float>(rows);
+  c.take<uint8_t>(T > 0 ? T : 1);
+  c.take<int32_t>(E);
+  c.take<int32_t>(E + 1);
+  c.take<int32_t>(rows);
+  c.take<int32_t>(rows);
+  c.take<char>(permute_scratch_bytes(T, E));
+  c.take<uint16_t>(rows * H);
+  carve_fp8(c, static_cast<int>(rows), H, F);
+  return c.used + 256;
+}
+
+int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                    const uint8_t* up_codes, const float* up_scale, const uint8_t* down_codes,
+                    const float* down_scale, int T, int H, int E, int k, int F, uint16_t* y,
+                    int32_t* topk_idx_out, float* gates_out, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(T, H, E, k) || F <= 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !bias || !y || !up_codes || !up_scale || !down_codes || !down_scale)
+    return MOE_ERR_INVALID_ARG;
+  if (H % 64 || F % 64 || !aligned16(x) || !aligned16(w_router) || !aligned16(y) ||
+      !aligned16(up_codes) || !aligned16(down_codes))
+    return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  const size_t rows = static_cast<size_t>(T) * k;
+  float* logits = c.take<float>(static_cast<size_t>(T) * E);
+  int32_t* idx = c.take<int32_t>(rows);
+  float* gates = c.take<float>(rows);
+  uint8_t* tie = c.take<uint8_t>(T);
+  int32_t* counts = c.take<int32_t>(E);
+  int32_t* offsets = c.take<int32_t>(E + 1);
+  int32_t* row_token = c.take<int32_t>(rows);
+  int32_t* slot_row = c.take<int32_t>(rows);
+  void* perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
+  uint16_t* y_perm = c.take<uint16_t>(rows * H);
+  const Fp8Ws w = carve_fp8(c, static_cast<int>(rows), H, F);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  if (topk_idx_out) idx = topk_idx_out;
+  if (gates_out) gates = gates_out;
+  int st = router_logits(x, H, w_router, T, H, E, 1, logits, stream);
+  if (st) return st;
+  st = launch_topk(logits, bias, T, E, k, idx, gates, tie, stream);
+  if (st) return st;
+  st = launch_permute(idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, nullptr,
+                      perm_scratch, stream);
+  if (st) return st;
+  // the tokens are quantised straight from x in expert order (row_token), no bf16 x_perm
+  st = ffn_fp8(x, H, T, row_token, offsets, up_codes, up_scale, down_codes, down_scale,
+               static_cast<int>(rows), H, F, E, y_perm, w, stream);
   if (st) return st;
   return launch_combine(y_perm, static_cast<int>(rows), slot_row, gates, T, H, k, y, stream);
 }

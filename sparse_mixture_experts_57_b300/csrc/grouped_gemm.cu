@@ -51,6 +51,9 @@ struct KArgs {
   int epi;
   int kchunk;  // CHUNKED kernels: K-blocks (of 64) accumulated per TMEM partial sum
   int* status;
+  const uint32_t* a_amax;  // E4M3 kernels: activation amax (fp32 bits)
+  const float* w_scale;    // E4M3 kernels: per-group weight scale
+  uint32_t* out_amax;      // max of the stored squared-ReLU outputs, or null
 };
 
 template <int BN>
@@ -164,17 +167,22 @@ __device__ __forceinline__ void store_one(const KArgs& a, long long row, int col
 // sums the partial tiles in fp32 registers. tcgen05's fp32 accumulation error grows about
 // linearly with the number of accumulated products, so short chunks keep the result close
 // to an fp32 dot product. Used for the GEMMs that feed the router's top-k decision.
-template <int BN, int STAGES, bool SWAP, bool CHUNKED = false>
+// F8: E4M3 operands (kind::f8f6f4, K = 32 per MMA): a 128-byte K-slice holds 128 elements,
+// the last slice may run past K (TMA fills zeros), and the epilogue applies the per-tensor
+// scales (a_amax / 448) * w_scale[group].
+template <int BN, int STAGES, bool SWAP, bool CHUNKED = false, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tm_act,
                    const __grid_constant__ CUtensorMap tm_w, const KArgs a) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
+  constexpr int BKE = F8 ? 2 * BK : BK;  // K elements per 128-byte slice
   constexpr int RT = SWAP ? BN : BM;  // routed rows per tile
   constexpr int CT = SWAP ? BM : BN;  // output features per tile
   constexpr uint32_t TMEM_COLS = tmem_cols<BN>();
   constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+  static_assert(!(F8 && CHUNKED), "E4M3 kernels have no chunked variant");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
   static_assert(!CHUNKED || (!SWAP && BN <= 128), "chunked accumulation: rows-as-M, BN <= 128");
 
@@ -260,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int n_ct = (a.N + CT - 1) / CT;
   const int total = s_pref[E] * n_ct;
-  const int KB = a.K / BK;
+  const int KB = (a.K + BKE - 1) / BKE;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
-          const int kc = kb * BK;
+          const int kc = kb * BKE;
           const int kw = a.k_wrap ? (kc % a.k_wrap) : kc;
           if (!SWAP) {
             tma_load_2d(sA + stage * A_BYTES, &tm_act, &full[stage], kc, row0, pol_a);
@@ -330,8 +338,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint64_t adesc = sdesc_k_sw128(smem_u32(sA + stage * A_BYTES));
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(sB + stage * B_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < BK / UK; ++kk)
-            umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kin | kk) != 0);
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            if constexpr (F8)
+              umma_e4m3(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kin | kk) != 0);
+            else
+              umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kin | kk) != 0);
+          }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -358,6 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int m = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    float vmax = 0.f;  // E4M3 squared-ReLU kernels: max of the stored outputs
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, rt, ct;
       decode_tile(tile, n_ct, s_pref, E, e, rt, ct);
@@ -416,6 +429,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_STRIDE;
+      float scale = 1.f;
+      if constexpr (F8) scale = __fdiv_rn(__uint_as_float(*a.a_amax), kFp8Div) * a.w_scale[e];
       if (!SWAP) {
         const int ncols = min(BN, a.N - col0);
         for (int n0 = 0; n0 < ncols; n0 += 16) {
@@ -424,8 +439,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
           float v[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-          if (m < valid_rows) store_row16(a, row0 + m, col0 + n0, v);
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * scale;
+          if (m < valid_rows) {
+            if (F8 && a.out_amax) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float t = fmaxf(v[i], 0.f);
+                vmax = fmaxf(vmax, t * t);
+              }
+            }
+            store_row16(a, row0 + m, col0 + n0, v);
+          }
         }
       } else {
         const int f = col0 + m;
@@ -436,7 +460,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (f < a.N) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              if (n0 + i < valid_rows) store_one(a, row0 + n0 + i, f, __uint_as_float(r[i]));
+              if (n0 + i < valid_rows) {
+                const float v = __uint_as_float(r[i]) * scale;
+                if (F8 && a.out_amax) {
+                  const float t = fmaxf(v, 0.f);
+                  vmax = fmaxf(vmax, t * t);
+                }
+                store_one(a, row0 + n0 + i, f, v);
+              }
           }
         }
       }
@@ -446,6 +477,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
+    }
+    if (F8 && a.out_amax) {
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, d));
+      // squared-ReLU outputs are >= 0: their fp32 bit patterns order like their values
+      if (lane == 0 && vmax > 0.f) atomicMax(a.out_amax, __float_as_uint(vmax));
     }
   }
 
@@ -502,17 +539,32 @@ bool map_3d(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint64_t E
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool SWAP, bool CHUNKED = false>
+template <int BN, int STAGES, bool SWAP, bool CHUNKED = false, bool F8 = false>
 int launch_variant(const GroupedGemm& g, const KArgs& ka, cudaStream_t s) {
   CUtensorMap tm_act, tm_w;
   const int act_box = SWAP ? BN : BM;
   const int w_box = SWAP ? BM : BN;
   const int Kw = g.k_wrap ? g.k_wrap : g.K;
-  if (!map_2d(&tm_act, g.act, g.K, g.rows, g.act_ld, act_box)) return MOE_ERR_CUDA;
-  if (!map_3d(&tm_w, g.w, Kw, g.N, g.E, w_box)) return MOE_ERR_CUDA;
+  if constexpr (F8) {
+    // one byte per element: 128-element K slices
+    const uint64_t ad[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.rows)};
+    const uint64_t as[1] = {static_cast<uint64_t>(g.act_ld)};
+    const uint32_t ab[2] = {2 * BK, static_cast<uint32_t>(act_box)};
+    if (!encode_tmap(&tm_act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.act, ad, as, ab))
+      return MOE_ERR_CUDA;
+    const uint64_t wd[3] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N),
+                            static_cast<uint64_t>(g.E)};
+    const uint64_t ws[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N) * g.K};
+    const uint32_t wb[3] = {2 * BK, static_cast<uint32_t>(w_box), 1};
+    if (!encode_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w, wd, ws, wb))
+      return MOE_ERR_CUDA;
+  } else {
+    if (!map_2d(&tm_act, g.act, g.K, g.rows, g.act_ld, act_box)) return MOE_ERR_CUDA;
+    if (!map_3d(&tm_w, g.w, Kw, g.N, g.E, w_box)) return MOE_ERR_CUDA;
+  }
   constexpr size_t smem = smem_bytes<BN, STAGES>();
   static_assert(smem <= 232448, "shared memory per CTA");
-  auto kern = k_grouped_gemm<BN, STAGES, SWAP, CHUNKED>;
+  auto kern = k_grouped_gemm<BN, STAGES, SWAP, CHUNKED, F8>;
   static int configured_device = -1;
   int dev = 0;
   MOE_CUDA(cudaGetDevice(&dev));
@@ -569,6 +621,8 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   if (g.K % BK || g.N % 16 || (g.k_wrap && (g.k_wrap % BK || g.K % g.k_wrap)) || g.E < 1 ||
       g.E > MAX_GROUPS)
     return MOE_ERR_UNSUPPORTED;
+  if (g.fp8 && (g.k_wrap || g.precise || !g.a_amax || !g.w_scale || g.act_ld % 16))
+    return MOE_ERR_UNSUPPORTED;
   KArgs ka;
   ka.offsets = g.offsets;
   ka.dense_rows = g.rows;
@@ -582,6 +636,9 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   ka.lo_offset = g.lo_offset;
   ka.epi = g.epi;
   ka.kchunk = 4;  // 256-deep partial sums in the chunked variant
+  ka.a_amax = g.a_amax;
+  ka.w_scale = g.w_scale;
+  ka.out_amax = g.epi == EPI_SQRELU_BF16 ? g.out_amax : nullptr;
   ka.status = status_word();
   if (!ka.status) return MOE_ERR_CUDA;
   GroupedGemm gg = g;
@@ -591,6 +648,19 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   // Few rows per group: put the weights on the MMA's M side and the rows on N.
   const double avg_rows = static_cast<double>(g.rows) / gg.E;
   bool swap = g.force_mode == 2 || (g.force_mode == 0 && avg_rows <= 48.0);
+  if (g.fp8) {
+    if (swap) {
+      if (avg_rows <= 16.0) return launch_variant<16, 10, true, false, true>(gg, ka, s);
+      if (avg_rows <= 32.0) return launch_variant<32, 8, true, false, true>(gg, ka, s);
+      return launch_variant<64, 8, true, false, true>(gg, ka, s);
+    }
+    switch (pick_bn_rows_as_m(g.N)) {
+      case 256: return launch_variant<256, 4, false, false, true>(gg, ka, s);
+      case 224: return launch_variant<224, 4, false, false, true>(gg, ka, s);
+      case 192: return launch_variant<192, 5, false, false, true>(gg, ka, s);
+      default: return launch_variant<128, 6, false, false, true>(gg, ka, s);
+    }
+  }
   if (swap) {
     if (avg_rows <= 16.0) return launch_variant<16, 10, true>(gg, ka, s);
     if (avg_rows <= 32.0) return launch_variant<32, 8, true>(gg, ka, s);

@@ -107,6 +107,13 @@ struct GroupedGemm {
   int epi;
   int force_mode;        // 0 auto, 1 rows-as-M, 2 weights-as-M (swap)
   int precise;           // 1: fp32 partial sums every 256 of K (for routing inputs)
+  // E4M3 operands (act and w hold one byte per element): the epilogue multiplies by
+  // (a_amax / 448) * w_scale[e]; with EPI_SQRELU_BF16, out_amax (if set) receives the max
+  // of the stored values (fp32 bits).
+  int fp8 = 0;
+  const uint32_t* a_amax = nullptr;
+  const float* w_scale = nullptr;
+  uint32_t* out_amax = nullptr;
 };
 int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s);
 
@@ -148,6 +155,18 @@ int launch_quant_act(const uint16_t* src, long long ld, long long src_rows,
                      const int32_t* row_token, const int32_t* offsets, const int32_t* poff,
                      int E, int K, int P_max, const uint32_t* amax, uint8_t* codes, uint8_t* sf,
                      cudaStream_t s);
+
+// ------------------------------------------------------------------------------- FP8 ----
+// Per-tensor E4M3: s = amax / 448, q = E4M3(v / s). Codes are one byte per element.
+constexpr float kFp8Div = 448.0f;
+// Quantise rows of src (bf16, row stride ld) into out [rows, K] E4M3 bytes. Row r reads src
+// row row_map[r] when row_map is set, else row r. Matrix r / rows_per_scale uses the scale
+// of amax[r / rows_per_scale] (rows_per_scale = 0: one scale for all rows).
+int launch_quant_fp8(const uint16_t* src, long long ld, const int32_t* row_map, long long rows,
+                     int K, long long rows_per_scale, const uint32_t* amax, uint8_t* out,
+                     cudaStream_t s);
+// s[i] = amax[i] / 448 in place.
+int launch_finalize_fp8_scale(float* s, int G, cudaStream_t stream);
 
 struct Fp4Gemm {
   const uint8_t* a_codes;  // [P, K/2], rows padded per group (poff)
