@@ -263,6 +263,35 @@ def latent_moe(x, w_in, w_out, w_router, bias, w_up, w_down, kp: int,
 
 
 # ----------------------------------------------------------------------------------------
+# Shared expert ([N3] §2.2: the shared-expert computation, like the routing gate, stays in
+# the hidden size H). Reading: an FFN of the routed experts' form (up, squared ReLU, down)
+# applied to every token with weight 1 and added to the routed output. Several shared
+# experts of width F_s sum to one FFN whose intermediate width is their total.
+# ----------------------------------------------------------------------------------------
+
+
+def shared_ffn(x, w_up_s, w_down_s) -> np.ndarray:
+    """max(0, x @ W_up_s^T)^2 @ W_down_s^T for every token (W_up_s [F_s, H], W_down_s [H, F_s])."""
+    return expert_ffn(x, w_up_s, w_down_s)
+
+
+def moe_layer_shared(x, w_router, bias, w_up, w_down, w_up_s, w_down_s, k: int) -> dict:
+    """Routed MoE layer plus the shared expert: y = routed(x) + shared(x)."""
+    out = moe_layer(x, w_router, bias, w_up, w_down, k)
+    out["y_routed"] = out["y"]
+    out["y"] = out["y"] + shared_ffn(x, w_up_s, w_down_s)
+    return out
+
+
+def latent_moe_shared(x, w_in, w_out, w_router, bias, w_up, w_down, w_up_s, w_down_s, kp: int,
+                      router_on_latent: bool = True) -> dict:
+    """LatentMoE plus a shared expert in H: y = W_out(latent routed(x)) + shared(x)."""
+    out = latent_moe(x, w_in, w_out, w_router, bias, w_up, w_down, kp, router_on_latent)
+    out["y"] = out["y"] + shared_ffn(x, w_up_s, w_down_s)
+    return out
+
+
+# ----------------------------------------------------------------------------------------
 # NVFP4 ([N3] §2.4): E2M1 elements, one E4M3 scale per 16-element micro-block, and a
 # second-level FP32 per-tensor scale. Blocks run along the contraction (K) axis.
 # Scale and code decisions are made in float32, the precision the pages give to the

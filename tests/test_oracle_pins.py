@@ -477,13 +477,51 @@ def check_fp8_layer_paths(o):
     np.testing.assert_allclose(got, ref[toks], rtol=1e-10, atol=1e-10)
 
 
+def check_shared_expert(o):
+    """Shared expert: brute force, a zero shared expert changes nothing, and with one routed
+    expert (k = 1) equal to the shared one the layer is twice the dense FFN."""
+    rng = np.random.default_rng(26)
+    T, H, E, k, F, Fs = 5, 16, 3, 2, 8, 12
+    x = moe_synth.bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wr = moe_synth.bf16_bits(rng.standard_normal((E, H)).astype(np.float32))
+    bias = np.zeros(E, np.float32)
+    wu = moe_synth.bf16_bits(rng.standard_normal((E, F, H)).astype(np.float32) * 0.3)
+    wd = moe_synth.bf16_bits(rng.standard_normal((E, H, F)).astype(np.float32) * 0.3)
+    wus = moe_synth.bf16_bits(rng.standard_normal((Fs, H)).astype(np.float32) * 0.3)
+    wds = moe_synth.bf16_bits(rng.standard_normal((H, Fs)).astype(np.float32) * 0.3)
+    xf, wusf, wdsf = o.widen_bf16(x), o.widen_bf16(wus), o.widen_bf16(wds)
+    sh = np.array([[math.fsum(max(math.fsum(xf[t, i] * wusf[f, i] for i in range(H)), 0.0) ** 2
+                              * wdsf[j, f] for f in range(Fs)) for j in range(H)]
+                   for t in range(T)])
+    np.testing.assert_allclose(o.shared_ffn(x, wus, wds), sh, rtol=1e-12, atol=1e-12)
+    base = o.moe_layer(x, wr, bias, wu, wd, k)["y"]
+    got = o.moe_layer_shared(x, wr, bias, wu, wd, wus, wds, k)["y"]
+    np.testing.assert_allclose(got, base + sh, rtol=1e-12, atol=1e-12)
+    z = np.zeros_like(wus)
+    np.testing.assert_array_equal(o.moe_layer_shared(x, wr, bias, wu, wd, z, z.T.copy(), k)["y"],
+                                  base)
+    one = o.moe_layer_shared(x, wr[:1], bias[:1], wus[None], wds[None], wus, wds, 1)["y"]
+    np.testing.assert_allclose(one, 2 * sh, rtol=1e-12, atol=1e-12)
+    # LatentMoE: the shared expert is added in H, after the projection back
+    L = 8
+    w_in = moe_synth.bf16_bits(rng.standard_normal((L, H)).astype(np.float32) * 0.3)
+    w_out = moe_synth.bf16_bits(rng.standard_normal((H, L)).astype(np.float32) * 0.3)
+    wrl = moe_synth.bf16_bits(rng.standard_normal((E, L)).astype(np.float32))
+    wul = moe_synth.bf16_bits(rng.standard_normal((E, F, L)).astype(np.float32) * 0.3)
+    wdl = moe_synth.bf16_bits(rng.standard_normal((E, L, F)).astype(np.float32) * 0.3)
+    lat = o.latent_moe(x, w_in, w_out, wrl, bias, wul, wdl, k)["y"]
+    np.testing.assert_allclose(
+        o.latent_moe_shared(x, w_in, w_out, wrl, bias, wul, wdl, wus, wds, k)["y"], lat + sh,
+        rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = [check_route_closed_form, check_topk_brute_force, check_layer_brute_force,
               check_ffn_closed_form, check_single_expert_is_dense_ffn, check_identical_experts,
               check_k_equals_E, check_forced_expert, check_gate_and_count_invariants,
               check_latent_identity, check_latent_brute_force, check_combine_weights,
               check_e2m1_table, check_e4m3_table, check_nvfp4_block, check_nvfp4_bounds,
               check_nvfp4_brute_force, check_grouped_ffn_nvfp4, check_nvfp4_layer_paths,
-              check_fp8_quantize, check_fp8_layer_paths]
+              check_fp8_quantize, check_fp8_layer_paths, check_shared_expert]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
