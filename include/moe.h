@@ -186,6 +186,33 @@ int latent_moe(const uint16_t* x, const uint16_t* w_in, const uint16_t* w_out,
                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Shared expert (NVIDIA Nemotron 3 notes §2.2: the shared-expert computation, like the routing
+ * gate, stays in the hidden size H). This library's reading: an FFN of the routed experts'
+ * form applied to every token with weight 1 and added to the routed output,
+ *   y = routed(x) + max(0, x . w_up_shared^T)^2 . w_down_shared^T,
+ * with w_up_shared [Fs, H] and w_down_shared [H, Fs] bf16. Several shared experts are one
+ * FFN whose intermediate size Fs is their total (stack their matrices along Fs).
+ * moe_forward_shared: moe_forward plus the shared expert (its output joins the combine's fp32
+ *   sum). latent_moe_shared: latent_moe plus the shared expert on x in H (added in the
+ *   epilogue of the L -> H projection). Fs must be a multiple of 64. Workspace: the
+ *   matching *_workspace_size().
+ * ------------------------------------------------------------------------------------- */
+size_t moe_forward_shared_workspace_size(int T, int H, int E, int k, int F, int Fs);
+int moe_forward_shared(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                       const uint16_t* w_up, const uint16_t* w_down, const uint16_t* w_up_shared,
+                       const uint16_t* w_down_shared, int T, int H, int E, int k, int F, int Fs,
+                       uint16_t* y, int32_t* topk_idx_out, float* gates_out, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+size_t latent_moe_shared_workspace_size(int T, int H, int L, int Ep, int kp, int F, int Fs,
+                                        int router_on_latent);
+int latent_moe_shared(const uint16_t* x, const uint16_t* w_in, const uint16_t* w_out,
+                      const uint16_t* w_router, const float* bias, int router_on_latent,
+                      const uint16_t* w_up, const uint16_t* w_down, const uint16_t* w_up_shared,
+                      const uint16_t* w_down_shared, int T, int H, int L, int Ep, int kp, int F,
+                      int Fs, uint16_t* y, int32_t* topk_idx_out, float* gates_out,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * NVFP4 expert FFNs (NVIDIA Nemotron 3 notes §2.4: E2M1 elements in 16-element micro-blocks,
  * an E4M3 scale per block, a second-level FP32 scale per tensor). For a tensor with
  * amax A the global scale is g = A / (6 * 448); each block of 16 consecutive K elements gets

@@ -26,7 +26,8 @@ import numpy as np
 # 发布了Nemotron 3" (混合Mamba Transformer MoE架构: a learned router picks 6 of 128).
 # ----------------------------------------------------------------------------------------
 
-TAG_X, TAG_ROUTER, TAG_BIAS, TAG_UP, TAG_DOWN, TAG_WIN, TAG_WOUT = range(1, 8)
+TAG_X, TAG_ROUTER, TAG_BIAS, TAG_UP, TAG_DOWN, TAG_WIN, TAG_WOUT, TAG_UP_S, TAG_DOWN_S = \
+    range(1, 10)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -168,6 +169,13 @@ def layer_inputs(w: Workload, experts=None, with_experts: bool = True) -> dict:
         out["w_up"] = expert_stack(w.seed, TAG_UP, w.E, w.F, D, experts)
         out["w_down"] = expert_stack(w.seed, TAG_DOWN, w.E, D, w.F, experts)
     return out
+
+
+def shared_expert_inputs(w: Workload, Fs: int) -> dict:
+    """Weights of one shared expert in H: w_up_shared [Fs, H] ~ N(0, 1/H) and
+    w_down_shared [H, Fs] ~ N(0, 1/Fs), bfloat16 bits."""
+    return {"w_up_shared": normal_bf16(w.seed, TAG_UP_S, (Fs, w.H), 1.0 / math.sqrt(w.H)),
+            "w_down_shared": normal_bf16(w.seed, TAG_DOWN_S, (w.H, Fs), 1.0 / math.sqrt(Fs))}
 
 
 def random_topk(seed: int, T: int, E: int, k: int, skew: float = 0.0) -> np.ndarray:

@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     SIGNATURES,
     get_device_status,
     latent_moe,
+    latent_moe_shared,
     latent_moe_workspace_size,
     lib,
     moe_combine,
@@ -19,6 +20,7 @@ from ._binding import (  # noqa: F401
     moe_forward_fp8_workspace_size,
     moe_forward_nvfp4,
     moe_forward_nvfp4_workspace_size,
+    moe_forward_shared,
     moe_forward_workspace_size,
     moe_grouped_ffn,
     moe_grouped_ffn_fp8,

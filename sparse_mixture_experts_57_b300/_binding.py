@@ -52,6 +52,12 @@ SIGNATURES = {
     "moe_forward_fp8_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP,
                              _VP, _VP, _SZ, _VP]),
+    "moe_forward_shared_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_forward_shared": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP,
+                                _VP, _VP, _VP, _SZ, _VP]),
+    "latent_moe_shared_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "latent_moe_shared": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
+                               _I, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "latent_moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "latent_moe": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP,
                         _VP, _VP, _SZ, _VP]),
@@ -388,4 +394,53 @@ def moe_forward_fp8(x, w_router, bias, w_up: Fp8Weights, w_down: Fp8Weights, k: 
     _check(L.moe_forward_fp8(_ptr(x), _ptr(w_router), _ptr(bias), *w_up.ptrs(), *w_down.ptrs(),
                              T, H, E, k, F, _ptr(y), _ptr(topk_idx_out), _ptr(gates_out),
                              _ptr(ws), ws.numel(), _stream(stream)), "moe_forward_fp8")
+    return y
+
+
+# ---------------------------------------------------------------------- shared expert ----
+
+def moe_forward_shared(x, w_router, bias, w_up, w_down, w_up_shared, w_down_shared, k: int, *,
+                       out=None, topk_idx_out=None, gates_out=None, workspace=None, stream=None):
+    bf = torch.bfloat16
+    for t, n, d in ((x, "x", 2), (w_router, "w_router", 2), (w_up, "w_up", 3),
+                    (w_down, "w_down", 3), (w_up_shared, "w_up_shared", 2),
+                    (w_down_shared, "w_down_shared", 2)):
+        _cuda_tensor(t, bf, n, d)
+    _cuda_tensor(bias, torch.float32, "bias", 1)
+    T, H = x.shape
+    E, F, _ = w_up.shape
+    Fs = w_up_shared.shape[0]
+    y = out if out is not None else torch.empty((T, H), dtype=bf, device=x.device)
+    L = lib()
+    ws = _workspace(L.moe_forward_shared_workspace_size(T, H, E, k, F, Fs), x.device, workspace)
+    _check(L.moe_forward_shared(_ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_up), _ptr(w_down),
+                                _ptr(w_up_shared), _ptr(w_down_shared), T, H, E, k, F, Fs,
+                                _ptr(y), _ptr(topk_idx_out), _ptr(gates_out), _ptr(ws),
+                                ws.numel(), _stream(stream)), "moe_forward_shared")
+    return y
+
+
+def latent_moe_shared(x, w_in, w_out, w_router, bias, w_up, w_down, w_up_shared, w_down_shared,
+                      kp: int, *, router_on_latent: bool = True, out=None, topk_idx_out=None,
+                      gates_out=None, workspace=None, stream=None):
+    bf = torch.bfloat16
+    for t, n, d in ((x, "x", 2), (w_in, "w_in", 2), (w_out, "w_out", 2),
+                    (w_router, "w_router", 2), (w_up, "w_up", 3), (w_down, "w_down", 3),
+                    (w_up_shared, "w_up_shared", 2), (w_down_shared, "w_down_shared", 2)):
+        _cuda_tensor(t, bf, n, d)
+    _cuda_tensor(bias, torch.float32, "bias", 1)
+    T, H = x.shape
+    Lat = w_in.shape[0]
+    Ep, F, _ = w_up.shape
+    Fs = w_up_shared.shape[0]
+    y = out if out is not None else torch.empty((T, H), dtype=bf, device=x.device)
+    L = lib()
+    ws = _workspace(L.latent_moe_shared_workspace_size(T, H, Lat, Ep, kp, F, Fs,
+                                                       int(router_on_latent)), x.device,
+                    workspace)
+    _check(L.latent_moe_shared(_ptr(x), _ptr(w_in), _ptr(w_out), _ptr(w_router), _ptr(bias),
+                               int(router_on_latent), _ptr(w_up), _ptr(w_down), _ptr(w_up_shared),
+                               _ptr(w_down_shared), T, H, Lat, Ep, kp, F, Fs, _ptr(y),
+                               _ptr(topk_idx_out), _ptr(gates_out), _ptr(ws), ws.numel(),
+                               _stream(stream)), "latent_moe_shared")
     return y

@@ -155,7 +155,8 @@ int ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_up,
 int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int Dr, int parts,
           const uint16_t* w_router, const float* bias, const uint16_t* w_up,
           const uint16_t* w_down, int T, int D, int E, int k, int F, uint16_t* y,
-          int32_t* idx_out, float* gates_out, const LayerWs& w, cudaStream_t s) {
+          int32_t* idx_out, float* gates_out, const LayerWs& w, cudaStream_t s,
+          const uint16_t* addend = nullptr) {
   int st = router_logits(xr, ldr, w_router, T, Dr, E, parts, w.logits, s);
   if (st) return st;
   int32_t* idx = idx_out ? idx_out : w.idx;
@@ -168,7 +169,39 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
   const int rows = T * k;
   st = ffn(w.x_perm, w.offsets, w_up, w_down, rows, D, F, E, w.h, w.y_perm, s);
   if (st) return st;
-  return launch_combine(w.y_perm, rows, w.slot_row, gates, T, D, k, y, s);
+  return launch_combine(w.y_perm, rows, w.slot_row, gates, T, D, k, y, s, addend);
+}
+
+// The shared expert on every token: h_s = max(0, x . w_up_s^T)^2, then
+// out = h_s . w_down_s^T (+ add when given: EPI_ADD_BF16 with add [T, N_out] bf16).
+int shared_expert(const uint16_t* x, int64_t ldx, int T, int H, int Fs, const uint16_t* w_up_s,
+                  const uint16_t* w_down_s, uint16_t* h_s, uint16_t* out,
+                  cudaStream_t s) {
+  GroupedGemm up{};
+  up.act = x;
+  up.act_ld = ldx;
+  up.rows = T;
+  up.w = w_up_s;
+  up.E = 1;
+  up.N = Fs;
+  up.K = H;
+  up.out = h_s;
+  up.ldo = Fs;
+  up.epi = EPI_SQRELU_BF16;
+  int st = launch_grouped_gemm(up, s);
+  if (st) return st;
+  GroupedGemm dn{};
+  dn.act = h_s;
+  dn.act_ld = Fs;
+  dn.rows = T;
+  dn.w = w_down_s;
+  dn.E = 1;
+  dn.N = H;
+  dn.K = Fs;
+  dn.out = out;
+  dn.ldo = H;
+  dn.epi = EPI_BF16;
+  return launch_grouped_gemm(dn, s);
 }
 
 // NVFP4 expert FFN buffers. P bounds the padded rows: every group rounded up to whole
@@ -775,6 +808,113 @@ int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bi
                static_cast<int>(rows), H, F, E, y_perm, w, stream);
   if (st) return st;
   return launch_combine(y_perm, static_cast<int>(rows), slot_row, gates, T, H, k, y, stream);
+}
+
+size_t moe_forward_shared_workspace_size(int T, int H, int E, int k, int F, int Fs) {
+  if (!dims_ok(T, H, E, k) || F <= 0 || Fs <= 0) return 0;
+  Carver c(nullptr, 0);
+  carve_layer(c, T, H, E, k, F);
+  c.take<uint16_t>(static_cast<size_t>(T) * Fs);  // h of the shared expert
+  c.take<uint16_t>(static_cast<size_t>(T) * H);   // its output
+  return c.used + 256;
+}
+
+int moe_forward_shared(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                       const uint16_t* w_up, const uint16_t* w_down, const uint16_t* w_up_shared,
+                       const uint16_t* w_down_shared, int T, int H, int E, int k, int F, int Fs,
+                       uint16_t* y, int32_t* topk_idx_out, float* gates_out, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(T, H, E, k) || F <= 0 || Fs <= 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !bias || !w_up || !w_down || !w_up_shared || !w_down_shared || !y)
+    return MOE_ERR_INVALID_ARG;
+  if (H % 64 || F % 64 || Fs % 64 || !aligned16(x) || !aligned16(w_router) || !aligned16(w_up) ||
+      !aligned16(w_down) || !aligned16(w_up_shared) || !aligned16(w_down_shared) || !aligned16(y))
+    return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  const LayerWs w = carve_layer(c, T, H, E, k, F);
+  uint16_t* h_s = c.take<uint16_t>(static_cast<size_t>(T) * Fs);
+  uint16_t* y_s = c.take<uint16_t>(static_cast<size_t>(T) * H);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  int st = shared_expert(x, H, T, H, Fs, w_up_shared, w_down_shared, h_s, y_s, stream);
+  if (st) return st;
+  // the combine adds the shared expert's output into its fp32 sum
+  return layer(x, H, x, H, H, 1, w_router, bias, w_up, w_down, T, H, E, k, F, y, topk_idx_out,
+               gates_out, w, stream, y_s);
+}
+
+size_t latent_moe_shared_workspace_size(int T, int H, int L, int Ep, int kp, int F, int Fs,
+                                        int router_on_latent) {
+  const size_t base = latent_moe_workspace_size(T, H, L, Ep, kp, F, router_on_latent);
+  if (!base || Fs <= 0) return 0;
+  return base + align_up(static_cast<size_t>(T) * Fs * 2, 256) +
+         align_up(static_cast<size_t>(T) * H * 2, 256) + 512;
+}
+
+int latent_moe_shared(const uint16_t* x, const uint16_t* w_in, const uint16_t* w_out,
+                      const uint16_t* w_router, const float* bias, int router_on_latent,
+                      const uint16_t* w_up, const uint16_t* w_down, const uint16_t* w_up_shared,
+                      const uint16_t* w_down_shared, int T, int H, int L, int Ep, int kp, int F,
+                      int Fs, uint16_t* y, int32_t* topk_idx_out, float* gates_out,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(T, L, Ep, kp) || H <= 0 || F <= 0 || Fs <= 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_in || !w_out || !w_router || !bias || !w_up || !w_down || !w_up_shared ||
+      !w_down_shared || !y)
+    return MOE_ERR_INVALID_ARG;
+  if (H % 64 || L % 64 || F % 64 || Fs % 64 || !aligned16(x) || !aligned16(w_in) ||
+      !aligned16(w_out) || !aligned16(w_router) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(w_up_shared) || !aligned16(w_down_shared) || !aligned16(y))
+    return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  const int lat_ld = router_on_latent ? 3 * L : L;
+  uint16_t* x_lat = c.take<uint16_t>(static_cast<size_t>(T) * lat_ld);
+  uint16_t* y_lat = c.take<uint16_t>(static_cast<size_t>(T) * L);
+  const LayerWs w = carve_layer(c, T, L, Ep, kp, F);
+  uint16_t* h_s = c.take<uint16_t>(static_cast<size_t>(T) * Fs);
+  uint16_t* y_s = c.take<uint16_t>(static_cast<size_t>(T) * H);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+
+  // shared expert in H on the token itself (Nemotron 3 notes §2.2)
+  int st = shared_expert(x, H, T, H, Fs, w_up_shared, w_down_shared, h_s, y_s, stream);
+  if (st) return st;
+  GroupedGemm g{};
+  g.act = x;
+  g.act_ld = H;
+  g.rows = T;
+  g.w = w_in;
+  g.E = 1;
+  g.N = L;
+  g.K = H;
+  g.out = x_lat;
+  g.ldo = lat_ld;
+  g.lo_offset = L;
+  g.epi = router_on_latent ? EPI_SPLIT_BF16 : EPI_BF16;
+  g.precise = router_on_latent;
+  st = launch_grouped_gemm(g, stream);
+  if (st) return st;
+  if (router_on_latent)
+    st = layer(x_lat, lat_ld, x_lat, lat_ld, L, 3, w_router, bias, w_up, w_down, T, L, Ep, kp, F,
+               y_lat, topk_idx_out, gates_out, w, stream);
+  else
+    st = layer(x_lat, lat_ld, x, H, H, 1, w_router, bias, w_up, w_down, T, L, Ep, kp, F, y_lat,
+               topk_idx_out, gates_out, w, stream);
+  if (st) return st;
+  // y = y_lat . w_out^T + shared expert output (added in the GEMM's fp32 epilogue)
+  GroupedGemm o{};
+  o.act = y_lat;
+  o.act_ld = L;
+  o.rows = T;
+  o.w = w_out;
+  o.E = 1;
+  o.N = H;
+  o.K = L;
+  o.out = y;
+  o.ldo = H;
+  o.epi = EPI_ADD_BF16;
+  o.add = y_s;
+  o.ld_add = H;
+  return launch_grouped_gemm(o, stream);
 }
 
 }  // extern "C"

@@ -2,7 +2,8 @@
 //
 // "Nemotron 3 Nano" summary (shd-paper.top), 技术框架: a combination layer forms the
 // weighted combination of the chosen experts' outputs.
-//   y[t, :] = sum_j gates[t, j] * y_perm[slot_row[t, j], :]
+//   y[t, :] = addend[t, :] + sum_j gates[t, j] * y_perm[slot_row[t, j], :]
+// (addend: the shared expert's output, or nothing)
 // Deterministic (no atomics), fp32 accumulation, 16-byte loads and stores.
 #include <cuda_bf16.h>
 
@@ -29,7 +30,8 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 // back to back, so even a 64-token decode batch keeps thousands of loads in flight.
 __global__ void k_combine(const uint16_t* __restrict__ y_perm, int rows,
                           const int32_t* __restrict__ slot_row, const float* __restrict__ gates,
-                          int T, int H, int k, uint16_t* __restrict__ y) {
+                          int T, int H, int k, const uint16_t* __restrict__ addend,
+                          uint16_t* __restrict__ y) {
   griddep_wait();
   griddep_launch_dependents();
   const int nvec = H / 8;
@@ -40,6 +42,8 @@ __global__ void k_combine(const uint16_t* __restrict__ y_perm, int rows,
   const int32_t* sr = slot_row + t * k;
   const float* gg = gates + t * k;
   float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (addend)  // the shared expert's output joins the fp32 sum
+    acc8(a, __ldg(reinterpret_cast<const uint4*>(addend + t * H) + v), 1.f);
 #pragma unroll 4
   for (int j = 0; j < k; ++j) {
     const int r = __ldg(sr + j);
@@ -56,12 +60,12 @@ __global__ void k_combine(const uint16_t* __restrict__ y_perm, int rows,
 }  // namespace
 
 int launch_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row, const float* gates,
-                   int T, int H, int k, uint16_t* y, cudaStream_t s) {
+                   int T, int H, int k, uint16_t* y, cudaStream_t s, const uint16_t* addend) {
   if (T <= 0) return MOE_OK;
   const int threads = 256;
   const long long n = static_cast<long long>(T) * (H / 8);
   return launch_pdl(k_combine, dim3(static_cast<unsigned>((n + threads - 1) / threads)),
-                    dim3(threads), 0, s, y_perm, rows, slot_row, gates, T, H, k, y);
+                    dim3(threads), 0, s, y_perm, rows, slot_row, gates, T, H, k, addend, y);
 }
 
 }  // namespace moe

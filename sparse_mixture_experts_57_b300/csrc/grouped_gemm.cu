@@ -51,6 +51,8 @@ struct KArgs {
   int epi;
   int kchunk;  // CHUNKED kernels: K-blocks (of 64) accumulated per TMEM partial sum
   int* status;
+  const uint16_t* add;     // EPI_ADD_BF16: bf16 addend, row stride ld_add
+  long long ld_add;
   const uint32_t* a_amax;  // E4M3 kernels: activation amax (fp32 bits)
   const float* w_scale;    // E4M3 kernels: per-group weight scale
   uint32_t* out_amax;      // max of the stored squared-ReLU outputs, or null
@@ -111,6 +113,19 @@ __device__ __forceinline__ void store_row16(const KArgs& a, long long row, int c
       v[i] = t * t;
     }
   }
+  if (a.epi == EPI_ADD_BF16) {
+    const uint4* ap = reinterpret_cast<const uint4*>(a.add + row * a.ld_add + col);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 u = __ldg(ap + h);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * h + 2 * i] += __uint_as_float(w[i] << 16);
+        v[8 * h + 2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+      }
+    }
+  }
   uint32_t hi[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) hi[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
@@ -152,6 +167,7 @@ __device__ __forceinline__ void store_one(const KArgs& a, long long row, int col
     const float t = fmaxf(v, 0.f);
     v = t * t;
   }
+  if (a.epi == EPI_ADD_BF16) v += __uint_as_float(static_cast<uint32_t>(a.add[row * a.ld_add + col]) << 16);
   __nv_bfloat16* base = static_cast<__nv_bfloat16*>(a.out) + row * a.ldo + col;
   const __nv_bfloat16 h = __float2bfloat16_rn(v);
   *base = h;
@@ -623,6 +639,7 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
     return MOE_ERR_UNSUPPORTED;
   if (g.fp8 && (g.k_wrap || g.precise || !g.a_amax || !g.w_scale || g.act_ld % 16))
     return MOE_ERR_UNSUPPORTED;
+  if (g.epi == EPI_ADD_BF16 && (!g.add || g.ld_add % 8 || g.precise)) return MOE_ERR_UNSUPPORTED;
   KArgs ka;
   ka.offsets = g.offsets;
   ka.dense_rows = g.rows;
@@ -636,6 +653,8 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   ka.lo_offset = g.lo_offset;
   ka.epi = g.epi;
   ka.kchunk = 4;  // 256-deep partial sums in the chunked variant
+  ka.add = g.add;
+  ka.ld_add = g.ld_add;
   ka.a_amax = g.a_amax;
   ka.w_scale = g.w_scale;
   ka.out_amax = g.epi == EPI_SQRELU_BF16 ? g.out_amax : nullptr;

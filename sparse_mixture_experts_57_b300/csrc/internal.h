@@ -86,6 +86,7 @@ enum Epilogue : int {
   EPI_F32 = 2,          // out = acc (fp32)
   EPI_SPLIT_BF16 = 3,   // acc = hi + mid + lo, three bf16 planes at out, out + lo_offset,
                         // out + 2 * lo_offset (about fp32 accuracy for the router input)
+  EPI_ADD_BF16 = 4,     // out = bf16(acc + add[row, col]) (add: bf16, row stride ld_add)
 };
 
 // One grouped GEMM: for every group e and every row r in [offsets[e], offsets[e+1]):
@@ -110,6 +111,8 @@ struct GroupedGemm {
   // E4M3 operands (act and w hold one byte per element): the epilogue multiplies by
   // (a_amax / 448) * w_scale[e]; with EPI_SQRELU_BF16, out_amax (if set) receives the max
   // of the stored values (fp32 bits).
+  const uint16_t* add = nullptr;  // EPI_ADD_BF16 only
+  int64_t ld_add = 0;
   int fp8 = 0;
   const uint32_t* a_amax = nullptr;
   const float* w_scale = nullptr;
@@ -200,7 +203,9 @@ int launch_permute(const int32_t* idx, const uint16_t* x, int64_t ldx, int T, in
                    int k, int32_t* counts, int32_t* offsets, int32_t* row_token,
                    int32_t* slot_row, uint16_t* x_perm, void* scratch, cudaStream_t s);
 
+// y = addend + gate-weighted sum of the rows (addend [T, H] bf16, or null).
 int launch_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row,
-                   const float* gates, int T, int H, int k, uint16_t* y, cudaStream_t s);
+                   const float* gates, int T, int H, int k, uint16_t* y, cudaStream_t s,
+                   const uint16_t* addend = nullptr);
 
 }  // namespace moe
