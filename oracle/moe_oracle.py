@@ -374,7 +374,50 @@ def nvfp4_dequantize(mat, g: np.float32 | None = None) -> np.ndarray:
     return nvfp4_quantize(mat, g)["deq"]
 
 
-def moe_tokens_nvfp4(x_all, x_rows, idx_rows, gates_rows, w_up, w_down, h_amax=None):
+def nvfp4_quantize_2d(mat, g: np.float32 | None = None) -> dict:
+    """NVFP4 with 2-D weight blocks ([N3] §2.4: 2-D block scaling for weights): one E4M3
+    scale per 16 rows x 16 K elements (a last block of fewer rows when rows % 16 != 0).
+
+    sb = E4M3(amax(16x16 block) / (6 g)); every element of the block is coded as in
+    nvfp4_quantize with that scale. Returns q [rows, K], sb [rows, K/16] (each row's
+    scale, repeated over the block's rows), g and deq.
+    """
+    a32 = np.asarray(_f64(mat), dtype=np.float32)
+    rows, K = a32.shape
+    if K % NVFP4_BLOCK:
+        raise ValueError("K must be a multiple of 16")
+    if g is None:
+        g = nvfp4_global_scale(np.max(np.abs(a32)) if a32.size else 0.0)
+    g = np.float32(g)
+    nb = K // NVFP4_BLOCK
+    sb = np.zeros((rows, nb), dtype=np.float32)
+    for r0 in range(0, rows, NVFP4_BLOCK):
+        blk = a32[r0:r0 + NVFP4_BLOCK].reshape(-1, nb, NVFP4_BLOCK)
+        bmax = np.max(np.abs(blk), axis=(0, 2))                      # per 16x16 block
+        if g > 0:
+            ratio = bmax / (np.float32(E2M1_MAX) * g)                    # float32 arithmetic
+            sb[r0:r0 + NVFP4_BLOCK] = e4m3_round(ratio.astype(np.float64)).astype(np.float32)
+    denom = (sb * g).astype(np.float32)
+    blocks = a32.reshape(rows, nb, NVFP4_BLOCK)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        scaled = np.where(denom[:, :, None] > 0, blocks / denom[:, :, None], np.float32(0))
+    q = e2m1_round(scaled.astype(np.float64))
+    deq = q * denom.astype(np.float64)[:, :, None]
+    return {"q": q.reshape(rows, K), "sb": sb.astype(np.float64), "g": g,
+            "deq": deq.reshape(rows, K)}
+
+
+def nvfp4_weight_dequantize(w, weight_blocks: str = "1d") -> np.ndarray:
+    """Dequantised NVFP4 weight matrix with 1-D (16 along K) or 2-D (16x16) block scales."""
+    if weight_blocks == "2d":
+        return nvfp4_quantize_2d(w)["deq"]
+    if weight_blocks != "1d":
+        raise ValueError(weight_blocks)
+    return nvfp4_dequantize(w)
+
+
+def moe_tokens_nvfp4(x_all, x_rows, idx_rows, gates_rows, w_up, w_down, h_amax=None,
+                     weight_blocks: str = "1d"):
     """NVFP4 layer output for a subset of tokens.
 
     Expert weights are quantised per expert matrix. The routed activations use one
@@ -392,7 +435,7 @@ def moe_tokens_nvfp4(x_all, x_rows, idx_rows, gates_rows, w_up, w_down, h_amax=N
         for j in range(k):
             e = int(idx_rows[i][j])
             if e not in wu_cache:
-                wu_cache[e] = nvfp4_dequantize(w_up[e])
+                wu_cache[e] = nvfp4_weight_dequantize(w_up[e], weight_blocks)
             a = xr[i:i + 1] @ wu_cache[e].T
             hs.append((i, j, e, np.maximum(a, 0.0) ** 2))
     if h_amax is None:
@@ -401,13 +444,13 @@ def moe_tokens_nvfp4(x_all, x_rows, idx_rows, gates_rows, w_up, w_down, h_amax=N
     wd_cache: dict[int, np.ndarray] = {}
     for i, j, e, h in hs:
         if e not in wd_cache:
-            wd_cache[e] = nvfp4_dequantize(w_down[e])
+            wd_cache[e] = nvfp4_weight_dequantize(w_down[e], weight_blocks)
         hq = nvfp4_dequantize(h.astype(np.float32), gh)
         out[i] += float(gates_rows[i][j]) * (hq @ wd_cache[e].T)[0]
     return out
 
 
-def nvfp4_hidden_amax(x, idx, w_up) -> float:
+def nvfp4_hidden_amax(x, idx, w_up, weight_blocks: str = "1d") -> float:
     """amax of the hidden activations h over every routed (token, expert) pair, with the
     tokens and the up-projection weights in NVFP4 as in grouped_ffn_nvfp4. This is the
     tensor-wide amax that sets the global scale of h; moe_tokens_nvfp4 takes it as h_amax
@@ -417,12 +460,12 @@ def nvfp4_hidden_amax(x, idx, w_up) -> float:
     amax = 0.0
     for e in np.unique(idx):
         toks = np.nonzero((idx == e).any(axis=1))[0]
-        a = xq[toks] @ nvfp4_dequantize(w_up[int(e)]).T
+        a = xq[toks] @ nvfp4_weight_dequantize(w_up[int(e)], weight_blocks).T
         amax = max(amax, float(np.max(np.maximum(a, 0.0) ** 2)))
     return amax
 
 
-def grouped_ffn_nvfp4(x_perm, offsets, w_up, w_down) -> np.ndarray:
+def grouped_ffn_nvfp4(x_perm, offsets, w_up, w_down, weight_blocks: str = "1d") -> np.ndarray:
     """The expert FFNs with NVFP4 operands ([N3] §2.4).
 
     Each expert matrix is quantised with its own global scale. The permuted activations are
@@ -437,22 +480,25 @@ def grouped_ffn_nvfp4(x_perm, offsets, w_up, w_down) -> np.ndarray:
     for e in range(E):
         a, b = int(offsets[e]), int(offsets[e + 1])
         if b > a:
-            hs[e] = np.maximum(xq[a:b] @ nvfp4_dequantize(w_up[e]).T, 0.0) ** 2
+            hs[e] = np.maximum(xq[a:b] @ nvfp4_weight_dequantize(w_up[e], weight_blocks).T,
+                               0.0) ** 2
     h_amax = max((float(np.max(np.abs(h))) for h in hs.values()), default=0.0)
     gh = nvfp4_global_scale(np.float32(h_amax))
     out = np.zeros((xp.shape[0], np.asarray(w_down).shape[1]))
     for e, h in hs.items():
         a, b = int(offsets[e]), int(offsets[e + 1])
-        out[a:b] = nvfp4_dequantize(h.astype(np.float32), gh) @ nvfp4_dequantize(w_down[e]).T
+        out[a:b] = (nvfp4_dequantize(h.astype(np.float32), gh)
+                    @ nvfp4_weight_dequantize(w_down[e], weight_blocks).T)
     return out
 
 
-def moe_layer_nvfp4(x, w_router, bias, w_up, w_down, k: int) -> dict:
+def moe_layer_nvfp4(x, w_router, bias, w_up, w_down, k: int, weight_blocks: str = "1d") -> dict:
     """Routed MoE layer with NVFP4 experts: bf16 routing, NVFP4 expert FFNs, fp64 combine."""
     r = route(x, w_router, bias, k)
     E = np.asarray(w_router).shape[0]
     p = permute(r["idx"], E)
-    y_perm = grouped_ffn_nvfp4(gather_rows(x, p["row_token"]), p["offsets"], w_up, w_down)
+    y_perm = grouped_ffn_nvfp4(gather_rows(x, p["row_token"]), p["offsets"], w_up, w_down,
+                               weight_blocks)
     T = np.asarray(x).shape[0]
     return {"y": combine(y_perm, p["slot_row"], r["gates"], T, k), **r, **p}
 

@@ -515,13 +515,69 @@ def check_shared_expert(o):
         rtol=1e-12, atol=1e-12)
 
 
+def _brute_nvfp4_2d(mat, g):
+    """2-D NVFP4 by table search: one scale per 16x16 block, then every element as in 1-D."""
+    e2 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    e4_vals = [(m * 2.0 ** -9 if ex == 0 else (1 + m / 8) * 2.0 ** (ex - 7))
+               for code in range(127) for ex, m in [(code >> 3, code & 7)]]
+    a = np.asarray(mat, np.float32)
+    out = np.zeros(a.shape)
+    g = np.float32(g)
+    for r0 in range(0, a.shape[0], 16):
+        for b in range(a.shape[1] // 16):
+            blk = a[r0:r0 + 16, 16 * b:16 * b + 16]
+            ratio = np.float32(np.max(np.abs(blk)) / np.float32(np.float32(6) * g))
+            sb = min(_nearest_even(float(ratio), e4_vals, list(range(127))), 448.0) if g > 0 else 0.0
+            den = np.float32(np.float32(sb) * g)
+            for r in range(blk.shape[0]):
+                for i in range(16):
+                    if den > 0:
+                        s = float(np.float32(blk[r, i] / den))
+                        q = 6.0 if abs(s) > 6 else _nearest_even(abs(s), e2, list(range(8)))
+                        out[r0 + r, 16 * b + i] = np.copysign(q, s) * float(den)
+    return out
+
+
+def check_nvfp4_2d(o):
+    """2-D weight blocks: brute force on a matrix with a ragged last row block; a matrix whose
+    16-row groups repeat one row equals the 1-D quantisation; the 2-D grouped FFN matches a
+    brute-force evaluation."""
+    rng = np.random.default_rng(27)
+    a = (rng.standard_normal((37, 48)) * np.exp(rng.uniform(-5, 3, (37, 1)))).astype(np.float32)
+    g = o.nvfp4_global_scale(np.max(np.abs(a)))
+    np.testing.assert_array_equal(o.nvfp4_quantize_2d(a)["deq"], _brute_nvfp4_2d(a, g))
+    rep = np.repeat(a[:3], 16, axis=0)
+    np.testing.assert_array_equal(o.nvfp4_quantize_2d(rep)["deq"], o.nvfp4_quantize(rep)["deq"])
+    E, D, F = 2, 32, 16
+    x = rng.standard_normal((5, D)).astype(np.float32)
+    offsets = np.array([0, 2, 5])
+    wu = rng.standard_normal((E, F, D)).astype(np.float32)
+    wd = rng.standard_normal((E, D, F)).astype(np.float32)
+    got = o.grouped_ffn_nvfp4(x, offsets, wu, wd, weight_blocks="2d")
+    xq = _brute_nvfp4(x, o.nvfp4_global_scale(np.max(np.abs(x))))
+    hs = []
+    for e in range(E):
+        wq = _brute_nvfp4_2d(wu[e], o.nvfp4_global_scale(np.max(np.abs(wu[e]))))
+        for r in range(offsets[e], offsets[e + 1]):
+            hs.append([max(math.fsum(xq[r, i] * wq[f, i] for i in range(D)), 0.0) ** 2
+                       for f in range(F)])
+    hs = np.array(hs)
+    hq = _brute_nvfp4(hs, o.nvfp4_global_scale(np.float32(np.max(hs))))
+    ref = np.zeros((5, D))
+    for e in range(E):
+        wq = _brute_nvfp4_2d(wd[e], o.nvfp4_global_scale(np.max(np.abs(wd[e]))))
+        for r in range(offsets[e], offsets[e + 1]):
+            ref[r] = [math.fsum(hq[r, f] * wq[i, f] for f in range(F)) for i in range(D)]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = [check_route_closed_form, check_topk_brute_force, check_layer_brute_force,
               check_ffn_closed_form, check_single_expert_is_dense_ffn, check_identical_experts,
               check_k_equals_E, check_forced_expert, check_gate_and_count_invariants,
               check_latent_identity, check_latent_brute_force, check_combine_weights,
               check_e2m1_table, check_e4m3_table, check_nvfp4_block, check_nvfp4_bounds,
               check_nvfp4_brute_force, check_grouped_ffn_nvfp4, check_nvfp4_layer_paths,
-              check_fp8_quantize, check_fp8_layer_paths, check_shared_expert]
+              check_fp8_quantize, check_fp8_layer_paths, check_shared_expert, check_nvfp4_2d]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
