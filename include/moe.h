@@ -247,6 +247,14 @@ int moe_quantize_nvfp4_weights(const uint16_t* w, int G, int N, int K, uint8_t* 
  * rows per expert). Layout: x_perm [rows, H] bf16, offsets [E+1] int32, y_perm [rows, H] bf16;
  * up weights quantised from [E, F, H], down weights from [E, H, F].
  * Workspace: moe_grouped_ffn_nvfp4_workspace_size(). */
+/* moe_quantize_nvfp4_weights_2d: as moe_quantize_nvfp4_weights, with 2-D weight blocks
+ * (NVIDIA Nemotron 3 notes §2.4: 2-D block scaling for weights): one block scale per 16 rows
+ * x 16 K elements, sb = E4M3(amax(16x16 block) / (6 g)); the last row block may have fewer
+ * rows. The output formats are the 1-D ones (each row holds its block's scale), so the NVFP4
+ * FFN calls take these weights unchanged. */
+int moe_quantize_nvfp4_weights_2d(const uint16_t* w, int G, int N, int K, uint8_t* codes,
+                                  uint8_t* scales, float* global_scale, cudaStream_t stream);
+
 size_t moe_grouped_ffn_nvfp4_workspace_size(int rows, int H, int F, int E);
 int moe_grouped_ffn_nvfp4(const uint16_t* x_perm, const int32_t* offsets,
                           const uint8_t* up_codes, const uint8_t* up_scales,

@@ -39,6 +39,7 @@ SIGNATURES = {
     "moe_nvfp4_codes_bytes": (_SZ, [_I, _I, _I]),
     "moe_nvfp4_scales_bytes": (_SZ, [_I, _I, _I]),
     "moe_quantize_nvfp4_weights": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _VP]),
+    "moe_quantize_nvfp4_weights_2d": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _VP]),
     "moe_grouped_ffn_nvfp4_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "moe_grouped_ffn_nvfp4": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP,
                                    _VP, _SZ, _VP]),
@@ -272,7 +273,10 @@ class Nvfp4Weights:
         return _ptr(self.codes), _ptr(self.scales), _ptr(self.gscale)
 
 
-def moe_quantize_nvfp4_weights(w, *, stream=None) -> Nvfp4Weights:
+def moe_quantize_nvfp4_weights(w, *, blocks: str = "1d", stream=None) -> Nvfp4Weights:
+    """blocks="1d": one scale per 16 K elements of a row; "2d": per 16 rows x 16 K."""
+    if blocks not in ("1d", "2d"):
+        raise ValueError("blocks must be '1d' or '2d'")
     _cuda_tensor(w, torch.bfloat16, "w", 3)
     G, N, K = w.shape
     L = lib()
@@ -282,8 +286,8 @@ def moe_quantize_nvfp4_weights(w, *, stream=None) -> Nvfp4Weights:
     codes = torch.empty((G, N, K // 2), dtype=torch.uint8, device=w.device)
     scales = torch.empty((ns,), dtype=torch.uint8, device=w.device)
     gscale = torch.empty((G,), dtype=torch.float32, device=w.device)
-    _check(L.moe_quantize_nvfp4_weights(_ptr(w), G, N, K, _ptr(codes), _ptr(scales),
-                                        _ptr(gscale), _stream(stream)),
+    fn = L.moe_quantize_nvfp4_weights if blocks == "1d" else L.moe_quantize_nvfp4_weights_2d
+    _check(fn(_ptr(w), G, N, K, _ptr(codes), _ptr(scales), _ptr(gscale), _stream(stream)),
            "moe_quantize_nvfp4_weights")
     return Nvfp4Weights(codes, scales, gscale, G, N, K)
 

@@ -617,6 +617,21 @@ int moe_quantize_nvfp4_weights(const uint16_t* w, int G, int N, int K, uint8_t* 
   return launch_finalize_gscale(global_scale, G, stream);
 }
 
+int moe_quantize_nvfp4_weights_2d(const uint16_t* w, int G, int N, int K, uint8_t* codes,
+                                  uint8_t* scales, float* global_scale, cudaStream_t stream) {
+  if (G < 1 || G > 1024 || N < 1 || K < 64) return MOE_ERR_INVALID_ARG;
+  if (!w || !codes || !scales || !global_scale) return MOE_ERR_INVALID_ARG;
+  if (K % 64 || !aligned16(w) || !aligned16(codes) || !aligned16(scales))
+    return MOE_ERR_UNSUPPORTED;
+  MOE_CUDA(cudaMemsetAsync(global_scale, 0, sizeof(float) * G, stream));
+  uint32_t* amax = reinterpret_cast<uint32_t*>(global_scale);
+  int st = launch_amax_bf16(w, static_cast<long long>(N) * K, G, amax, stream);
+  if (st) return st;
+  st = launch_quant_weights_2d(w, G, N, K, amax, codes, scales, stream);
+  if (st) return st;
+  return launch_finalize_gscale(global_scale, G, stream);
+}
+
 size_t moe_grouped_ffn_nvfp4_workspace_size(int rows, int H, int F, int E) {
   if (rows < 0 || H <= 0 || F <= 0 || E < 1 || E > 1024) return 0;
   Carver c(nullptr, 0);

@@ -144,6 +144,9 @@ int launch_amax_bf16(const uint16_t* src, long long elems_per_matrix, int G, uin
 // Quantise G weight matrices [N, K] with per-matrix global scales from amax[g].
 int launch_quant_weights(const uint16_t* w, int G, int N, int K, const uint32_t* amax,
                          uint8_t* codes, uint8_t* sf, cudaStream_t s);
+// The same with 2-D (16 rows x 16 K) weight blocks: the block scale is repeated per row.
+int launch_quant_weights_2d(const uint16_t* w, int G, int N, int K, const uint32_t* amax,
+                            uint8_t* codes, uint8_t* sf, cudaStream_t s);
 // g[i] = amax[i] / 2688 in place (amax held as fp32 bits in the same words).
 int launch_finalize_gscale(float* g, int G, cudaStream_t s);
 // poff = exclusive scan of round_up(offsets[e+1] - offsets[e], 128): expert segments padded

@@ -113,6 +113,28 @@ __device__ __forceinline__ uint32_t quant64(const uint4* __restrict__ src, float
   return sf;
 }
 
+// Codes of 16 values with block divisor denom = sb * g (0 gives zero codes): two words,
+// element 2i in the low nibble of its byte.
+__device__ __forceinline__ void code16(const float (&v)[16], float denom, uint32_t& w0,
+                                       uint32_t& w1) {
+  float s[16];
+  if (denom > 0x1p-100f && denom < 0x1p100f) {
+    const float y = __frcp_rn(denom);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = div_markstein(v[i], denom, y);
+  } else if (denom > 0.f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = __fdiv_rn(v[i], denom);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = 0.f;
+  }
+  const float lo[8] = {s[0], s[1], s[2], s[3], s[4], s[5], s[6], s[7]};
+  const float hi[8] = {s[8], s[9], s[10], s[11], s[12], s[13], s[14], s[15]};
+  w0 = e2m1x8(lo);
+  w1 = e2m1x8(hi);
+}
+
 __device__ __forceinline__ uint32_t* sf_word(uint8_t* sf, long long row, int j, int KS) {
   const long long rb = row >> 7;
   const int r = static_cast<int>(row & 127);
@@ -168,6 +190,56 @@ __global__ void k_quant_weights(const uint16_t* __restrict__ w, int G, int N, in
   uint4* dst = reinterpret_cast<uint4*>(codes + row * (K / 2) + j * 32);
   dst[0] = out[0];
   dst[1] = out[1];
+}
+
+// 2-D weight blocks: one thread per (matrix, 16-row group, 16-element K block). The block
+// scale comes from the amax of the whole 16 x 16 block and is written for each of its rows;
+// rows past N in the last 128-row scale block get zero scales.
+__global__ void k_quant_weights_2d(const uint16_t* __restrict__ w, int G, int N, int K,
+                                   const uint32_t* __restrict__ amax, uint8_t* __restrict__ codes,
+                                   uint8_t* __restrict__ sf) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int KS = K / 64, NB = K / 16;
+  const long long rows_pad = static_cast<long long>((N + 127) / 128) * 128;
+  const long long groups = rows_pad / 16;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= G * groups * NB) return;
+  const long long gi = i / NB;            // 16-row group in the padded stack
+  const int b = static_cast<int>(i - gi * NB);
+  const int g = static_cast<int>(gi / groups);
+  const int r0 = static_cast<int>(gi - g * groups) * 16;
+  const int nrows = max(0, min(16, N - r0));
+  const float gs = global_scale(amax + g);
+  float bmax = 0.f;
+  for (int r = 0; r < nrows; ++r) {
+    const uint16_t* p = w + (static_cast<long long>(g) * N + r0 + r) * K + b * 16;
+    for (int c = 0; c < 16; ++c) bmax = fmaxf(bmax, fabsf(__uint_as_float(static_cast<uint32_t>(p[c]) << 16)));
+  }
+  uint32_t sb = 0u;
+  float denom = 0.f;
+  if (gs > 0.f) {
+    sb = static_cast<uint32_t>(
+        __nv_cvt_float_to_fp8(__fdiv_rn(bmax, __fmul_rn(6.0f, gs)), __NV_SATFINITE, __NV_E4M3));
+    denom = __fmul_rn(e4m3_value(sb), gs);
+  }
+  for (int r = 0; r < 16; ++r) {
+    const long long ar = static_cast<long long>(g) * rows_pad + r0 + r;  // padded stack row
+    uint8_t* sfb = reinterpret_cast<uint8_t*>(sf_word(sf, ar, b >> 2, KS)) + (b & 3);
+    if (r >= nrows) {
+      *sfb = 0;
+      continue;
+    }
+    *sfb = static_cast<uint8_t>(sb);
+    const long long row = static_cast<long long>(g) * N + r0 + r;
+    const uint16_t* p = w + row * K + b * 16;
+    float v[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(static_cast<uint32_t>(p[c]) << 16);
+    uint32_t w0, w1;
+    code16(v, denom, w0, w1);
+    *reinterpret_cast<uint2*>(codes + row * (K / 2) + b * 8) = make_uint2(w0, w1);
+  }
 }
 
 __global__ void k_finalize_gscale(float* g, int G) {
@@ -270,6 +342,14 @@ int launch_quant_weights(const uint16_t* w, int G, int N, int K, const uint32_t*
   if (n <= 0) return MOE_OK;
   return launch_pdl(k_quant_weights, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
                     s, w, G, N, K, amax, codes, sf);
+}
+
+int launch_quant_weights_2d(const uint16_t* w, int G, int N, int K, const uint32_t* amax,
+                            uint8_t* codes, uint8_t* sf, cudaStream_t s) {
+  const long long n = static_cast<long long>(G) * ((N + 127) / 128) * 8 * (K / 16);
+  if (n <= 0) return MOE_OK;
+  return launch_pdl(k_quant_weights_2d, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256),
+                    0, s, w, G, N, K, amax, codes, sf);
 }
 
 int launch_finalize_gscale(float* g, int G, cudaStream_t s) {

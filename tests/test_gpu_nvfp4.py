@@ -134,6 +134,48 @@ def test_quantize_weights_bit_exact(moe):
         assert (rows[N:] == 0).all(), "scales of rows past N must be zero"
 
 
+def test_quantize_weights_2d_bit_exact(moe):
+    """2-D (16 rows x 16 K) weight blocks: every code value and every block scale (read per
+    row from the tile-ordered atoms) equal the oracle's, including the ragged last row block."""
+    G, N, K = 3, 200, 320
+    rng = np.random.default_rng(32)
+    w = rng.standard_normal((G, N, K)).astype(np.float32) / np.sqrt(K)
+    w[1] *= np.exp2(-(np.arange(N) % 24))[:, None].astype(np.float32)
+    w[2, :, :32] = 0.0
+    wb = moe_synth.bf16_bits(w)
+    nv = moe.moe_quantize_nvfp4_weights(to_dev(wb), blocks="2d")
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    codes = nv.codes.cpu().numpy()
+    sf = nv.scales.cpu().numpy().reshape(G, -1)
+    gs = nv.gscale.cpu().numpy()
+    for g in range(G):
+        ref = O.nvfp4_quantize_2d(wb[g])
+        assert np.float32(gs[g]).tobytes() == np.float32(ref["g"]).tobytes(), g
+        np.testing.assert_array_equal(decode_codes(codes[g]), ref["q"], err_msg=f"codes {g}")
+        rows = scale_rows(sf[g], N, K)
+        np.testing.assert_array_equal(decode_e4m3(rows[:N]), ref["sb"], err_msg=f"scales {g}")
+        assert (rows[N:] == 0).all()
+
+
+def test_grouped_ffn_nvfp4_2d_weights(moe):
+    counts, H, F = [300, 0, 1, 129, 57, 200], 320, 192
+    E = len(counts)
+    off = _offsets(counts)
+    rows = int(off[-1])
+    seed = rows + H + 5
+    xp = moe_synth.normal_bf16(seed, 50, (rows, H), 1.0)
+    wu = moe_synth.expert_stack(seed, moe_synth.TAG_UP, E, F, H)
+    wd = moe_synth.expert_stack(seed, moe_synth.TAG_DOWN, E, H, F)
+    nu = moe.moe_quantize_nvfp4_weights(to_dev(wu), blocks="2d")
+    nd = moe.moe_quantize_nvfp4_weights(to_dev(wd), blocks="2d")
+    y = moe.moe_grouped_ffn_nvfp4(to_dev(xp), to_dev(off), nu, nd)
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    ref = O.grouped_ffn_nvfp4(xp, off, wu, wd, weight_blocks="2d")
+    _rel_checks(bf16_out(y), ref, "nvfp4 grouped ffn, 2-D weight blocks")
+
+
 # ------------------------------------------------------------------- grouped FFN ----
 
 def _offsets(counts):
