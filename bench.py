@@ -237,6 +237,16 @@ def run_ours(args, w: moe_synth.Workload):
                               P(ws_fp8), ws_fp8.numel(), sp), "moe_forward_fp8")
 
     def step(e_ffn0=None, e_ffn1=None):
+        if args.gathered:
+            # the whole layer through moe_forward_gathered (token rows gathered by the GEMM)
+            if e_ffn0 is not None:
+                e_ffn0.record(stream)
+            chk(L.moe_forward_gathered(P(d["x"]), P(d["w_router"]), P(d["bias"]), P(d["w_up"]),
+                                       P(d["w_down"]), T, H, E, k, F, P(y), P(idx), P(gates),
+                                       P(ws_fwd), ws_fwd.numel(), sp), "moe_forward_gathered")
+            if e_ffn1 is not None:
+                e_ffn1.record(stream)
+            return
         if w.fp8:
             if e_ffn0 is not None:
                 e_ffn0.record(stream)
@@ -371,7 +381,7 @@ def run_ours(args, w: moe_synth.Workload):
 
     peaks, peak_src = load_peaks()
     alg = layer_algorithmic(w, counts_from_routing(routing, E))
-    launches = 1 if (w.latent or w.nvfp4 or w.fp8) else 2   # calls inside the FFN bracket
+    launches = 1 if (w.latent or w.nvfp4 or w.fp8 or args.gathered) else 2  # calls bracketed
     p_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
     p_fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
     t_fp8_flops = alg["flops_experts"] / p_fp8 / 1e12
@@ -393,7 +403,8 @@ def run_ours(args, w: moe_synth.Workload):
         achieved = alg["flops_experts"] / (ffn / 1e3) / 1e12
         peak = p_fp4
         unit = "TFLOP/s"
-    elif w.latent:
+    elif w.latent or args.gathered:
+        # the whole layer call is bracketed; its tcgen05 GEMMs dominate
         bound = "tensor"
         dom_units = alg["flops"]
         achieved = dom_units / (ffn / 1e3) / 1e12
@@ -416,7 +427,7 @@ def run_ours(args, w: moe_synth.Workload):
     else:
         t_flops = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
     roof_ms = max(t_flops, alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
-    traffic = read_traffic(w.name, alg["touched"])
+    traffic = None if args.gathered else read_traffic(w.name, alg["touched"])
     out = {
         "metric": METRIC,
         "value": world * T / (ms / 1e3),
@@ -437,6 +448,8 @@ def run_ours(args, w: moe_synth.Workload):
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": ("whole latent layer (tcgen05 GEMMs dominate)" if w.latent
+                                else "whole layer, token rows gathered by the up-projection"
+                                if args.gathered
                                 else "whole NVFP4 layer (block-scaled tcgen05 GEMMs dominate)"
                                 if w.nvfp4
                                 else "whole FP8 layer (E4M3 tcgen05 grouped GEMMs dominate)"
@@ -605,9 +618,13 @@ def main():
     ap.add_argument("--E", type=int, default=None,
                     help="override the expert count of a standard layer (scaled case)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--gathered", action="store_true",
+                    help="standard layer: time moe_forward_gathered (whole-layer bracket)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = moe_synth.WORKLOADS[args.workload]
+    if args.gathered and (w.latent or w.nvfp4 or w.fp8):
+        ap.error("--gathered applies to the bf16 standard layer")
     if args.T is not None or args.E is not None:
         import dataclasses
         if w.latent and args.E is not None:

@@ -163,6 +163,17 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* bias,
                 int32_t* topk_idx_out, float* gates_out,
                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_forward_gathered: moe_forward whose up-projection, when the rows sit on the MMA's M side
+ * (more than 48 rows per expert on average), gathers the routed token rows straight from x
+ * with TMA tile::gather4, so the permuted copy x_perm is never written; otherwise identical
+ * to moe_forward. Same arguments and workspace (moe_forward_workspace_size()). On B300 the
+ * 32 gather4 copies per 128-row K-slice make the up-projection slower than reading a
+ * materialised x_perm, so moe_forward does not use it. */
+int moe_forward_gathered(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                         const uint16_t* w_up, const uint16_t* w_down, int T, int H, int E, int k,
+                         int F, uint16_t* y, int32_t* topk_idx_out, float* gates_out,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * latent_moe: the LatentMoE layer (NVIDIA Nemotron 3 notes §2.2, Fig. 3b).
  *   x_lat = x . w_in^T                      (H -> L, bf16 projection)

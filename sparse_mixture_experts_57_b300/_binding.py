@@ -34,6 +34,8 @@ SIGNATURES = {
     "moe_combine": (_I, [_VP, _I, _VP, _VP, _I, _I, _I, _VP, _VP]),
     "moe_linear": (_I, [_VP, _VP, _I, _I, _I, _VP, _VP]),
     "moe_forward_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward_gathered": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP,
+                                  _VP, _SZ, _VP]),
     "moe_forward": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ,
                          _VP]),
     "moe_nvfp4_codes_bytes": (_SZ, [_I, _I, _I]),
@@ -215,7 +217,8 @@ def moe_forward_workspace_size(T, H, E, k, F) -> int:
 
 
 def moe_forward(x, w_router, bias, w_up, w_down, k: int, *, out=None, topk_idx_out=None,
-                gates_out=None, workspace=None, stream=None):
+                gates_out=None, workspace=None, stream=None, gathered: bool = False):
+    """gathered=True calls moe_forward_gathered (token rows gathered by the up-projection)."""
     bf = torch.bfloat16
     _cuda_tensor(x, bf, "x", 2)
     _cuda_tensor(w_router, bf, "w_router", 2)
@@ -227,9 +230,10 @@ def moe_forward(x, w_router, bias, w_up, w_down, k: int, *, out=None, topk_idx_o
     y = out if out is not None else torch.empty((T, H), dtype=bf, device=x.device)
     L = lib()
     ws = _workspace(L.moe_forward_workspace_size(T, H, E, k, F), x.device, workspace)
-    _check(L.moe_forward(_ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_up), _ptr(w_down), T, H, E,
-                         k, F, _ptr(y), _ptr(topk_idx_out), _ptr(gates_out), _ptr(ws),
-                         ws.numel(), _stream(stream)), "moe_forward")
+    fn = L.moe_forward_gathered if gathered else L.moe_forward
+    _check(fn(_ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_up), _ptr(w_down), T, H, E,
+              k, F, _ptr(y), _ptr(topk_idx_out), _ptr(gates_out), _ptr(ws),
+              ws.numel(), _stream(stream)), "moe_forward")
     return y
 
 

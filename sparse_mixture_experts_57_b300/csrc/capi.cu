@@ -118,13 +118,18 @@ int router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_router, int 
   return launch_router_logits(x, ldx, w_router, T, D, E, parts, logits, s);
 }
 
+// Expert FFNs. The up-projection reads x_perm [rows, D], or, when row_token is given, gathers
+// the rows from x_src (src_rows rows, row stride ld_src) by token: x_perm is never written.
 int ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_up,
         const uint16_t* w_down, int rows, int D, int F, int E, uint16_t* h, uint16_t* y_perm,
-        cudaStream_t s) {
+        cudaStream_t s, const int32_t* row_token = nullptr, const uint16_t* x_src = nullptr,
+        int64_t ld_src = 0, int src_rows = 0) {
   GroupedGemm up{};
-  up.act = x_perm;
-  up.act_ld = D;
+  up.act = row_token ? x_src : x_perm;
+  up.act_ld = row_token ? ld_src : D;
   up.rows = rows;
+  up.row_token = row_token;
+  up.src_rows = src_rows;
   up.w = w_up;
   up.E = E;
   up.N = F;
@@ -156,18 +161,25 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
           const uint16_t* w_router, const float* bias, const uint16_t* w_up,
           const uint16_t* w_down, int T, int D, int E, int k, int F, uint16_t* y,
           int32_t* idx_out, float* gates_out, const LayerWs& w, cudaStream_t s,
-          const uint16_t* addend = nullptr) {
+          const uint16_t* addend = nullptr, bool gather_tokens = false) {
   int st = router_logits(xr, ldr, w_router, T, Dr, E, parts, w.logits, s);
   if (st) return st;
   int32_t* idx = idx_out ? idx_out : w.idx;
   float* gates = gates_out ? gates_out : w.gates;
   st = launch_topk(w.logits, bias, T, E, k, idx, gates, w.tie, s);
   if (st) return st;
-  st = launch_permute(idx, x, ldx, T, D, E, k, w.counts, w.offsets, w.row_token, w.slot_row,
-                      w.x_perm, w.perm_scratch, s);
-  if (st) return st;
+  // gather_tokens: with the rows on the MMA's M side the up-projection gathers its token
+  // rows itself (TMA gather4), so the permutation only builds the maps (no x_perm copy).
   const int rows = T * k;
-  st = ffn(w.x_perm, w.offsets, w_up, w_down, rows, D, F, E, w.h, w.y_perm, s);
+  const bool gather = gather_tokens && grouped_gemm_rows_as_m(rows, E);
+  st = launch_permute(idx, x, ldx, T, D, E, k, w.counts, w.offsets, w.row_token, w.slot_row,
+                      gather ? nullptr : w.x_perm, w.perm_scratch, s);
+  if (st) return st;
+  if (gather)
+    st = ffn(nullptr, w.offsets, w_up, w_down, rows, D, F, E, w.h, w.y_perm, s, w.row_token, x,
+             ldx, T);
+  else
+    st = ffn(w.x_perm, w.offsets, w_up, w_down, rows, D, F, E, w.h, w.y_perm, s);
   if (st) return st;
   return launch_combine(w.y_perm, rows, w.slot_row, gates, T, D, k, y, s, addend);
 }
@@ -518,6 +530,23 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* bias,
   if (!c.ok()) return MOE_ERR_WORKSPACE;
   return layer(x, H, x, H, H, 1, w_router, bias, w_up, w_down, T, H, E, k, F, y, topk_idx_out,
                gates_out, w, stream);
+}
+
+int moe_forward_gathered(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                         const uint16_t* w_up, const uint16_t* w_down, int T, int H, int E, int k,
+                         int F, uint16_t* y, int32_t* topk_idx_out, float* gates_out,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(T, H, E, k) || F <= 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !bias || !w_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (H % 64 || F % 64 || !aligned16(x) || !aligned16(w_router) || !aligned16(w_up) ||
+      !aligned16(w_down) || !aligned16(y))
+    return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  const LayerWs w = carve_layer(c, T, H, E, k, F);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  return layer(x, H, x, H, H, 1, w_router, bias, w_up, w_down, T, H, E, k, F, y, topk_idx_out,
+               gates_out, w, stream, nullptr, true);
 }
 
 size_t latent_moe_workspace_size(int T, int H, int L, int Ep, int kp, int F,

@@ -51,6 +51,8 @@ struct KArgs {
   int epi;
   int kchunk;  // CHUNKED kernels: K-blocks (of 64) accumulated per TMEM partial sum
   int* status;
+  const int* row_token;    // GATHER kernels: token of each routed row
+  int src_rows;            // GATHER kernels: rows of the gathered activation tensor
   const uint16_t* add;     // EPI_ADD_BF16: bf16 addend, row stride ld_add
   long long ld_add;
   const uint32_t* a_amax;  // E4M3 kernels: activation amax (fp32 bits)
@@ -68,7 +70,7 @@ __host__ __device__ constexpr uint32_t tmem_cols() {
 template <int BN, int STAGES>
 constexpr size_t smem_bytes() {
   return 1024 + size_t(STAGES) * (BM * BK * 2 + BN * BK * 2) + (2 * STAGES + 4) * 8 + 16 +
-         3 * (MAX_GROUPS + 1) * 4;
+         3 * (MAX_GROUPS + 1) * 4 + BM * 4;
 }
 
 __device__ __forceinline__ void record(int* status, int code) { atomicCAS(status, 0, code); }
@@ -186,7 +188,12 @@ __device__ __forceinline__ void store_one(const KArgs& a, long long row, int col
 // F8: E4M3 operands (kind::f8f6f4, K = 32 per MMA): a 128-byte K-slice holds 128 elements,
 // the last slice may run past K (TMA fills zeros), and the epilogue applies the per-tensor
 // scales (a_amax / 448) * w_scale[group].
-template <int BN, int STAGES, bool SWAP, bool CHUNKED = false, bool F8 = false>
+// GATHER (rows-as-M, bf16): the activation rows of a tile are gathered from the token
+// tensor by row_token with TMA gather4 (32 per K-slice), so the permuted copy of the tokens
+// is never written. The whole producer warp loads a tile's 128 token ids into shared memory;
+// lane 0 issues the copies. Rows past the group's end gather an out-of-range row (zeros).
+template <int BN, int STAGES, bool SWAP, bool CHUNKED = false, bool F8 = false,
+          bool GATHER = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tm_act,
                    const __grid_constant__ CUtensorMap tm_w, const KArgs a) {
@@ -199,6 +206,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;
   constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
   static_assert(!(F8 && CHUNKED), "E4M3 kernels have no chunked variant");
+  static_assert(!GATHER || (!SWAP && !CHUNKED && !F8), "gathered rows: bf16 rows-as-M only");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
   static_assert(!CHUNKED || (!SWAP && BN <= 128), "chunked accumulation: rows-as-M, BN <= 128");
 
@@ -216,6 +224,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   int* s_pref = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_off = s_pref + (MAX_GROUPS + 1);
   int* s_cnt = s_off + (MAX_GROUPS + 1);
+  int* s_tok = s_cnt + (MAX_GROUPS + 1);  // GATHER: token ids of the producer's current tile
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -286,7 +295,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int total = s_pref[E] * n_ct;
   const int KB = (a.K + BKE - 1) / BKE;
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // ------------------------------------------------------- TMA producer (gathered rows)
+    const uint64_t pol_w = policy_evict_last();
+    const uint64_t pol_a = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      int e, rt, ct;
+      decode_tile(tile, n_ct, s_pref, E, e, rt, ct);
+      const int rbeg = rt * BM;
+      const int valid_rows = min(BM, s_cnt[e] - rbeg);
+      const int col0 = ct * CT;
+#pragma unroll
+      for (int j = 0; j < BM / 32; ++j) {
+        const int i = lane + 32 * j;
+        s_tok[i] = i < valid_rows ? __ldg(a.row_token + s_off[e] + rbeg + i) : a.src_rows;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+          const int kc = kb * BKE;
+          uint8_t* dst = sA + stage * A_BYTES;
+#pragma unroll 4
+          for (int g4 = 0; g4 < BM / 4; ++g4)
+            tma_gather4(dst + g4 * 512, &tm_act, &full[stage], kc, s_tok[4 * g4],
+                        s_tok[4 * g4 + 1], s_tok[4 * g4 + 2], s_tok[4 * g4 + 3], pol_a);
+          tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kc, col0, e, pol_w);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);  // s_tok is rewritten only after lane 0 is done
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      record(a.status, MOE_ERR_TIMEOUT);
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
       const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_last();
@@ -555,7 +609,8 @@ bool map_3d(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint64_t E
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool SWAP, bool CHUNKED = false, bool F8 = false>
+template <int BN, int STAGES, bool SWAP, bool CHUNKED = false, bool F8 = false,
+          bool GATHER = false>
 int launch_variant(const GroupedGemm& g, const KArgs& ka, cudaStream_t s) {
   CUtensorMap tm_act, tm_w;
   const int act_box = SWAP ? BN : BM;
@@ -575,12 +630,15 @@ int launch_variant(const GroupedGemm& g, const KArgs& ka, cudaStream_t s) {
     if (!encode_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w, wd, ws, wb))
       return MOE_ERR_CUDA;
   } else {
-    if (!map_2d(&tm_act, g.act, g.K, g.rows, g.act_ld, act_box)) return MOE_ERR_CUDA;
+    // gathered rows: a one-row box over the whole token tensor
+    if (!map_2d(&tm_act, g.act, g.K, GATHER ? g.src_rows : g.rows, g.act_ld,
+                GATHER ? 1 : act_box))
+      return MOE_ERR_CUDA;
     if (!map_3d(&tm_w, g.w, Kw, g.N, g.E, w_box)) return MOE_ERR_CUDA;
   }
   constexpr size_t smem = smem_bytes<BN, STAGES>();
   static_assert(smem <= 232448, "shared memory per CTA");
-  auto kern = k_grouped_gemm<BN, STAGES, SWAP, CHUNKED, F8>;
+  auto kern = k_grouped_gemm<BN, STAGES, SWAP, CHUNKED, F8, GATHER>;
   static int configured_device = -1;
   int dev = 0;
   MOE_CUDA(cudaGetDevice(&dev));
@@ -632,6 +690,10 @@ bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool grouped_gemm_rows_as_m(int rows, int E) {
+  return static_cast<double>(rows) / (E > 0 ? E : 1) > 48.0;
+}
+
 int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   if (g.rows <= 0) return MOE_OK;
   if (g.K % BK || g.N % 16 || (g.k_wrap && (g.k_wrap % BK || g.K % g.k_wrap)) || g.E < 1 ||
@@ -640,6 +702,9 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   if (g.fp8 && (g.k_wrap || g.precise || !g.a_amax || !g.w_scale || g.act_ld % 16))
     return MOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_ADD_BF16 && (!g.add || g.ld_add % 8 || g.precise)) return MOE_ERR_UNSUPPORTED;
+  if (g.row_token && (g.fp8 || g.precise || g.k_wrap || !g.offsets || g.src_rows <= 0 ||
+                      g.force_mode == 2))
+    return MOE_ERR_UNSUPPORTED;
   KArgs ka;
   ka.offsets = g.offsets;
   ka.dense_rows = g.rows;
@@ -655,6 +720,8 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   ka.kchunk = 4;  // 256-deep partial sums in the chunked variant
   ka.add = g.add;
   ka.ld_add = g.ld_add;
+  ka.row_token = g.row_token;
+  ka.src_rows = g.src_rows;
   ka.a_amax = g.a_amax;
   ka.w_scale = g.w_scale;
   ka.out_amax = g.epi == EPI_SQRELU_BF16 ? g.out_amax : nullptr;
@@ -664,6 +731,14 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   if (!g.offsets) gg.E = 1;
 
   if (g.precise) return launch_variant<128, 6, false, true>(gg, ka, s);
+  if (g.row_token) {  // gathered activation rows: always rows-as-M
+    switch (pick_bn_rows_as_m(g.N)) {
+      case 256: return launch_variant<256, 4, false, false, false, true>(gg, ka, s);
+      case 224: return launch_variant<224, 4, false, false, false, true>(gg, ka, s);
+      case 192: return launch_variant<192, 5, false, false, false, true>(gg, ka, s);
+      default: return launch_variant<128, 6, false, false, false, true>(gg, ka, s);
+    }
+  }
   // Few rows per group: put the weights on the MMA's M side and the rows on N.
   const double avg_rows = static_cast<double>(g.rows) / gg.E;
   bool swap = g.force_mode == 2 || (g.force_mode == 0 && avg_rows <= 48.0);

@@ -111,6 +111,10 @@ struct GroupedGemm {
   // E4M3 operands (act and w hold one byte per element): the epilogue multiplies by
   // (a_amax / 448) * w_scale[e]; with EPI_SQRELU_BF16, out_amax (if set) receives the max
   // of the stored values (fp32 bits).
+  // Gathered activations (bf16, rows-as-M): row r of group e reads act row
+  // row_token[offsets[e] + r] (act has src_rows rows); x_perm is never materialised.
+  const int32_t* row_token = nullptr;
+  int src_rows = 0;
   const uint16_t* add = nullptr;  // EPI_ADD_BF16 only
   int64_t ld_add = 0;
   int fp8 = 0;
@@ -119,6 +123,9 @@ struct GroupedGemm {
   uint32_t* out_amax = nullptr;
 };
 int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s);
+// Whether a grouped GEMM of `rows` routed rows over E groups runs with the rows on the MMA's
+// M side (and can then gather its activation rows itself).
+bool grouped_gemm_rows_as_m(int rows, int E);
 
 // Tiled TMA descriptor (rank 2 or 3), zero fill out of bounds, 128-byte swizzle unless
 // another is given. dims and box are innermost first; strides_bytes holds the rank - 1 outer

@@ -95,6 +95,21 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// Four rows at arbitrary row coordinates r0..r3, one 128-byte box each (the tensor map's box
+// is one row high), placed 128 bytes apart at dst with the map's swizzle applied by smem
+// address: 32 of these fill a 128-row K-slice exactly like one tiled load. Rows out of range
+// are filled with zeros.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                            int c0, int r0, int r1, int r2, int r3,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3), "l"(policy)
+      : "memory");
+}
+
 // TMA store of a shared-memory tile to global memory, tracked by the issuing thread's bulk
 // async-groups.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int c0,

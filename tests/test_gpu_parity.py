@@ -178,6 +178,25 @@ def test_layer_shapes(moe, T, H, E, k, F):
     _layer_full(moe, moe_synth.Workload("shape", T=T, H=H, E=E, k=k, F=F, seed=T + H))
 
 
+@pytest.mark.parametrize("T,H,E,k,F", [(513, 256, 32, 4, 192), (700, 512, 8, 3, 448),
+                                       (64, 128, 16, 2, 64)])
+def test_layer_gathered_tokens(moe, T, H, E, k, F):
+    """moe_forward_gathered: the up-projection gathers the token rows itself (TMA gather4)
+    when the rows sit on the MMA's M side (first two shapes); the last shape falls back to a
+    materialised x_perm (weights on M)."""
+    w = moe_synth.Workload("gathered", T=T, H=H, E=E, k=k, F=F, seed=T + H + 3)
+    inp = moe_synth.layer_inputs(w)
+    dev = {key: to_dev(v) for key, v in inp.items()}
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    y = moe.moe_forward(dev["x"], dev["w_router"], dev["bias"], dev["w_up"], dev["w_down"], k,
+                        topk_idx_out=idx, gathered=True)
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    ref = O.moe_layer(inp["x"], inp["w_router"], inp["bias"], inp["w_up"], inp["w_down"], k)
+    same = check_selection(idx.cpu().numpy(), ref, inp["bias"], k)
+    assert_close(bf16_out(y)[same], ref["y"][same], f"gathered layer T={T}")
+
+
 def test_layer_nano_decode_full(moe):
     """The whole decode workload (64 tokens, 128 experts, top-6) against the oracle."""
     _layer_full(moe, moe_synth.WORKLOADS["nano_decode"])
