@@ -95,6 +95,25 @@ def layer_algorithmic(w: moe_synth.Workload, counts: np.ndarray) -> dict:
             "ffn_bytes_per_launch": ffn_bytes_per_launch}
 
 
+def kernels_per_step(w: moe_synth.Workload, gathered: bool = False) -> int:
+    """Library kernels one timed step launches (memsets excluded), mirroring the C library's
+    choices: the fused small-batch routing kernel (T <= 256, E <= 256, routing width <= 6144)
+    or router logits + top-k + permutation (one small-batch block, or mark/count/scan)."""
+    T, E, k = w.T, w.E, w.k
+    d_route = (w.latent * (3 if w.router_on_latent else 0) or w.H) if w.latent else w.H
+    fused = T <= 256 and E <= 256 and d_route <= 6144 and k <= 32
+    words = (T + 31) // 32
+    perm = 1 if (words <= 64 and words * E <= 8192) else 3
+    if w.nvfp4:   # route (1 or 2 + perm), amax x, pad, quantise x, up, quantise h, down, combine
+        return (1 if fused else 2 + perm) + 7
+    if w.fp8:     # route (1 or 2 + perm), amax x, quantise x, up, quantise h, down, combine
+        return (1 if fused else 2 + perm) + 6
+    route = 2 if fused else (2 + perm + 1)     # + the row copy
+    if w.latent:  # projection in, routing in the latent space, FFN, combine, projection out
+        return 1 + route + 2 + 1 + 1
+    return route + 2 + 1
+
+
 # ------------------------------------------------------------------------ clock sampler ----
 
 class ClockSampler:
@@ -191,8 +210,8 @@ def run_ours(args, w: moe_synth.Workload):
     slot_row = torch.empty((rows,), dtype=torch.int32, device=dev)
     x_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev)
     y_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev)
-    ws_route = torch.empty(L.moe_route_workspace_size(T, D, E, k), dtype=torch.uint8, device=dev)
-    ws_perm = torch.empty(L.moe_permute_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
+    ws_rd = torch.empty(L.moe_route_dispatch_workspace_size(T, D, E, k), dtype=torch.uint8,
+                        device=dev)
     ws_ffn = torch.empty(L.moe_grouped_ffn_workspace_size(rows, D, F, E), dtype=torch.uint8,
                          device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -271,10 +290,10 @@ def run_ours(args, w: moe_synth.Workload):
             if e_ffn1 is not None:
                 e_ffn1.record(stream)
             return
-        chk(L.moe_route(P(d["x"]), P(d["w_router"]), P(d["bias"]), T, H, E, k, P(idx), P(gates),
-                        P(tie), P(ws_route), ws_route.numel(), sp), "moe_route")
-        chk(L.moe_permute(P(idx), P(d["x"]), T, H, E, k, P(counts), P(offsets), P(row_token),
-                          P(slot_row), P(x_perm), P(ws_perm), ws_perm.numel(), sp), "moe_permute")
+        chk(L.moe_route_dispatch(P(d["x"]), P(d["w_router"]), P(d["bias"]), T, H, E, k, P(idx),
+                                 P(gates), P(tie), P(counts), P(offsets), P(row_token),
+                                 P(slot_row), P(x_perm), P(ws_rd), ws_rd.numel(), sp),
+            "moe_route_dispatch")
         if e_ffn0 is not None:
             e_ffn0.record(stream)
         chk(L.moe_grouped_ffn(P(x_perm), P(offsets), P(d["w_up"]), P(d["w_down"]), rows, H, F, E,
@@ -287,7 +306,7 @@ def run_ours(args, w: moe_synth.Workload):
     # kernels per step: route 2, permutation 2-4, FFN 2, combine 1 (bf16); the latent layer
     # adds its two projections; the NVFP4 layer replaces the gather by amax, padding,
     # two quantisations and the two block-scaled GEMMs
-    launches_per_step = 11 if w.latent else (12 if w.nvfp4 else (11 if w.fp8 else 9))
+    launches_per_step = kernels_per_step(w, args.gathered)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -330,6 +349,10 @@ def run_ours(args, w: moe_synth.Workload):
     clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(s_ev, e_ev)]
     ffn_ms = [a.elapsed_time(b) for a, b in zip(f0, f1)]
+    # phases of a step: before the bracketed call(s), inside them, after them
+    phase_ms = {"before_bracket": statistics.mean(s.elapsed_time(a) for s, a in zip(s_ev, f0)),
+                "bracket": statistics.mean(ffn_ms),
+                "after_bracket": statistics.mean(b.elapsed_time(e) for b, e in zip(f1, e_ev))}
     ms = statistics.mean(step_ms)
     ffn = statistics.mean(ffn_ms)
     if world > 1:
@@ -468,6 +491,7 @@ def run_ours(args, w: moe_synth.Workload):
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
                 "ms_per_step": e2e},
         "gpu_launches": launches_per_step * K,
+        "phase_ms": phase_ms,
         "clocks": clocks.summary(),
         "wall_s": wall,
     }

@@ -91,6 +91,20 @@ int moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int H, int E,
                 cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * moe_route_dispatch: moe_route followed by moe_permute, with the same outputs as the two
+ * calls (topk_idx, gates, tie_flag; counts, offsets, row_token, slot_row, x_perm; D plays
+ * the role of H). For small batches (T <= 256, E <= 256, D <= 6144) the router logits, the
+ * top-k and the dispatch maps run as one kernel, followed by the row copy.
+ * Workspace: moe_route_dispatch_workspace_size().
+ * ------------------------------------------------------------------------------------- */
+size_t moe_route_dispatch_workspace_size(int T, int D, int E, int k);
+int moe_route_dispatch(const uint16_t* x, const uint16_t* w_router, const float* bias, int T,
+                       int D, int E, int k, int32_t* topk_idx, float* gates, uint8_t* tie_flag,
+                       int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
+                       uint16_t* x_perm, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * moe_permute_noalloc: moe_permute for callers that cannot provide a workspace.
  * The pages have no counterpart to this call; it exists for integration only. Some callers
  * cannot hand the library device memory for scratch, for example a host runtime whose own

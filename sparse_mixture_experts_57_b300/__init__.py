@@ -30,5 +30,6 @@ from ._binding import (  # noqa: F401
     moe_quantize_fp8_weights,
     moe_quantize_nvfp4_weights,
     moe_route,
+    moe_route_dispatch,
     status_string,
 )

@@ -25,6 +25,9 @@ SIGNATURES = {
     "moe_get_device_status": (_I, [_VP, ctypes.POINTER(_I)]),
     "moe_route_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "moe_route": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_route_dispatch_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "moe_route_dispatch": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                _VP, _VP, _SZ, _VP]),
     "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_permute": (_I, [_VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "moe_permute_noalloc_max_scratch_bytes": (_SZ, []),
@@ -152,6 +155,32 @@ def moe_route(x, w_router, bias, k: int, *, workspace=None, stream=None):
     _check(L.moe_route(_ptr(x), _ptr(w_router), _ptr(bias), T, D, E, k, _ptr(idx), _ptr(gates),
                        _ptr(tie), _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
     return idx, gates, tie
+
+
+def moe_route_dispatch(x, w_router, bias, k: int, *, workspace=None, stream=None):
+    """moe_route then moe_permute in one call; returns (idx, gates, tie, permutation dict)."""
+    bf = torch.bfloat16
+    _cuda_tensor(x, bf, "x", 2)
+    _cuda_tensor(w_router, bf, "w_router", 2)
+    _cuda_tensor(bias, torch.float32, "bias", 1)
+    T, D = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+    tie = torch.empty((T,), dtype=torch.uint8, device=dev)
+    p = {"counts": torch.empty((E,), dtype=torch.int32, device=dev),
+         "offsets": torch.empty((E + 1,), dtype=torch.int32, device=dev),
+         "row_token": torch.empty((T * k,), dtype=torch.int32, device=dev),
+         "slot_row": torch.empty((T * k,), dtype=torch.int32, device=dev),
+         "x_perm": torch.empty((T * k, D), dtype=bf, device=dev)}
+    L = lib()
+    ws = _workspace(L.moe_route_dispatch_workspace_size(T, D, E, k), dev, workspace)
+    _check(L.moe_route_dispatch(_ptr(x), _ptr(w_router), _ptr(bias), T, D, E, k, _ptr(idx),
+                                _ptr(gates), _ptr(tie), _ptr(p["counts"]), _ptr(p["offsets"]),
+                                _ptr(p["row_token"]), _ptr(p["slot_row"]), _ptr(p["x_perm"]),
+                                _ptr(ws), ws.numel(), _stream(stream)), "moe_route_dispatch")
+    return idx, gates, tie, p
 
 
 def moe_permute(topk_idx, x, E: int, *, workspace=None, stream=None):

@@ -68,6 +68,7 @@ struct LayerWs {
   int32_t* offsets;
   int32_t* row_token;
   int32_t* slot_row;
+  int* sync;  // counters of the fused small-batch routing kernel
   void* perm_scratch;
   uint16_t* x_perm;
   uint16_t* h;
@@ -85,6 +86,7 @@ LayerWs carve_layer(Carver& c, int T, int D, int E, int k, int F) {
   w.offsets = c.take<int32_t>(E + 1);
   w.row_token = c.take<int32_t>(rows);
   w.slot_row = c.take<int32_t>(rows);
+  w.sync = c.take<int>(route_fused_sync_ints(T));
   w.perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
   w.x_perm = c.take<uint16_t>(rows * D);
   w.h = c.take<uint16_t>(rows * F);
@@ -162,19 +164,31 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
           const uint16_t* w_down, int T, int D, int E, int k, int F, uint16_t* y,
           int32_t* idx_out, float* gates_out, const LayerWs& w, cudaStream_t s,
           const uint16_t* addend = nullptr, bool gather_tokens = false) {
-  int st = router_logits(xr, ldr, w_router, T, Dr, E, parts, w.logits, s);
-  if (st) return st;
   int32_t* idx = idx_out ? idx_out : w.idx;
   float* gates = gates_out ? gates_out : w.gates;
-  st = launch_topk(w.logits, bias, T, E, k, idx, gates, w.tie, s);
-  if (st) return st;
   // gather_tokens: with the rows on the MMA's M side the up-projection gathers its token
   // rows itself (TMA gather4), so the permutation only builds the maps (no x_perm copy).
   const int rows = T * k;
   const bool gather = gather_tokens && grouped_gemm_rows_as_m(rows, E);
-  st = launch_permute(idx, x, ldx, T, D, E, k, w.counts, w.offsets, w.row_token, w.slot_row,
-                      gather ? nullptr : w.x_perm, w.perm_scratch, s);
-  if (st) return st;
+  int st;
+  if (route_fused_ok(T, Dr, E, k, parts)) {
+    // small batches: logits, top-k and the dispatch maps in one kernel, then the row copy
+    st = launch_route_fused(xr, ldr, w_router, bias, T, Dr, E, k, parts, w.logits, idx, gates,
+                            w.tie, w.counts, w.offsets, w.row_token, w.slot_row, w.sync, s);
+    if (st) return st;
+    if (!gather) {
+      st = launch_gather_rows(w.row_token, x, ldx, rows, D, w.x_perm, s);
+      if (st) return st;
+    }
+  } else {
+    st = router_logits(xr, ldr, w_router, T, Dr, E, parts, w.logits, s);
+    if (st) return st;
+    st = launch_topk(w.logits, bias, T, E, k, idx, gates, w.tie, s);
+    if (st) return st;
+    st = launch_permute(idx, x, ldx, T, D, E, k, w.counts, w.offsets, w.row_token, w.slot_row,
+                        gather ? nullptr : w.x_perm, w.perm_scratch, s);
+    if (st) return st;
+  }
   if (gather)
     st = ffn(nullptr, w.offsets, w_up, w_down, rows, D, F, E, w.h, w.y_perm, s, w.row_token, x,
              ldx, T);
@@ -417,7 +431,8 @@ size_t moe_route_workspace_size(int T, int D, int E, int k) {
   (void)D;
   (void)k;
   if (T < 0 || E < 1) return 0;
-  return align_up(static_cast<size_t>(T) * E * sizeof(float), 256) + 256;
+  return align_up(static_cast<size_t>(T) * E * sizeof(float), 256) +
+         align_up(route_fused_sync_ints(T) * sizeof(int), 256) + 256;
 }
 
 int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int D, int E,
@@ -429,10 +444,56 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, in
   if (D % 8 || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_UNSUPPORTED;
   Carver c(workspace, workspace_bytes);
   float* logits = c.take<float>(static_cast<size_t>(T) * E);
+  int* sync = c.take<int>(route_fused_sync_ints(T));
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  if (route_fused_ok(T, D, E, k, 1))  // small batches: logits and top-k in one kernel
+    return launch_route_fused(x, D, w_router, bias, T, D, E, k, 1, logits, topk_idx, gates,
+                              tie_flag, nullptr, nullptr, nullptr, nullptr, sync, stream);
   int st = router_logits(x, D, w_router, T, D, E, 1, logits, stream);
   if (st) return st;
   return launch_topk(logits, bias, T, E, k, topk_idx, gates, tie_flag, stream);
+}
+
+size_t moe_route_dispatch_workspace_size(int T, int D, int E, int k) {
+  if (!dims_ok(T, D, E, k)) return 0;
+  return moe_route_workspace_size(T, D, E, k) + permute_scratch_bytes(T, E) + 512;
+}
+
+int moe_route_dispatch(const uint16_t* x, const uint16_t* w_router, const float* bias, int T,
+                       int D, int E, int k, int32_t* topk_idx, float* gates, uint8_t* tie_flag,
+                       int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* slot_row,
+                       uint16_t* x_perm, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
+  if (!dims_ok(T, D, E, k)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T == 0) {
+    MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream));
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), stream));
+    return MOE_OK;
+  }
+  if (!x || !w_router || !bias || !topk_idx || !gates || !row_token || !slot_row || !x_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (D % 8 || !aligned16(x) || !aligned16(w_router) || !aligned16(x_perm))
+    return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  float* logits = c.take<float>(static_cast<size_t>(T) * E);
+  int* sync = c.take<int>(route_fused_sync_ints(T));
+  void* scratch = c.take<char>(permute_scratch_bytes(T, E));
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  if (route_fused_ok(T, D, E, k, 1)) {
+    // small batches: logits, top-k and the dispatch maps in one kernel, then the row copy
+    const int st = launch_route_fused(x, D, w_router, bias, T, D, E, k, 1, logits, topk_idx,
+                                      gates, tie_flag, counts, offsets, row_token, slot_row,
+                                      sync, stream);
+    if (st) return st;
+    return launch_gather_rows(row_token, x, D, T * k, D, x_perm, stream);
+  }
+  int st = router_logits(x, D, w_router, T, D, E, 1, logits, stream);
+  if (st) return st;
+  st = launch_topk(logits, bias, T, E, k, topk_idx, gates, tie_flag, stream);
+  if (st) return st;
+  return launch_permute(topk_idx, x, D, T, D, E, k, counts, offsets, row_token, slot_row, x_perm,
+                        scratch, stream);
 }
 
 size_t moe_permute_workspace_size(int T, int E, int k) {
@@ -701,6 +762,7 @@ size_t moe_forward_nvfp4_workspace_size(int T, int H, int E, int k, int F) {
   c.take<int32_t>(E + 1);                                       // offsets
   c.take<int32_t>(rows);                                        // row_token
   c.take<int32_t>(rows);                                        // slot_row
+  c.take<int>(route_fused_sync_ints(T));
   c.take<char>(permute_scratch_bytes(T, E));
   c.take<uint16_t>(rows * H);                                   // y_perm
   carve_fp4(c, static_cast<int>(rows), H, F, E);
@@ -732,6 +794,7 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
   int32_t* offsets = c.take<int32_t>(E + 1);
   int32_t* row_token = c.take<int32_t>(rows);
   int32_t* slot_row = c.take<int32_t>(rows);
+  int* sync = c.take<int>(route_fused_sync_ints(T));
   void* perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
   uint16_t* y_perm = c.take<uint16_t>(rows * H);
   const Fp4Ws w = carve_fp4(c, static_cast<int>(rows), H, F, E);
@@ -739,13 +802,20 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
   if (topk_idx_out) idx = topk_idx_out;
   if (gates_out) gates = gates_out;
   // routing and dispatch stay in bf16/fp32; the expert FFNs run in NVFP4
-  int st = router_logits(x, H, w_router, T, H, E, 1, logits, stream);
-  if (st) return st;
-  st = launch_topk(logits, bias, T, E, k, idx, gates, tie, stream);
-  if (st) return st;
-  st = launch_permute(idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, nullptr,
-                      perm_scratch, stream);
-  if (st) return st;
+  int st;
+  if (route_fused_ok(T, H, E, k, 1)) {  // small batches: routing and maps in one kernel
+    st = launch_route_fused(x, H, w_router, bias, T, H, E, k, 1, logits, idx, gates, tie, counts,
+                            offsets, row_token, slot_row, sync, stream);
+    if (st) return st;
+  } else {
+    st = router_logits(x, H, w_router, T, H, E, 1, logits, stream);
+    if (st) return st;
+    st = launch_topk(logits, bias, T, E, k, idx, gates, tie, stream);
+    if (st) return st;
+    st = launch_permute(idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, nullptr,
+                        perm_scratch, stream);
+    if (st) return st;
+  }
   st = ffn_nvfp4(x, H, T, row_token, offsets, {up_codes, up_scales, up_gscale},
                  {down_codes, down_scales, down_gscale}, static_cast<int>(rows), H, F, E, y_perm,
                  w, stream);
@@ -806,6 +876,7 @@ size_t moe_forward_fp8_workspace_size(int T, int H, int E, int k, int F) {
   c.take<int32_t>(E + 1);
   c.take<int32_t>(rows);
   c.take<int32_t>(rows);
+  c.take<int>(route_fused_sync_ints(T));
   c.take<char>(permute_scratch_bytes(T, E));
   c.take<uint16_t>(rows * H);
   carve_fp8(c, static_cast<int>(rows), H, F);
@@ -834,19 +905,27 @@ int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bi
   int32_t* offsets = c.take<int32_t>(E + 1);
   int32_t* row_token = c.take<int32_t>(rows);
   int32_t* slot_row = c.take<int32_t>(rows);
+  int* sync = c.take<int>(route_fused_sync_ints(T));
   void* perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
   uint16_t* y_perm = c.take<uint16_t>(rows * H);
   const Fp8Ws w = carve_fp8(c, static_cast<int>(rows), H, F);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
   if (topk_idx_out) idx = topk_idx_out;
   if (gates_out) gates = gates_out;
-  int st = router_logits(x, H, w_router, T, H, E, 1, logits, stream);
-  if (st) return st;
-  st = launch_topk(logits, bias, T, E, k, idx, gates, tie, stream);
-  if (st) return st;
-  st = launch_permute(idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, nullptr,
-                      perm_scratch, stream);
-  if (st) return st;
+  int st;
+  if (route_fused_ok(T, H, E, k, 1)) {  // small batches: routing and maps in one kernel
+    st = launch_route_fused(x, H, w_router, bias, T, H, E, k, 1, logits, idx, gates, tie, counts,
+                            offsets, row_token, slot_row, sync, stream);
+    if (st) return st;
+  } else {
+    st = router_logits(x, H, w_router, T, H, E, 1, logits, stream);
+    if (st) return st;
+    st = launch_topk(logits, bias, T, E, k, idx, gates, tie, stream);
+    if (st) return st;
+    st = launch_permute(idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, nullptr,
+                        perm_scratch, stream);
+    if (st) return st;
+  }
   // the tokens are quantised straight from x in expert order (row_token), no bf16 x_perm
   st = ffn_fp8(x, H, T, row_token, offsets, up_codes, up_scale, down_codes, down_scale,
                static_cast<int>(rows), H, F, E, y_perm, w, stream);

@@ -207,6 +207,20 @@ int launch_router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_route
 int launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx,
                 float* gates, uint8_t* tie, cudaStream_t s);
 
+// Small batches (T <= 256, E <= 256): router logits, top-k and, when row_token is set, the
+// dispatch maps (counts, offsets, row_token, slot_row) in one kernel. `sync` holds
+// route_fused_sync_ints(T) ints of scratch (zeroed by the launch).
+bool route_fused_ok(int T, int D, int E, int k, int parts);
+size_t route_fused_sync_ints(int T);
+int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
+                       const float* bias, int T, int D, int E, int k, int parts, float* logits,
+                       int32_t* idx, float* gates, uint8_t* tie, int32_t* counts,
+                       int32_t* offsets, int32_t* row_token, int32_t* slot_row, int* sync,
+                       cudaStream_t s);
+// x_perm[r] = x[row_token[r]] for r < rows.
+int launch_gather_rows(const int32_t* row_token, const uint16_t* x, int64_t ldx, int rows, int H,
+                       uint16_t* x_perm, cudaStream_t s);
+
 // Permutation pieces.
 size_t permute_scratch_bytes(int T, int E);
 int launch_permute(const int32_t* idx, const uint16_t* x, int64_t ldx, int T, int H, int E,

@@ -6,11 +6,14 @@
 // sigmoid scores plus a per-expert bias that enters the selection only, with the gates
 // renormalised from the unbiased scores of the chosen experts.
 //
-// Two pieces: router logits (a small-batch CUDA-core kernel here; large batches use the
+// Two pieces: router logits (small-batch CUDA-core kernels here; large batches use the
 // tcgen05 grouped GEMM with an fp32 epilogue), then a warp-per-token top-k.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "internal.h"
+#include "scan.cuh"
 
 namespace moe {
 namespace {
@@ -75,23 +78,72 @@ __global__ void k_router_logits(const uint16_t* __restrict__ x, long long ldx,
   }
 }
 
-// Warp per token. Each lane holds experts e = lane + 32*i. The k best biased scores are
-// extracted by k (+1 for the gap) rounds of a warp-wide arg-max; ties go to the lower index.
-template <int VPL>
-__global__ void k_topk(const float* __restrict__ logits, const float* __restrict__ bias, int T,
-                       int E, int k, int32_t* __restrict__ idx, float* __restrict__ gates,
-                       uint8_t* __restrict__ tie) {
+// Small batches: one CTA per (8 tokens, 8 experts). The CTA stages its 8 token rows (all
+// `parts` planes) in shared memory once; warp w then streams expert e0 + w's router row
+// from global memory and dots it with the 8 staged rows. Each router row is read once per
+// 8-token group and each token row once per 8-expert group, instead of once per warp.
+constexpr int kSmallTok = 8, kSmallExp = 8;
+constexpr int kSmallMaxElems = 6144;  // staged elements per token row (all planes)
+
+__global__ void __launch_bounds__(256)
+    k_router_logits_small(const uint16_t* __restrict__ x, long long ldx,
+                          const uint16_t* __restrict__ w, int T, int D, int E, int parts,
+                          float* __restrict__ logits) {
   griddep_wait();
   griddep_launch_dependents();
+  extern __shared__ uint4 sx[];  // [kSmallTok][parts * D / 8]
+  const int t0 = blockIdx.x * kSmallTok;
+  const int nvec = D / 8, rowv = parts * nvec;
+  for (int i = threadIdx.x; i < kSmallTok * rowv; i += blockDim.x) {
+    const int t = i / rowv, v = i - t * rowv;
+    sx[i] = t0 + t < T ? __ldg(reinterpret_cast<const uint4*>(x + (t0 + t) * ldx) + v)
+                       : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
+  const int e = blockIdx.y * kSmallExp + (threadIdx.x >> 5);
+  if (e >= E) return;
+  const uint4* wrow = reinterpret_cast<const uint4*>(w + static_cast<long long>(e) * D);
+  float acc[kSmallTok];
+#pragma unroll
+  for (int i = 0; i < kSmallTok; ++i) acc[i] = 0.f;
+#pragma unroll 2
+  for (int v = lane; v < nvec; v += 32) {
+    const uint4 wv = __ldg(wrow + v);
+#pragma unroll
+    for (int i = 0; i < kSmallTok; ++i)
+      for (int p = 0; p < parts; ++p) acc[i] = dot8(sx[i * rowv + p * nvec + v], wv, acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < kSmallTok; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  }
+  if (lane < kSmallTok && t0 + lane < T) {
+    float v = acc[0];
+#pragma unroll
+    for (int i = 1; i < kSmallTok; ++i)
+      if (lane == i) v = acc[i];
+    logits[static_cast<long long>(t0 + lane) * E + e] = v;
+  }
+}
+
+// Top-k of one token, by one warp. Each lane holds experts e = lane + 32*i. The k best
+// biased scores are extracted by k (+1 for the gap) rounds of a warp-wide arg-max; ties go to
+// the lower index. `row` points at the token's E logits; with CG the logits are read from L2
+// (they were written by other CTAs of the same kernel).
+template <int VPL, bool CG>
+__device__ __forceinline__ void topk_token(const float* __restrict__ row,
+                                           const float* __restrict__ bias, long long t, int E,
+                                           int k, int32_t* __restrict__ idx,
+                                           float* __restrict__ gates, uint8_t* __restrict__ tie) {
+  const int lane = threadIdx.x & 31;
   float s[VPL], u[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      const float z = logits[t * E + e];
+      const float z = CG ? __ldcg(row + e) : row[e];
       s[i] = 1.f / (1.f + expf(-z));
       const float ui = s[i] + bias[e];
       u[i] = (ui == ui) ? ui : -INFINITY;  // NaN never wins
@@ -152,11 +204,183 @@ __global__ void k_topk(const float* __restrict__ logits, const float* __restrict
   if (tie && lane == 0) tie[t] = (k < E && (uk - uk1) < 1e-5f) ? 1 : 0;
 }
 
+template <int VPL>
+__global__ void k_topk(const float* __restrict__ logits, const float* __restrict__ bias, int T,
+                       int E, int k, int32_t* __restrict__ idx, float* __restrict__ gates,
+                       uint8_t* __restrict__ tie) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  topk_token<VPL, false>(logits + t * E, bias, t, E, k, idx, gates, tie);
+}
+
+// Small batches, routing and dispatch maps in one kernel. Grid (token groups of 8, expert
+// groups of 8), 256 threads:
+//  1. every CTA computes its 8 x 8 tile of router logits (as k_router_logits_small);
+//  2. the last CTA to finish a token group (an atomic count per group) runs the top-k of its
+//     8 tokens, one warp per token;
+//  3. with perm set, the last token group to finish builds the dispatch maps for all tokens
+//     in shared memory: per-expert counts and offsets, then row_token / slot_row with rows of
+//     one expert in ascending token order (a token-word x expert bit matrix, as moe_permute).
+// Which CTA takes steps 2 and 3 depends on timing; what they compute does not. The counters
+// (sync[0 .. groups]) must be zero at entry and are zero again at exit.
+constexpr int kFusedMaxT = 256, kFusedMaxE = 256;
+
+template <int VPL>
+__global__ void __launch_bounds__(256)
+    k_route_small(const uint16_t* __restrict__ x, long long ldx, const uint16_t* __restrict__ w,
+                  const float* __restrict__ bias, int T, int D, int E, int k, int parts,
+                  float* __restrict__ logits, int32_t* __restrict__ idx,
+                  float* __restrict__ gates, uint8_t* __restrict__ tie, int perm,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ row_token, int32_t* __restrict__ slot_row,
+                  int* __restrict__ sync, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ uint4 sx[];
+  __shared__ int s_flag;
+  __shared__ int warp_sums[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * kSmallTok;
+  // 1. logits tile
+  {
+    const int nvec = D / 8, rowv = parts * nvec;
+    for (int i = tid; i < kSmallTok * rowv; i += blockDim.x) {
+      const int t = i / rowv, v = i - t * rowv;
+      sx[i] = t0 + t < T ? __ldg(reinterpret_cast<const uint4*>(x + (t0 + t) * ldx) + v)
+                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+    const int e = blockIdx.y * kSmallExp + warp;
+    if (e < E) {
+      const uint4* wrow = reinterpret_cast<const uint4*>(w + static_cast<long long>(e) * D);
+      float acc[kSmallTok];
+#pragma unroll
+      for (int i = 0; i < kSmallTok; ++i) acc[i] = 0.f;
+#pragma unroll 2
+      for (int v = lane; v < nvec; v += 32) {
+        const uint4 wv = __ldg(wrow + v);
+#pragma unroll
+        for (int i = 0; i < kSmallTok; ++i)
+          for (int p = 0; p < parts; ++p) acc[i] = dot8(sx[i * rowv + p * nvec + v], wv, acc[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < kSmallTok; ++i) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+      }
+      if (lane < kSmallTok && t0 + lane < T) {
+        float v = acc[0];
+#pragma unroll
+        for (int i = 1; i < kSmallTok; ++i)
+          if (lane == i) v = acc[i];
+        logits[static_cast<long long>(t0 + lane) * E + e] = v;
+      }
+    }
+  }
+  // 2. the last CTA of this token group: top-k of its tokens
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_flag = atomicAdd(sync + blockIdx.x, 1) == static_cast<int>(gridDim.y) - 1;
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  if (warp < kSmallTok && t0 + warp < T)
+    topk_token<VPL, true>(logits + static_cast<long long>(t0 + warp) * E, bias, t0 + warp, E, k,
+                          idx, gates, tie);
+  if (tid == 0) sync[blockIdx.x] = 0;
+  if (!perm) return;
+  // 3. the last token group: dispatch maps for all tokens
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_flag = atomicAdd(sync + gridDim.x, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  const int W = (T + 31) / 32;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(sx);  // [W][E]
+  int* wpref = reinterpret_cast<int*>(bits + W * E);  // [W][E]
+  for (int i = tid; i < W * E; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  bool bad = false;
+  for (int i = tid; i < T * k; i += blockDim.x) {
+    const int t = i / k;
+    const int e = __ldcg(idx + i);
+    if (e < 0 || e >= E) {
+      bad = true;
+      continue;
+    }
+    const uint32_t bit = 1u << (t & 31);
+    if (atomicOr(&bits[(t >> 5) * E + e], bit) & bit) bad = true;
+  }
+  if (__syncthreads_or(bad) && tid == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+  int c = 0;
+  if (tid < E) {
+    for (int wd = 0; wd < W; ++wd) {
+      wpref[wd * E + tid] = c;
+      c += __popc(bits[wd * E + tid]);
+    }
+    counts[tid] = c;
+  }
+  int total;
+  const int excl = block_exclusive_scan(c, warp_sums, &total);
+  __shared__ int s_off[kFusedMaxE];
+  if (tid < E) {
+    offsets[tid] = excl;
+    s_off[tid] = excl;
+  }
+  if (tid == 0) offsets[E] = total;
+  __syncthreads();
+  for (int i = tid; i < T * k; i += blockDim.x) {
+    const int t = i / k;
+    const int e = __ldcg(idx + i);
+    if (e < 0 || e >= E) {
+      slot_row[i] = -1;
+      continue;
+    }
+    const int o = (t >> 5) * E + e;
+    const int row = s_off[e] + wpref[o] + __popc(bits[o] & ((1u << (t & 31)) - 1u));
+    row_token[row] = t;
+    slot_row[i] = row;
+  }
+  if (tid == 0) sync[gridDim.x] = 0;
+}
+
+// x_perm[r, :] = x[row_token[r], :], one warp per row (16-byte vectors).
+__global__ void k_gather_rows(const int32_t* __restrict__ row_token, const uint16_t* __restrict__ x,
+                              long long ldx, int rows, int H, uint16_t* __restrict__ x_perm) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (r >= rows) return;
+  const int t = row_token[r];
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * ldx);
+  uint4* dst = reinterpret_cast<uint4*>(x_perm + r * H);
+  for (int v = lane; v < H / 8; v += 32) dst[v] = __ldg(src + v);
+}
+
 }  // namespace
 
 int launch_router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_router, int T, int D,
                          int E, int parts, float* logits, cudaStream_t s) {
   if (T <= 0) return MOE_OK;
+  if (static_cast<long long>(parts) * D <= kSmallMaxElems) {
+    const dim3 grid((T + kSmallTok - 1) / kSmallTok, (E + kSmallExp - 1) / kSmallExp);
+    const size_t smem = static_cast<size_t>(kSmallTok) * parts * D * 2;
+    static int configured_device = -1;
+    int dev = 0;
+    MOE_CUDA(cudaGetDevice(&dev));
+    if (configured_device != dev) {
+      MOE_CUDA(cudaFuncSetAttribute(k_router_logits_small,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmallTok * kSmallMaxElems * 2));
+      configured_device = dev;
+    }
+    return launch_pdl(k_router_logits_small, grid, dim3(32 * kSmallExp), smem, s, x,
+                      static_cast<long long>(ldx), w_router, T, D, E, parts, logits);
+  }
   const long long warps = static_cast<long long>((T + kTokPerWarp - 1) / kTokPerWarp) * E;
   const int threads = 256;
   const long long blocks = (warps * 32 + threads - 1) / threads;
@@ -176,6 +400,53 @@ int launch_topk(const float* logits, const float* bias, int T, int E, int k, int
   if (E <= 256) return launch_pdl(k_topk<8>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
   if (E <= 512) return launch_pdl(k_topk<16>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
   return launch_pdl(k_topk<32>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
+}
+
+bool route_fused_ok(int T, int D, int E, int k, int parts) {
+  return T >= 1 && T <= kFusedMaxT && E >= 1 && E <= kFusedMaxE && k <= 32 &&
+         static_cast<long long>(parts) * D <= kSmallMaxElems && D % 8 == 0;
+}
+
+size_t route_fused_sync_ints(int T) { return static_cast<size_t>((T + kSmallTok - 1) / kSmallTok) + 1; }
+
+int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
+                       const float* bias, int T, int D, int E, int k, int parts, float* logits,
+                       int32_t* idx, float* gates, uint8_t* tie, int32_t* counts,
+                       int32_t* offsets, int32_t* row_token, int32_t* slot_row, int* sync,
+                       cudaStream_t s) {
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  MOE_CUDA(cudaMemsetAsync(sync, 0, route_fused_sync_ints(T) * sizeof(int), s));
+  const dim3 grid((T + kSmallTok - 1) / kSmallTok, (E + kSmallExp - 1) / kSmallExp);
+  const int W = (T + 31) / 32;
+  const size_t smem = std::max(static_cast<size_t>(kSmallTok) * parts * D * 2,
+                               static_cast<size_t>(W) * E * 8);
+  const int perm = row_token != nullptr;
+  auto go = [&](auto kern) -> int {
+    static int configured_device = -1;
+    int dev = 0;
+    MOE_CUDA(cudaGetDevice(&dev));
+    if (configured_device != dev) {
+      MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmallTok * kSmallMaxElems * 2));
+      configured_device = dev;
+    }
+    return launch_pdl(kern, grid, dim3(256), smem, s, x, static_cast<long long>(ldx), w_router,
+                      bias, T, D, E, k, parts, logits, idx, gates, tie, perm, counts, offsets,
+                      row_token, slot_row, sync, status);
+  };
+  if (E <= 32) return go(k_route_small<1>);
+  if (E <= 64) return go(k_route_small<2>);
+  if (E <= 128) return go(k_route_small<4>);
+  return go(k_route_small<8>);
+}
+
+int launch_gather_rows(const int32_t* row_token, const uint16_t* x, int64_t ldx, int rows, int H,
+                       uint16_t* x_perm, cudaStream_t s) {
+  if (rows <= 0) return MOE_OK;
+  const long long threads = static_cast<long long>(rows) * 32;
+  return launch_pdl(k_gather_rows, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
+                    0, s, row_token, x, static_cast<long long>(ldx), rows, H, x_perm);
 }
 
 }  // namespace moe

@@ -75,6 +75,34 @@ def test_route(moe, T, D, E, k):
     _route_case(moe, T, D, E, k, seed=T + E)
 
 
+@pytest.mark.parametrize("T,D,E,k", [(64, 2688, 128, 6), (1, 256, 16, 2), (200, 512, 256, 8),
+                                     (33, 1024, 40, 3), (600, 256, 64, 4)])
+def test_route_dispatch(moe, T, D, E, k):
+    """moe_route_dispatch (one fused kernel for small batches, T <= 256 and E <= 256; the
+    separate route and permute kernels above that) against the oracle's route and permute."""
+    w = moe_synth.Workload("rd", T=T, H=D, E=E, k=k, F=64, seed=T + D + E)
+    inp = moe_synth.layer_inputs(w, with_experts=False)
+    idx, gates, tie, p = moe.moe_route_dispatch(to_dev(inp["x"]), to_dev(inp["w_router"]),
+                                                to_dev(inp["bias"]), k)
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    ref = O.route(inp["x"], inp["w_router"], inp["bias"], k)
+    gi = idx.cpu().numpy()
+    same = check_selection(gi, ref, inp["bias"], k)
+    g = gates.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(gates_by_expert(gi, g)[same],
+                               gates_by_expert(ref["idx"], ref["gates"])[same],
+                               rtol=1e-4, atol=1e-6)
+    # the dispatch maps are a function of the GPU's own selection: bit-exact against the
+    # oracle's permutation of that selection
+    pref = O.permute(gi, E)
+    for key in ("counts", "offsets", "row_token", "slot_row"):
+        np.testing.assert_array_equal(p[key].cpu().numpy(), pref[key], err_msg=key)
+    np.testing.assert_array_equal(moe_synth.from_torch_bf16(p["x_perm"]),
+                                  inp["x"][pref["row_token"]])
+    assert (tie.cpu().numpy() == (ref["gap"] < 1e-5)).mean() > 0.99
+
+
 def test_route_nano_prefill_full(moe):
     w = moe_synth.WORKLOADS["nano_prefill"]
     ties = _route_case(moe, w.T, w.H, w.E, w.k, w.seed, w.bias)
