@@ -742,6 +742,8 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   // Few rows per group: put the weights on the MMA's M side and the rows on N.
   const double avg_rows = static_cast<double>(g.rows) / gg.E;
   bool swap = g.force_mode == 2 || (g.force_mode == 0 && avg_rows <= 48.0);
+  // Many rows per group: 256 x 256 tiles on CTA pairs.
+  if (!swap && grouped_gemm_2sm_ok(g)) return launch_grouped_gemm_2sm(g, s);
   if (g.fp8) {
     if (swap) {
       if (avg_rows <= 16.0) return launch_variant<16, 10, true, false, true>(gg, ka, s);

@@ -1,0 +1,436 @@
+// grouped_gemm_2sm.cu: the rows-as-M grouped GEMM on CTA pairs (tcgen05 cta_group::2).
+//
+// The expert FFN contraction ("NVIDIA Nemotron 3: Efficient and Open Intelligence" notes,
+// §2.2) for batches with many rows per expert:
+//   out[r, n] = epi( scale * sum_k act[r, k] * w[e, n, k] )   for r in group e's row segment
+// A pair of CTAs (a cluster of two) computes a 256-row x 256-column tile: each CTA stages its
+// own 128 activation rows and its half (128 rows) of the weight tile, and one MMA of M = 256,
+// N = 256 reads both CTAs' shared memory and writes 128 accumulator rows into each CTA's TMEM.
+// Per SM that is 32 KB of operands per 512 MMA-cycles, half the weight bytes of a one-CTA
+// 128 x 256 tile.
+//
+// Roles (192 threads per CTA):
+//   warp 0 lane 0   TMA producer in both CTAs (6-stage ring, 128-byte swizzle). Each CTA
+//                   loads its halves of a stage into its own shared memory; both CTAs' loads
+//                   complete on the even CTA's stage barrier, which the even producer arms
+//                   with the byte count of the whole pair stage.
+//   warp 1 lane 0   even CTA: MMA issuer. It waits for the pair stage, issues the pair MMAs
+//                   and commits to the stage barriers of both CTAs at once.
+//   warps 2..5      epilogue in both CTAs: tcgen05.ld of the CTA's 128 accumulator rows,
+//                   scale/activation, bf16 stores, then a (remote) arrive on the even CTA's
+//                   accumulator-free barrier. The accumulator is double-buffered (2 x 256
+//                   TMEM columns).
+// Every mbarrier wait is bounded (the kernel then records MOE_ERR_TIMEOUT and returns); both
+// CTAs always reach the two cluster barriers (set-up and teardown).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "tc.cuh"
+#include "tc2.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;       // rows per CTA; a pair covers 256
+constexpr int PAIR_M = 256;
+constexpr int PAIR_N = 256;   // columns per pair tile; each CTA stages 128 weight rows
+constexpr int STAGES = 6;
+constexpr int NUM_THREADS = 192;
+constexpr int MAXG = 1024;
+constexpr uint32_t SLICE = 128;              // bytes of K per stage and row
+constexpr uint32_t A_BYTES = BM * SLICE;     // 16 KB
+constexpr uint32_t B_BYTES = 128 * SLICE;    // 16 KB
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_STRIDE = PAIR_N;
+
+struct KArgs2 {
+  const int* offsets;
+  int dense_rows;
+  int E, N, K;
+  int kpe;  // K elements per 128-byte slice: 64 (bf16) or 128 (E4M3)
+  int rows_total;
+  void* out;
+  long long ldo;
+  int epi;
+  const uint32_t* a_amax;
+  const float* w_scale;
+  uint32_t* out_amax;
+  int* status;
+};
+
+constexpr size_t smem_bytes2() {
+  return 1024 + size_t(STAGES) * (A_BYTES + B_BYTES) + (2 * STAGES + 4) * 8 + 16 +
+         3 * (MAXG + 1) * 4;
+}
+
+__device__ __forceinline__ void record2(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <bool F8>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tm_act,
+                       const __grid_constant__ CUtensorMap tm_w, const KArgs2 a) {
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(PAIR_M, PAIR_N) : idesc_bf16_f32(PAIR_M, PAIR_N);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);  // even CTA: pair stage
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;  // even CTA: both CTAs' epilogues have read the accumulator
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_pref = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_off = s_pref + (MAXG + 1);
+  int* s_cnt = s_off + (MAXG + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int E = a.E;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 8);  // one arrive per epilogue warp of either CTA
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_act);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc2(tmem_slot, TMEM_COLS);
+    tmem_relinquish2();
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  if (warp == 2) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int local = 0;
+    bool bad = false;
+    for (int e = e0; e < e1; ++e) {
+      const int lo = a.offsets ? a.offsets[e] : 0;
+      const int hi = a.offsets ? a.offsets[e + 1] : a.dense_rows;
+      int cnt = hi - lo;
+      if (lo < 0 || cnt < 0 || hi > a.rows_total) {
+        bad = true;
+        cnt = 0;
+      }
+      s_off[e] = lo;
+      s_cnt[e] = cnt;
+      local += (cnt + PAIR_M - 1) / PAIR_M;
+    }
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e1; ++e) {
+      s_pref[e] = run;
+      run += (s_cnt[e] + PAIR_M - 1) / PAIR_M;
+    }
+    if (lane == 31) s_pref[E] = incl;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record2(a.status, MOE_ERR_INVALID_ARG);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised and the pair's TMEM is allocated
+  tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_ct = (a.N + PAIR_N - 1) / PAIR_N;
+  const int total = s_pref[E] * n_ct;
+  const int KB = (a.K + a.kpe - 1) / a.kpe;
+  auto decode = [&](int tile, int& e, int& rt, int& ct) {
+    const int rtg = tile / n_ct;
+    ct = tile - rtg * n_ct;
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pref[mid + 1] > rtg)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    e = lo;
+    rt = rtg - s_pref[lo];
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ TMA producer
+      const uint64_t pol = policy_evict_last();
+      const uint32_t full0 = mapa_shared(full, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total; tile += npairs) {
+        int e, rt, ct;
+        decode(tile, e, rt, ct);
+        const int row0 = s_off[e] + rt * PAIR_M + static_cast<int>(rank) * BM;
+        const int col0 = ct * PAIR_N + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          // this stage's smem is free once the pair's MMAs that read it have completed
+          if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          // the odd CTA's bytes may land before this arming: the barrier's transaction count
+          // then dips below zero, but the phase cannot complete without this arrival
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
+          const int kc = kb * a.kpe;
+          tma2_load_2d(sA + stage * A_BYTES, &tm_act, full0 + stage * 8, kc, row0, pol);
+          tma2_load_3d(sB + stage * B_BYTES, &tm_w, full0 + stage * 8, kc, col0, e, pol);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record2(a.status, MOE_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // -------------------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total; tile += npairs) {
+        if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_cluster(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(sA + stage * A_BYTES));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K per 128-byte slice
+            if constexpr (F8)
+              umma2_e4m3(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb | kk) != 0);
+            else
+              umma2_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb | kk) != 0);
+          }
+          umma2_commit_both(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma2_commit_both(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record2(a.status, MOE_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const uint32_t remote_tempty = mapa_shared(tempty, 0);
+    float ascale = 1.f;
+    if constexpr (F8) ascale = __fdiv_rn(__uint_as_float(*a.a_amax), kFp8Div);
+    float vmax = 0.f;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < total; tile += npairs) {
+      int e, rt, ct;
+      decode(tile, e, rt, ct);
+      const int local = rt * PAIR_M + static_cast<int>(rank) * BM + m;
+      const bool valid = local < s_cnt[e];
+      const long long row = static_cast<long long>(s_off[e]) + local;
+      const int col0 = ct * PAIR_N;
+      const int ncols = min(PAIR_N, a.N - col0);
+      float scale = 1.f;
+      if constexpr (F8) scale = ascale * a.w_scale[e];
+      if (!mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag)) {
+        *abort_flag = 1;
+        record2(a.status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_STRIDE;
+      for (int n0 = 0; n0 < ncols; n0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tb + n0, r);
+        tmem_ld_wait();
+        if (!valid) continue;
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * scale;
+        if (a.epi == EPI_SQRELU_BF16) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float t = fmaxf(v[i], 0.f);
+            v[i] = t * t;
+            vmax = fmaxf(vmax, v[i]);
+          }
+        }
+        if (a.epi == EPI_F32) {
+          float4* p = reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * a.ldo + col0 + n0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        } else {
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) pk[i] = pack2_bf16(v[2 * i], v[2 * i + 1]);
+          uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * a.ldo + col0 + n0);
+          p[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          p[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(remote_tempty + acc * 8);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (a.out_amax) {
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, d));
+      if (lane == 0 && vmax > 0.f) atomicMax(a.out_amax, __float_as_uint(vmax));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no MMA of the pair is in flight and no epilogue still reads TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+bool grouped_gemm_2sm_ok(const GroupedGemm& g) {
+  if (g.row_token || g.precise || g.k_wrap || g.force_mode == 2) return false;
+  if (g.epi != EPI_BF16 && g.epi != EPI_SQRELU_BF16 && g.epi != EPI_F32) return false;
+  const int groups = g.offsets ? g.E : 1;
+  // a pair tile holds 256 rows: worth it with enough rows per group
+  return static_cast<double>(g.rows) / groups >= 256.0;
+}
+
+int launch_grouped_gemm_2sm(const GroupedGemm& g, cudaStream_t s) {
+  KArgs2 ka;
+  ka.offsets = g.offsets;
+  ka.dense_rows = g.rows;
+  ka.E = g.offsets ? g.E : 1;
+  ka.N = g.N;
+  ka.K = g.K;
+  ka.kpe = g.fp8 ? 128 : 64;
+  ka.rows_total = g.rows;
+  ka.out = g.out;
+  ka.ldo = g.ldo;
+  ka.epi = g.epi;
+  ka.a_amax = g.a_amax;
+  ka.w_scale = g.w_scale;
+  ka.out_amax = (g.fp8 && g.epi == EPI_SQRELU_BF16) ? g.out_amax : nullptr;
+  ka.status = status_word();
+  if (!ka.status) return MOE_ERR_CUDA;
+  const int E = g.offsets ? g.E : 1;
+  CUtensorMap tm_act, tm_w;
+  const CUtensorMapDataType dt = g.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t esz = g.fp8 ? 1 : 2;
+  const uint32_t box_k = static_cast<uint32_t>(ka.kpe);
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(g.act_ld) * esz};
+    const uint32_t box[2] = {box_k, BM};
+    if (!encode_tmap(&tm_act, dt, 2, g.act, dims, strides, box)) return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N),
+                              static_cast<uint64_t>(E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(g.K) * esz,
+                                 static_cast<uint64_t>(g.N) * g.K * esz};
+    const uint32_t box[3] = {box_k, 128, 1};
+    if (!encode_tmap(&tm_w, dt, 3, g.w, dims, strides, box)) return MOE_ERR_CUDA;
+  }
+  constexpr size_t smem = smem_bytes2();
+  static_assert(smem <= 232448, "shared memory per CTA");
+  auto kern = g.fp8 ? k_grouped_gemm_2sm<true> : k_grouped_gemm_2sm<false>;
+  static int configured[2] = {-1, -1};
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (configured[g.fp8 ? 1 : 0] != dev) {
+    MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(smem)));
+    configured[g.fp8 ? 1 : 0] = dev;
+  }
+  const long long pair_tiles = (static_cast<long long>(g.rows) / PAIR_M + E) *
+                               ((g.N + PAIR_N - 1) / PAIR_N);
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // the persistent grid is as many pairs as can be resident at once (pairs need two SMs of
+  // one GPC, so this can be below half the SM count); a second wave would double the time
+  static int max_pairs[2] = {0, 0}, max_pairs_dev[2] = {-1, -1};
+  const int v = g.fp8 ? 1 : 0;
+  if (max_pairs_dev[v] != dev) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    MOE_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+    max_pairs[v] = n > 0 ? n : 1;
+    max_pairs_dev[v] = dev;
+  }
+  const int pairs = static_cast<int>(pair_tiles < max_pairs[v] ? pair_tiles : max_pairs[v]);
+  if (pairs <= 0) return MOE_OK;
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, ka);
+  return e == cudaSuccess ? MOE_OK : cuda_status(e);
+}
+
+}  // namespace moe

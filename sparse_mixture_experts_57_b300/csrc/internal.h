@@ -123,6 +123,10 @@ struct GroupedGemm {
   uint32_t* out_amax = nullptr;
 };
 int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s);
+// The rows-as-M GEMM on CTA pairs (cta_group::2, 256 x 256 pair tiles): used by
+// launch_grouped_gemm for bf16/E4M3 GEMMs with at least 256 rows per group on average.
+bool grouped_gemm_2sm_ok(const GroupedGemm& g);
+int launch_grouped_gemm_2sm(const GroupedGemm& g, cudaStream_t s);
 // Whether a grouped GEMM of `rows` routed rows over E groups runs with the rows on the MMA's
 // M side (and can then gather its activation rows itself).
 bool grouped_gemm_rows_as_m(int rows, int E);
