@@ -77,7 +77,6 @@ template <bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tm_act,
                        const __grid_constant__ CUtensorMap tm_w, const KArgs2 a) {
-  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(PAIR_M, PAIR_N) : idesc_bf16_f32(PAIR_M, PAIR_N);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -162,6 +161,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int n_ct = (a.N + PAIR_N - 1) / PAIR_N;
   const int total = s_pref[E] * n_ct;
   const int KB = (a.K + a.kpe - 1) / a.kpe;
+  // MMA width of column tile ct: the last tile of a ragged N shrinks to a multiple of 32, its
+  // halves (nt / 2 weight rows) staged by the two CTAs as for a full tile
+  auto tile_n = [&](int ct) { return min(PAIR_N, (a.N - ct * PAIR_N + 31) & ~31); };
   auto decode = [&](int tile, int& e, int& rt, int& ct) {
     const int rtg = tile / n_ct;
     ct = tile - rtg * n_ct;
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int e, rt, ct;
         decode(tile, e, rt, ct);
         const int row0 = s_off[e] + rt * PAIR_M + static_cast<int>(rank) * BM;
-        const int col0 = ct * PAIR_N + static_cast<int>(rank) * 128;
+        const int col0 = ct * PAIR_N + static_cast<int>(rank) * (tile_n(ct) / 2);
         for (int kb = 0; kb < KB; ++kb) {
           // this stage's smem is free once the pair's MMAs that read it have completed
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -222,6 +224,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < total; tile += npairs) {
+        int e, rt, ct;
+        decode(tile, e, rt, ct);
+        const uint32_t idesc = F8 ? idesc_e4m3_f32(PAIR_M, tile_n(ct))
+                                  : idesc_bf16_f32(PAIR_M, tile_n(ct));
         if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -239,9 +245,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K per 128-byte slice
             if constexpr (F8)
-              umma2_e4m3(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb | kk) != 0);
+              umma2_e4m3(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
             else
-              umma2_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb | kk) != 0);
+              umma2_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
           }
           umma2_commit_both(&empty[stage]);
           if (++stage == STAGES) {

@@ -114,6 +114,8 @@ def _offsets(counts):
     ([40] * 30 + [700, 0], 512, 448),          # few rows per group (weights-as-M) and many
     ([3, 5, 1, 6] * 16, 2688, 1856),           # decode-like: Nano widths, ~4 rows per expert
     ([90, 410, 5, 260], 2688, 1856),           # Nano widths, rows-as-M
+    ([600, 0, 1, 300, 257, 500], 320, 448),    # >= 256 rows per group: CTA-pair tiles
+    ([1500, 700, 300], 2688, 1856),            # CTA-pair tiles at Nano widths
 ])
 def test_grouped_ffn_fp8(moe, counts, H, F):
     E = len(counts)

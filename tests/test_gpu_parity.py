@@ -164,6 +164,8 @@ def test_combine(moe, T, H, k):
     (700, 8, 3, 512, 448, 1.5),       # skewed, several row tiles, ragged tails
     (300, 32, 4, 320, 1856, 1.0),     # many N tiles with a ragged last tile
     (40, 128, 6, 2688, 1856, 0.0),    # decode-like: many experts with few rows
+    (1000, 8, 3, 320, 448, 1.0),      # >= 256 rows per expert: CTA-pair tiles, ragged N tail
+    (1200, 4, 2, 2688, 1856, 2.0),    # CTA-pair tiles at Nano widths, skewed
 ])
 def test_grouped_ffn(moe, T, E, k, H, F, skew):
     idx = moe_synth.random_topk(T * 3 + E, T, E, k, skew)
