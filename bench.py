@@ -529,7 +529,7 @@ def kernel_source_hash() -> str:
     import hashlib
     p = os.path.join(ROOT, "sparse_mixture_experts_57_b300", "csrc")
     h = hashlib.sha256()
-    for name in ("grouped_gemm.cu", "tc.cuh"):
+    for name in ("grouped_gemm.cu", "grouped_gemm_2sm.cu", "tc.cuh", "tc2.cuh"):
         with open(os.path.join(p, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()

@@ -148,17 +148,24 @@ __global__ void k_amax_bf16(const uint16_t* __restrict__ src, long long per_matr
   const int g = blockIdx.y;
   const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<long long>(g) * per_matrix);
   const long long nvec = per_matrix / 8;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   uint32_t m = 0u;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint4 v = __ldg(p + i);
+  auto fold = [&m](const uint4& v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      m = max(m, w[k] & 0x7fffu);
-      m = max(m, (w[k] >> 16) & 0x7fffu);
-    }
+    for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7fffu, (w[k] >> 16) & 0x7fffu));
+  };
+  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // four independent 16-byte loads in flight per thread
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    const uint4 v0 = __ldg(p + i), v1 = __ldg(p + i + stride), v2 = __ldg(p + i + 2 * stride),
+                v3 = __ldg(p + i + 3 * stride);
+    fold(v0);
+    fold(v1);
+    fold(v2);
+    fold(v3);
   }
+  for (; i < nvec; i += stride) fold(__ldg(p + i));
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
   // |bf16| bit patterns order like their values; as fp32 bits they keep that order.
@@ -329,7 +336,8 @@ int launch_amax_bf16(const uint16_t* src, long long elems_per_matrix, int G, uin
   if (G <= 0 || elems_per_matrix <= 0) return MOE_OK;
   const long long nvec = elems_per_matrix / 8;
   long long blocks = (nvec + 255) / 256;
-  const long long cap = 4LL * sm_count();  // with grid.y matrices, enough to fill the GPU
+  // one matrix: eight 256-thread blocks per SM; more matrices (grid.y) fill the GPU sooner
+  const long long cap = (G == 1 ? 8LL : 4LL) * sm_count();
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return launch_pdl(k_amax_bf16, dim3(static_cast<unsigned>(blocks), G), dim3(256), 0, s, src,

@@ -85,47 +85,83 @@ __global__ void k_router_logits(const uint16_t* __restrict__ x, long long ldx,
 constexpr int kSmallTok = 8, kSmallExp = 8;
 constexpr int kSmallMaxElems = 6144;  // staged elements per token row (all planes)
 
-__global__ void __launch_bounds__(256)
-    k_router_logits_small(const uint16_t* __restrict__ x, long long ldx,
-                          const uint16_t* __restrict__ w, int T, int D, int E, int parts,
-                          float* __restrict__ logits) {
-  griddep_wait();
-  griddep_launch_dependents();
-  extern __shared__ uint4 sx[];  // [kSmallTok][parts * D / 8]
-  const int t0 = blockIdx.x * kSmallTok;
-  const int nvec = D / 8, rowv = parts * nvec;
-  for (int i = threadIdx.x; i < kSmallTok * rowv; i += blockDim.x) {
+// Router logits of the 8 tokens t0.. against expert e (one warp per expert): the tokens are
+// staged in shared memory (sx), then each lane takes every 32nd 16-byte vector of the
+// expert's row, in ascending order. The row is streamed through a ring of kAhead registers
+// refilled one vector per iteration, so kAhead loads stay in flight while the loop body stays
+// small (these kernels run once per layer with a cold instruction cache: unrolling the
+// 8-token x kAhead-vector product multiplies the code that every SM must fetch).
+// Every thread of the CTA must call this.
+template <int PARTS>
+__device__ __forceinline__ void logits_tile(const uint16_t* __restrict__ x, long long ldx,
+                                            const uint16_t* __restrict__ w, int T, int D, int E,
+                                            int t0, uint4* sx, float* __restrict__ logits) {
+  constexpr int kAhead = 8;
+  const int nvec = D / 8, rowv = PARTS * nvec, n = kSmallTok * rowv;
+  const int nt = blockDim.x;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  auto xload = [&](int i) {
     const int t = i / rowv, v = i - t * rowv;
-    sx[i] = t0 + t < T ? __ldg(reinterpret_cast<const uint4*>(x + (t0 + t) * ldx) + v)
-                       : make_uint4(0u, 0u, 0u, 0u);
+    return t0 + t < T ? __ldg(reinterpret_cast<const uint4*>(x + (t0 + t) * ldx) + v) : zero;
+  };
+  int i = threadIdx.x;
+#pragma unroll 1
+  for (; i + 3 * nt < n; i += 4 * nt) {
+    const uint4 a = xload(i), b = xload(i + nt), c = xload(i + 2 * nt), d = xload(i + 3 * nt);
+    sx[i] = a;
+    sx[i + nt] = b;
+    sx[i + 2 * nt] = c;
+    sx[i + 3 * nt] = d;
   }
+#pragma unroll 1
+  for (; i < n; i += nt) sx[i] = xload(i);
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.y * kSmallExp + (threadIdx.x >> 5);
   if (e >= E) return;
   const uint4* wrow = reinterpret_cast<const uint4*>(w + static_cast<long long>(e) * D);
+  uint4 ring[kAhead];
+#pragma unroll
+  for (int j = 0; j < kAhead; ++j) ring[j] = lane + 32 * j < nvec ? __ldg(wrow + lane + 32 * j) : zero;
   float acc[kSmallTok];
 #pragma unroll
-  for (int i = 0; i < kSmallTok; ++i) acc[i] = 0.f;
-#pragma unroll 2
+  for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
+#pragma unroll 1
   for (int v = lane; v < nvec; v += 32) {
-    const uint4 wv = __ldg(wrow + v);
+    const uint4 wv = ring[0];
 #pragma unroll
-    for (int i = 0; i < kSmallTok; ++i)
-      for (int p = 0; p < parts; ++p) acc[i] = dot8(sx[i * rowv + p * nvec + v], wv, acc[i]);
+    for (int j = 0; j + 1 < kAhead; ++j) ring[j] = ring[j + 1];
+    const int vn = v + 32 * kAhead;
+    ring[kAhead - 1] = vn < nvec ? __ldg(wrow + vn) : zero;
+#pragma unroll
+    for (int t = 0; t < kSmallTok; ++t) {
+#pragma unroll
+      for (int p = 0; p < PARTS; ++p) acc[t] = dot8(sx[t * rowv + p * nvec + v], wv, acc[t]);
+    }
   }
 #pragma unroll
-  for (int i = 0; i < kSmallTok; ++i) {
+  for (int t = 0; t < kSmallTok; ++t) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
   }
   if (lane < kSmallTok && t0 + lane < T) {
     float v = acc[0];
 #pragma unroll
-    for (int i = 1; i < kSmallTok; ++i)
-      if (lane == i) v = acc[i];
+    for (int t = 1; t < kSmallTok; ++t)
+      if (lane == t) v = acc[t];
     logits[static_cast<long long>(t0 + lane) * E + e] = v;
   }
+}
+
+template <int PARTS>
+__global__ void __launch_bounds__(256)
+    k_router_logits_small(const uint16_t* __restrict__ x, long long ldx,
+                          const uint16_t* __restrict__ w, int T, int D, int E,
+                          float* __restrict__ logits) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ uint4 sx[];  // [kSmallTok][PARTS * D / 8]
+  logits_tile<PARTS>(x, ldx, w, T, D, E, blockIdx.x * kSmallTok, sx, logits);
 }
 
 // Top-k of one token, by one warp. Each lane holds experts e = lane + 32*i. The k best
@@ -227,10 +263,10 @@ __global__ void k_topk(const float* __restrict__ logits, const float* __restrict
 // (sync[0 .. groups]) must be zero at entry and are zero again at exit.
 constexpr int kFusedMaxT = 256, kFusedMaxE = 256;
 
-template <int VPL>
+template <int VPL, int PARTS>
 __global__ void __launch_bounds__(256)
     k_route_small(const uint16_t* __restrict__ x, long long ldx, const uint16_t* __restrict__ w,
-                  const float* __restrict__ bias, int T, int D, int E, int k, int parts,
+                  const float* __restrict__ bias, int T, int D, int E, int k,
                   float* __restrict__ logits, int32_t* __restrict__ idx,
                   float* __restrict__ gates, uint8_t* __restrict__ tie, int perm,
                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -241,44 +277,10 @@ __global__ void __launch_bounds__(256)
   extern __shared__ uint4 sx[];
   __shared__ int s_flag;
   __shared__ int warp_sums[33];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int t0 = blockIdx.x * kSmallTok;
   // 1. logits tile
-  {
-    const int nvec = D / 8, rowv = parts * nvec;
-    for (int i = tid; i < kSmallTok * rowv; i += blockDim.x) {
-      const int t = i / rowv, v = i - t * rowv;
-      sx[i] = t0 + t < T ? __ldg(reinterpret_cast<const uint4*>(x + (t0 + t) * ldx) + v)
-                         : make_uint4(0u, 0u, 0u, 0u);
-    }
-    __syncthreads();
-    const int e = blockIdx.y * kSmallExp + warp;
-    if (e < E) {
-      const uint4* wrow = reinterpret_cast<const uint4*>(w + static_cast<long long>(e) * D);
-      float acc[kSmallTok];
-#pragma unroll
-      for (int i = 0; i < kSmallTok; ++i) acc[i] = 0.f;
-#pragma unroll 2
-      for (int v = lane; v < nvec; v += 32) {
-        const uint4 wv = __ldg(wrow + v);
-#pragma unroll
-        for (int i = 0; i < kSmallTok; ++i)
-          for (int p = 0; p < parts; ++p) acc[i] = dot8(sx[i * rowv + p * nvec + v], wv, acc[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < kSmallTok; ++i) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
-      }
-      if (lane < kSmallTok && t0 + lane < T) {
-        float v = acc[0];
-#pragma unroll
-        for (int i = 1; i < kSmallTok; ++i)
-          if (lane == i) v = acc[i];
-        logits[static_cast<long long>(t0 + lane) * E + e] = v;
-      }
-    }
-  }
+  logits_tile<PARTS>(x, ldx, w, T, D, E, t0, sx, logits);
   // 2. the last CTA of this token group: top-k of its tokens
   __threadfence();
   __syncthreads();
@@ -358,6 +360,7 @@ __global__ void k_gather_rows(const int32_t* __restrict__ row_token, const uint1
   const int t = row_token[r];
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * ldx);
   uint4* dst = reinterpret_cast<uint4*>(x_perm + r * H);
+#pragma unroll 4
   for (int v = lane; v < H / 8; v += 32) dst[v] = __ldg(src + v);
 }
 
@@ -366,20 +369,22 @@ __global__ void k_gather_rows(const int32_t* __restrict__ row_token, const uint1
 int launch_router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_router, int T, int D,
                          int E, int parts, float* logits, cudaStream_t s) {
   if (T <= 0) return MOE_OK;
-  if (static_cast<long long>(parts) * D <= kSmallMaxElems) {
+  if ((parts == 1 || parts == 3) && static_cast<long long>(parts) * D <= kSmallMaxElems) {
     const dim3 grid((T + kSmallTok - 1) / kSmallTok, (E + kSmallExp - 1) / kSmallExp);
     const size_t smem = static_cast<size_t>(kSmallTok) * parts * D * 2;
-    static int configured_device = -1;
-    int dev = 0;
-    MOE_CUDA(cudaGetDevice(&dev));
-    if (configured_device != dev) {
-      MOE_CUDA(cudaFuncSetAttribute(k_router_logits_small,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kSmallTok * kSmallMaxElems * 2));
-      configured_device = dev;
-    }
-    return launch_pdl(k_router_logits_small, grid, dim3(32 * kSmallExp), smem, s, x,
-                      static_cast<long long>(ldx), w_router, T, D, E, parts, logits);
+    auto go = [&](auto kern) -> int {
+      static int configured_device = -1;
+      int dev = 0;
+      MOE_CUDA(cudaGetDevice(&dev));
+      if (configured_device != dev) {
+        MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kSmallTok * kSmallMaxElems * 2));
+        configured_device = dev;
+      }
+      return launch_pdl(kern, grid, dim3(32 * kSmallExp), smem, s, x,
+                        static_cast<long long>(ldx), w_router, T, D, E, logits);
+    };
+    return parts == 1 ? go(k_router_logits_small<1>) : go(k_router_logits_small<3>);
   }
   const long long warps = static_cast<long long>((T + kTokPerWarp - 1) / kTokPerWarp) * E;
   const int threads = 256;
@@ -404,6 +409,7 @@ int launch_topk(const float* logits, const float* bias, int T, int E, int k, int
 
 bool route_fused_ok(int T, int D, int E, int k, int parts) {
   return T >= 1 && T <= kFusedMaxT && E >= 1 && E <= kFusedMaxE && k <= 32 &&
+         (parts == 1 || parts == 3) &&
          static_cast<long long>(parts) * D <= kSmallMaxElems && D % 8 == 0;
 }
 
@@ -432,13 +438,19 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
       configured_device = dev;
     }
     return launch_pdl(kern, grid, dim3(256), smem, s, x, static_cast<long long>(ldx), w_router,
-                      bias, T, D, E, k, parts, logits, idx, gates, tie, perm, counts, offsets,
+                      bias, T, D, E, k, logits, idx, gates, tie, perm, counts, offsets,
                       row_token, slot_row, sync, status);
   };
-  if (E <= 32) return go(k_route_small<1>);
-  if (E <= 64) return go(k_route_small<2>);
-  if (E <= 128) return go(k_route_small<4>);
-  return go(k_route_small<8>);
+  if (parts == 3) {
+    if (E <= 32) return go(k_route_small<1, 3>);
+    if (E <= 64) return go(k_route_small<2, 3>);
+    if (E <= 128) return go(k_route_small<4, 3>);
+    return go(k_route_small<8, 3>);
+  }
+  if (E <= 32) return go(k_route_small<1, 1>);
+  if (E <= 64) return go(k_route_small<2, 1>);
+  if (E <= 128) return go(k_route_small<4, 1>);
+  return go(k_route_small<8, 1>);
 }
 
 int launch_gather_rows(const int32_t* row_token, const uint16_t* x, int64_t ldx, int rows, int H,
