@@ -213,7 +213,8 @@ int launch_topk(const float* logits, const float* bias, int T, int E, int k, int
 
 // Small batches (T <= 256, E <= 256): router logits, top-k and, when row_token is set, the
 // dispatch maps (counts, offsets, row_token, slot_row) in one kernel. `sync` holds
-// route_fused_sync_ints(T) ints of scratch (zeroed by the launch).
+// route_fused_sync_ints(T) ints of 8-byte aligned scratch; its contents at entry do not
+// matter (generation-tagged counters).
 bool route_fused_ok(int T, int D, int E, int k, int parts);
 size_t route_fused_sync_ints(int T);
 int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,

@@ -12,6 +12,9 @@
 
 #include <algorithm>
 
+#include <atomic>
+#include <cstdint>
+
 #include "internal.h"
 #include "scan.cuh"
 
@@ -259,9 +262,27 @@ __global__ void k_topk(const float* __restrict__ logits, const float* __restrict
 //  3. with perm set, the last token group to finish builds the dispatch maps for all tokens
 //     in shared memory: per-expert counts and offsets, then row_token / slot_row with rows of
 //     one expert in ascending token order (a token-word x expert bit matrix, as moe_permute).
-// Which CTA takes steps 2 and 3 depends on timing; what they compute does not. The counters
-// (sync[0 .. groups]) must be zero at entry and are zero again at exit.
+// Which CTA takes steps 2 and 3 depends on timing; what they compute does not.
+// "Last" is decided by flags rather than counters: each CTA stores the launch's generation
+// tag `gen` (a new nonzero 64-bit value per launch) into its own flag word, fences, and reads
+// its peers' flags; the SC fences guarantee that at least one CTA sees every flag set. Two
+// CTAs may both see it; both then compute and store the same values. Flags holding another
+// tag count as unset, so the scratch needs no clearing before a launch; the CTAs that finish
+// a step store 0 into its flags again (a captured graph that replays one tag finds them clear).
 constexpr int kFusedMaxT = 256, kFusedMaxE = 256;
+constexpr int kFusedGroups = kFusedMaxT / kSmallTok;    // token groups (grid.x) at most
+constexpr int kFusedExpGroups = kFusedMaxE / kSmallExp;  // expert groups (grid.y) at most
+
+// Warp-wide: store this CTA's flag (slot `mine` of `flags`), then true on every lane if all
+// n flags hold gen.
+__device__ __forceinline__ bool flag_all_set(unsigned long long* flags, int mine, int n,
+                                             unsigned long long gen) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) __stcg(flags + mine, gen);
+  __threadfence();
+  const bool set = lane >= n || lane == mine || __ldcg(flags + lane) == gen;
+  return __all_sync(0xffffffffu, set);
+}
 
 template <int VPL, int PARTS>
 __global__ void __launch_bounds__(256)
@@ -271,32 +292,42 @@ __global__ void __launch_bounds__(256)
                   float* __restrict__ gates, uint8_t* __restrict__ tie, int perm,
                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                   int32_t* __restrict__ row_token, int32_t* __restrict__ slot_row,
-                  int* __restrict__ sync, int* status) {
+                  unsigned long long* __restrict__ sync, unsigned long long gen, int* status) {
   griddep_wait();
   griddep_launch_dependents();
   extern __shared__ uint4 sx[];
   __shared__ int s_flag;
   __shared__ int warp_sums[33];
+  __shared__ float s_bias[kFusedMaxE];  // fetched now: only the last CTA of a group uses it
   const int tid = threadIdx.x, warp = tid >> 5;
   const int t0 = blockIdx.x * kSmallTok;
+  for (int e = tid; e < E; e += blockDim.x) s_bias[e] = __ldg(bias + e);
   // 1. logits tile
   logits_tile<PARTS>(x, ldx, w, T, D, E, t0, sx, logits);
   // 2. the last CTA of this token group: top-k of its tokens
-  __threadfence();
+  unsigned long long* gflags = sync + blockIdx.x * kFusedExpGroups;  // [grid.y] per group
+  unsigned long long* tflags = sync + kFusedGroups * kFusedExpGroups;  // [grid.x]
+  __threadfence();  // this thread's logits before the CTA's flag
   __syncthreads();
-  if (tid == 0) s_flag = atomicAdd(sync + blockIdx.x, 1) == static_cast<int>(gridDim.y) - 1;
+  if (warp == 0) {
+    const bool all = flag_all_set(gflags, blockIdx.y, gridDim.y, gen);
+    if (tid == 0) s_flag = all;
+  }
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
   if (warp < kSmallTok && t0 + warp < T)
-    topk_token<VPL, true>(logits + static_cast<long long>(t0 + warp) * E, bias, t0 + warp, E, k,
-                          idx, gates, tie);
-  if (tid == 0) sync[blockIdx.x] = 0;
+    topk_token<VPL, true>(logits + static_cast<long long>(t0 + warp) * E, s_bias, t0 + warp, E,
+                          k, idx, gates, tie);
+  if (tid < static_cast<int>(gridDim.y)) __stcg(gflags + tid, 0ull);
   if (!perm) return;
   // 3. the last token group: dispatch maps for all tokens
-  __threadfence();
+  __threadfence();  // this thread's top-k results before the group's flag
   __syncthreads();
-  if (tid == 0) s_flag = atomicAdd(sync + gridDim.x, 1) == static_cast<int>(gridDim.x) - 1;
+  if (warp == 0) {
+    const bool all = flag_all_set(tflags, blockIdx.x, gridDim.x, gen);
+    if (tid == 0) s_flag = all;
+  }
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
@@ -346,7 +377,7 @@ __global__ void __launch_bounds__(256)
     row_token[row] = t;
     slot_row[i] = row;
   }
-  if (tid == 0) sync[gridDim.x] = 0;
+  if (tid < static_cast<int>(gridDim.x)) __stcg(tflags + tid, 0ull);
 }
 
 // x_perm[r, :] = x[row_token[r], :], one warp per row (16-byte vectors).
@@ -413,7 +444,11 @@ bool route_fused_ok(int T, int D, int E, int k, int parts) {
          static_cast<long long>(parts) * D <= kSmallMaxElems && D % 8 == 0;
 }
 
-size_t route_fused_sync_ints(int T) { return static_cast<size_t>((T + kSmallTok - 1) / kSmallTok) + 1; }
+// 64-bit flag words (per token group: one per expert group; one per token group), as pairs
+// of ints
+size_t route_fused_sync_ints(int) {
+  return 2 * static_cast<size_t>(kFusedGroups * kFusedExpGroups + kFusedGroups);
+}
 
 int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
                        const float* bias, int T, int D, int E, int k, int parts, float* logits,
@@ -422,7 +457,9 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
                        cudaStream_t s) {
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
-  MOE_CUDA(cudaMemsetAsync(sync, 0, route_fused_sync_ints(T) * sizeof(int), s));
+  if (reinterpret_cast<uintptr_t>(sync) % 8) return MOE_ERR_UNSUPPORTED;
+  static std::atomic<unsigned long long> launches{0};
+  const unsigned long long gen = (launches.fetch_add(1) % ((1ull << 48) - 1)) + 1;  // never 0
   const dim3 grid((T + kSmallTok - 1) / kSmallTok, (E + kSmallExp - 1) / kSmallExp);
   const int W = (T + 31) / 32;
   const size_t smem = std::max(static_cast<size_t>(kSmallTok) * parts * D * 2,
@@ -439,7 +476,8 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
     }
     return launch_pdl(kern, grid, dim3(256), smem, s, x, static_cast<long long>(ldx), w_router,
                       bias, T, D, E, k, logits, idx, gates, tie, perm, counts, offsets,
-                      row_token, slot_row, sync, status);
+                      row_token, slot_row, reinterpret_cast<unsigned long long*>(sync), gen,
+                      status);
   };
   if (parts == 3) {
     if (E <= 32) return go(k_route_small<1, 3>);
