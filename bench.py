@@ -504,8 +504,9 @@ def run_ours(args, w: moe_synth.Workload):
 
 def read_traffic(workload: str, units: int):
     """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it still
-    describes the current kernel source (else null). The summary gives bytes per unit
-    (touched expert matrix) measured on a scaled case; a launch moves `units` of them."""
+    describes the current kernel source (else null). The summary gives either bytes per
+    launch measured on this workload's full-size launches, or bytes per unit (touched
+    expert matrix), in which case a launch moves `units` of them."""
     if "[" in workload:          # scaled cases have no committed counters
         return None
     path = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}.md")
@@ -518,11 +519,15 @@ def read_traffic(workload: str, units: int):
     for line in txt.splitlines():
         if line.startswith("traffic_bytes_per_unit:"):
             vals["t"] = float(line.split(":", 1)[1])
+        if line.startswith("traffic_bytes_per_launch:"):
+            vals["l"] = float(line.split(":", 1)[1])
         if line.startswith("kernel_source_sha256:"):
             vals["h"] = line.split(":", 1)[1].strip()
-    if "t" not in vals or vals.get("h") != kernel_source_hash():
+    if vals.get("h") != kernel_source_hash():
         return None
-    return vals["t"] * units
+    if "l" in vals:                # measured on this workload's full-size launches
+        return vals["l"]
+    return vals["t"] * units if "t" in vals else None
 
 
 def kernel_source_hash() -> str:
