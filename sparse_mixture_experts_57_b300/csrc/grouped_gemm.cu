@@ -35,7 +35,11 @@ constexpr int BM = 128;  // MMA M
 constexpr int BK = 64;   // K per pipeline stage: one 128-byte swizzle row of bf16
 constexpr int UK = 16;   // K per tcgen05.mma for 16-bit inputs
 constexpr int MAX_GROUPS = 1024;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 192;          // producer, MMA issuer, 4 epilogue warps
+constexpr int NUM_THREADS_CHUNKED = 320;  // producer, MMA issuer, 8 epilogue warps
+__host__ __device__ constexpr int kernel_threads(bool chunked) {
+  return chunked ? NUM_THREADS_CHUNKED : NUM_THREADS;
+}
 
 struct KArgs {
   const int* offsets;
@@ -194,7 +198,7 @@ __device__ __forceinline__ void store_one(const KArgs& a, long long row, int col
 // lane 0 issues the copies. Rows past the group's end gather an out-of-range row (zeros).
 template <int BN, int STAGES, bool SWAP, bool CHUNKED = false, bool F8 = false,
           bool GATHER = false>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tm_act,
                    const __grid_constant__ CUtensorMap tm_w, const KArgs a) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
@@ -208,7 +212,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   static_assert(!(F8 && CHUNKED), "E4M3 kernels have no chunked variant");
   static_assert(!GATHER || (!SWAP && !CHUNKED && !F8), "gathered rows: bf16 rows-as-M only");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
-  static_assert(!CHUNKED || (!SWAP && BN <= 128), "chunked accumulation: rows-as-M, BN <= 128");
+  static_assert(!CHUNKED || (!SWAP && BN % 128 == 0),
+                "chunked accumulation: rows-as-M, BN 128 or 256");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], kernel_threads(CHUNKED) - 64);  // every epilogue thread
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -449,11 +454,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const long long row0 = static_cast<long long>(s_off[e]) + rbeg;
       const int col0 = ct * CT;
       if constexpr (CHUNKED) {
-        const int ncols = min(BN, a.N - col0);
+        // eight epilogue warps: two per TMEM lane quadrant, each summing half the columns
+        constexpr int HB = BN / 2;
+        const int hc0 = ((warp - 2) >> 2) * HB;  // this warp's first column in the tile
+        const int ncols = min(BN, a.N - col0) - hc0;
         const int nchunks = (KB + a.kchunk - 1) / a.kchunk;
-        float sum[BN];
+        float sum[HB];
 #pragma unroll
-        for (int i = 0; i < BN; ++i) sum[i] = 0.f;
+        for (int i = 0; i < HB; ++i) sum[i] = 0.f;
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
           if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
@@ -463,15 +471,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t tb =
               tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_STRIDE;
+          // two loads in flight per wait. Columns past ncols (inside the accumulator) are
+          // summed too and never stored.
 #pragma unroll
-          for (int j = 0; j < BN / 16; ++j) {
-            if (j * 16 < ncols) {
-              uint32_t r[16];
-              tmem_ld16(tb + j * 16, r);
-              tmem_ld_wait();
+          for (int jb = 0; jb < HB / 32; ++jb) {
+            uint32_t r[2][16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) sum[j * 16 + i] += __uint_as_float(r[i]);
-            }
+            for (int u = 0; u < 2; ++u) tmem_ld16(tb + hc0 + jb * 32 + u * 16, r[u]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+              for (int i = 0; i < 16; ++i) sum[jb * 32 + u * 16 + i] += __uint_as_float(r[u][i]);
           }
           tc_fence_before();
           mbar_arrive(&tempty[acc]);
@@ -487,8 +498,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (m < valid_rows) {
 #pragma unroll
-          for (int j = 0; j < BN / 16; ++j)
-            if (j * 16 < ncols) store_row16(a, row0 + m, col0 + j * 16, sum + j * 16);
+          for (int j = 0; j < HB / 16; ++j)
+            if (j * 16 < ncols) store_row16(a, row0 + m, col0 + hc0 + j * 16, sum + j * 16);
         }
         continue;
       }
@@ -654,7 +665,7 @@ int launch_variant(const GroupedGemm& g, const KArgs& ka, cudaStream_t s) {
   const long long tiles = row_tiles * ((g.N + CT - 1) / CT);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   if (grid <= 0) return MOE_OK;
-  return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), smem, s, tm_act, tm_w, ka);
+  return launch_pdl(kern, dim3(grid), dim3(kernel_threads(CHUNKED)), smem, s, tm_act, tm_w, ka);
 }
 
 int pick_bn_rows_as_m(int N) {
@@ -730,7 +741,9 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   GroupedGemm gg = g;
   if (!g.offsets) gg.E = 1;
 
-  if (g.precise) return launch_variant<128, 6, false, true>(gg, ka, s);
+  if (g.precise)  // 256-wide tiles halve the operand bytes per MMA cycle of 128-wide ones
+    return g.N > 128 ? launch_variant<256, 4, false, true>(gg, ka, s)
+                     : launch_variant<128, 6, false, true>(gg, ka, s);
   if (g.row_token) {  // gathered activation rows: always rows-as-M
     switch (pick_bn_rows_as_m(g.N)) {
       case 256: return launch_variant<256, 4, false, false, false, true>(gg, ka, s);

@@ -243,15 +243,138 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ row,
   if (tie && lane == 0) tie[t] = (k < E && (uk - uk1) < 1e-5f) ? 1 : 0;
 }
 
+// Order-preserving map of a float (not NaN, not -0) to uint32 and back.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// The same selection as topk_token (order by biased score descending, lower index first on
+// equal scores; identical outputs) for many experts per lane: instead of k + 1 arg-max
+// rounds over all E scores, the k-th largest score is found bit by bit on order-preserving
+// keys (32 rounds of a per-lane count and a warp sum), the k winners are compacted into
+// lanes 0..k-1 in index order, ranked among themselves, and moved to lane = rank.
+template <int VPL, bool CG>
+__device__ __forceinline__ void topk_token_select(const float* __restrict__ row,
+                                                  const float* __restrict__ bias, long long t,
+                                                  int E, int k, int32_t* __restrict__ idx,
+                                                  float* __restrict__ gates,
+                                                  uint8_t* __restrict__ tie) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  float s[VPL];
+  uint32_t key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float z = CG ? __ldcg(row + e) : row[e];
+      s[i] = 1.f / (1.f + expf(-z));
+      const float ui = s[i] + bias[e];
+      // NaN never wins; -0 cannot arise (s > 0) but would compare equal to +0: fold it
+      key[i] = order_key((ui == ui) ? ui + 0.f : -INFINITY);
+    } else {
+      s[i] = 0.f;
+      key[i] = 0u;  // below every valid key (the key of -inf is 0x007fffff)
+    }
+  }
+  // 1. kth = the k-th largest key
+  uint32_t kth = 0u;
+#pragma unroll 1
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t cand = kth | (1u << b);
+    uint32_t c = 0u;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) c += key[i] >= cand ? 1u : 0u;
+    if (__reduce_add_sync(0xffffffffu, c) >= static_cast<uint32_t>(k)) kth = cand;
+  }
+  uint32_t gt = 0u, eq = 0u, below = 0u;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    gt += key[i] > kth ? 1u : 0u;
+    eq += key[i] == kth ? 1u : 0u;
+    if (key[i] < kth) below = max(below, key[i]);
+  }
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  eq = __reduce_add_sync(0xffffffffu, eq);
+  below = __reduce_max_sync(0xffffffffu, below);
+  const uint32_t need_eq = static_cast<uint32_t>(k) - gt;  // >= 1 equal keys are taken
+  const float uk = key_float(kth);
+  const float uk1 = eq > need_eq ? uk : key_float(below);
+  // 2. compact the winners into lanes 0..k-1 in index order (e = lane + 32 i: i major)
+  uint32_t my_key = 0u, base = 0u, eq_seen = 0u;
+  int my_e = 0;
+  float my_s = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const uint32_t eqm = __ballot_sync(0xffffffffu, key[i] == kth);
+    const bool win = key[i] > kth ||
+                     (key[i] == kth && eq_seen + __popc(eqm & lt_mask) < need_eq);
+    eq_seen += __popc(eqm);
+    const uint32_t m = __ballot_sync(0xffffffffu, win);
+    const uint32_t n = __popc(m);
+    const bool mine = lane >= static_cast<int>(base) && lane < static_cast<int>(base + n);
+    const int src = mine ? static_cast<int>(__fns(m, 0u, lane - static_cast<int>(base) + 1)) : lane;
+    const uint32_t kv = __shfl_sync(0xffffffffu, key[i], src);
+    const float sv = __shfl_sync(0xffffffffu, s[i], src);
+    if (mine) {
+      my_key = kv;
+      my_e = src + 32 * i;
+      my_s = sv;
+    }
+    base += n;
+  }
+  // 3. rank among the k winners: higher key first, then lower index
+  int rank = 0;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t kj = __shfl_sync(0xffffffffu, my_key, j);
+    const int ej = __shfl_sync(0xffffffffu, my_e, j);
+    rank += (kj > my_key || (kj == my_key && ej < my_e)) ? 1 : 0;
+  }
+  // 4. lane r takes the winner of rank r
+  int from = 0;
+  for (int j = 0; j < k; ++j) {
+    const int rj = __shfl_sync(0xffffffffu, rank, j);
+    if (rj == lane) from = j;
+  }
+  my_e = __shfl_sync(0xffffffffu, my_e, from);
+  my_s = __shfl_sync(0xffffffffu, my_s, from);
+  float sum = lane < k ? my_s : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    idx[t * k + lane] = my_e;
+    gates[t * k + lane] = my_s / sum;
+  }
+  if (tie && lane == 0) tie[t] = (k < E && (uk - uk1) < 1e-5f) ? 1 : 0;
+}
+
+// k + 1 arg-max rounds cost about (k + 1)(5 VPL + 40) instructions per token, the bitwise
+// selection about 32 (2 VPL + 8) + 15 VPL + 5 k + 100.
 template <int VPL>
-__global__ void k_topk(const float* __restrict__ logits, const float* __restrict__ bias, int T,
+__device__ __forceinline__ bool use_select(int k) {
+  return (k + 1) * (5 * VPL + 40) > 32 * (2 * VPL + 8) + 15 * VPL + 5 * k + 100;
+}
+
+// One token per warp; each warp's work is a dependent chain (k-th-key rounds or arg-max
+// rounds), so the kernel runs on latency and residency: the register cap keeps four
+// 256-thread CTAs per SM (two for 32 experts per lane, whose scores would not fit).
+template <int VPL>
+__global__ void __launch_bounds__(256, VPL >= 32 ? 2 : 4)
+    k_topk(const float* __restrict__ logits, const float* __restrict__ bias, int T,
                        int E, int k, int32_t* __restrict__ idx, float* __restrict__ gates,
                        uint8_t* __restrict__ tie) {
   griddep_wait();
   griddep_launch_dependents();
   const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
-  topk_token<VPL, false>(logits + t * E, bias, t, E, k, idx, gates, tie);
+  if (use_select<VPL>(k))
+    topk_token_select<VPL, false>(logits + t * E, bias, t, E, k, idx, gates, tie);
+  else
+    topk_token<VPL, false>(logits + t * E, bias, t, E, k, idx, gates, tie);
 }
 
 // Small batches, routing and dispatch maps in one kernel. Grid (token groups of 8, expert
@@ -316,9 +439,13 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
-  if (warp < kSmallTok && t0 + warp < T)
-    topk_token<VPL, true>(logits + static_cast<long long>(t0 + warp) * E, s_bias, t0 + warp, E,
-                          k, idx, gates, tie);
+  if (warp < kSmallTok && t0 + warp < T) {
+    const float* row = logits + static_cast<long long>(t0 + warp) * E;
+    if (use_select<VPL>(k))
+      topk_token_select<VPL, true>(row, s_bias, t0 + warp, E, k, idx, gates, tie);
+    else
+      topk_token<VPL, true>(row, s_bias, t0 + warp, E, k, idx, gates, tie);
+  }
   if (tid < static_cast<int>(gridDim.y)) __stcg(gflags + tid, 0ull);
   if (!perm) return;
   // 3. the last token group: dispatch maps for all tokens

@@ -76,7 +76,7 @@ def test_route(moe, T, D, E, k):
 
 
 @pytest.mark.parametrize("T,D,E,k", [(64, 2688, 128, 6), (1, 256, 16, 2), (200, 512, 256, 8),
-                                     (33, 1024, 40, 3), (600, 256, 64, 4)])
+                                     (33, 1024, 40, 3), (600, 256, 64, 4), (100, 512, 256, 16)])
 def test_route_dispatch(moe, T, D, E, k):
     """moe_route_dispatch (one fused kernel for small batches, T <= 256 and E <= 256; the
     separate route and permute kernels above that) against the oracle's route and permute."""
@@ -107,6 +107,36 @@ def test_route_nano_prefill_full(moe):
     w = moe_synth.WORKLOADS["nano_prefill"]
     ties = _route_case(moe, w.T, w.H, w.E, w.k, w.seed, w.bias)
     assert ties < 50
+
+
+@pytest.mark.parametrize("T,E,k", [(50, 512, 24), (40, 1000, 32), (64, 128, 6), (64, 256, 16),
+                                   (300, 256, 16), (20, 64, 8), (600, 512, 24)])
+def test_topk_exact_ties(moe, T, E, k):
+    """Zero router weights make every logit 0 and every score exactly 0.5; a bias on a grid
+    of 1/64 then makes biased scores exactly equal in large groups, so the selection and its
+    order follow the lower-index rule at every place, the k-th included, and the GPU must
+    reproduce the oracle's indices exactly. Covers the arg-max rounds (E=64, 128), the
+    bitwise k-th-key selection (E=512, 1000; E=256 with k=16), both in the fused small-batch
+    kernel (T <= 256, E <= 256) and in the separate top-k kernel."""
+    D = 64
+    rng = np.random.default_rng(T + E + k)
+    x = moe_synth.bf16_bits(rng.standard_normal((T, D)).astype(np.float32))
+    wr = np.zeros((E, D), np.uint16)
+    bias = (rng.integers(-6, 7, E) / 64.0).astype(np.float32)
+    ref = O.route(x, wr, bias, k)
+    idx, gates, tie = moe.moe_route(to_dev(x), to_dev(wr), to_dev(bias), k)
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+    np.testing.assert_allclose(gates.cpu().numpy(), ref["gates"], rtol=1e-6)
+    np.testing.assert_array_equal(tie.cpu().numpy().astype(bool), ref["gap"] < 1e-5)
+    idx2, _, _, p = moe.moe_route_dispatch(to_dev(x), to_dev(wr), to_dev(bias), k)
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    np.testing.assert_array_equal(idx2.cpu().numpy(), ref["idx"])
+    pref = O.permute(ref["idx"], E)
+    for key in ("counts", "offsets", "row_token", "slot_row"):
+        np.testing.assert_array_equal(p[key].cpu().numpy(), pref[key], err_msg=key)
 
 
 # --------------------------------------------------------------------------- permute ----
