@@ -15,7 +15,7 @@
 // low nibble; scales as 512-byte atoms, one per (128-row block, 64-element K step): row
 // 128 rb + 32 r1 + r0, block kb of the step at byte r0 * 16 + r1 * 4 + kb. One thread
 // quantises one row's 64-element K step: 128 bytes in, 32 code bytes and one 32-bit word of
-// four scales out.
+// four scales out (for routed activations the warp loads its 32 steps cooperatively).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -64,15 +64,15 @@ __device__ __forceinline__ float global_scale(const uint32_t* amax) {
   return __fdiv_rn(__uint_as_float(*amax), kNvfp4GlobalDiv);
 }
 
-// Quantise 64 consecutive bf16 values (src 16-byte aligned). Writes 32 code bytes and
-// returns the four block-scale bytes packed little-endian (block 0 in the low byte).
-__device__ __forceinline__ uint32_t quant64(const uint4* __restrict__ src, float g, uint4* dst) {
+// Quantise 64 consecutive bf16 values held as eight 16-byte vectors. Writes 32 code bytes
+// and returns the four block-scale bytes packed little-endian (block 0 in the low byte).
+__device__ __forceinline__ uint32_t quant64_regs(const uint4 (&x)[8], float g, uint4* dst) {
   uint32_t sf = 0u;
   uint32_t q[8];
   const float six_g = __fmul_rn(6.0f, g);
 #pragma unroll
   for (int blk = 0; blk < 4; ++blk) {
-    const uint4 a = __ldg(src + 2 * blk), b = __ldg(src + 2 * blk + 1);
+    const uint4 a = x[2 * blk], b = x[2 * blk + 1];
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float v[16];
 #pragma unroll
@@ -111,6 +111,14 @@ __device__ __forceinline__ uint32_t quant64(const uint4* __restrict__ src, float
   dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
   dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
   return sf;
+}
+
+// The same from global memory (src 16-byte aligned).
+__device__ __forceinline__ uint32_t quant64(const uint4* __restrict__ src, float g, uint4* dst) {
+  uint4 x[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = __ldg(src + i);
+  return quant64_regs(x, g, dst);
 }
 
 // Codes of 16 values with block divisor denom = sb * g (0 gives zero codes): two words,
@@ -279,6 +287,12 @@ __global__ void k_pad_offsets(const int32_t* __restrict__ offsets, int E,
 
 constexpr int kQuantThreads = 256;
 
+// Routed activations: one thread per (row, 64-element K step), as for weights, but the warp
+// first loads its 32 x 128 bytes cooperatively: in each of eight rounds, eight consecutive
+// lanes read one thread's 128-byte step (its row comes by shuffle), so every load covers
+// four whole 128-byte lines, and the vectors go through a per-warp shared-memory buffer,
+// XOR-swizzled so that neither the stores nor the per-thread reads conflict on banks.
+// (Each thread reading its own 128 bytes directly costs eight L1 wavefronts per line.)
 __global__ void __launch_bounds__(kQuantThreads)
     k_quant_act(const uint16_t* __restrict__ src, long long ld, long long src_rows,
                 const int32_t* __restrict__ row_token, const int32_t* __restrict__ offsets,
@@ -287,33 +301,56 @@ __global__ void __launch_bounds__(kQuantThreads)
                 uint8_t* __restrict__ sf, int* status) {
   griddep_wait();
   griddep_launch_dependents();
-  extern __shared__ int s_poff[];
+  extern __shared__ uint4 s_dyn[];  // [8 warps][256 vectors], then poff[E+1]
+  const int lane = threadIdx.x & 31;
+  uint4* stage = s_dyn + (threadIdx.x >> 5) * 256;
+  int* s_poff = reinterpret_cast<int*>(s_dyn + (kQuantThreads / 32) * 256);
   for (int i = threadIdx.x; i <= E; i += blockDim.x) s_poff[i] = poff[i];
   __syncthreads();
   const int KS = K / 64;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long p = i / KS;
   const int j = static_cast<int>(i - p * KS);
-  if (p >= s_poff[E] || p >= P_max) return;
-  long long srow = p;
-  if (offsets) {
-    int lo = 0, hi = E - 1;  // expert e with s_poff[e] <= p < s_poff[e+1]
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (s_poff[mid + 1] > p)
-        hi = mid;
-      else
-        lo = mid + 1;
+  const bool valid = p < s_poff[E] && p < P_max;
+  long long srow = -1;  // -1: no source row (past the end, or a padding row of a segment)
+  if (valid) {
+    srow = p;
+    if (offsets) {
+      int lo = 0, hi = E - 1;  // expert e with s_poff[e] <= p < s_poff[e+1]
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s_poff[mid + 1] > p)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      const int local = static_cast<int>(p - s_poff[lo]);
+      const int base = offsets[lo];
+      srow = local < offsets[lo + 1] - base
+                 ? (row_token ? row_token[base + local] : base + local)
+                 : -1;
     }
-    const int local = static_cast<int>(p - s_poff[lo]);
-    const int base = offsets[lo];
-    srow = local < offsets[lo + 1] - base ? (row_token ? row_token[base + local] : base + local)
-                                          : -1;
+    if (srow >= src_rows) {  // offsets or row_token outside the source tensor
+      if (j == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+      srow = -1;
+    }
   }
-  if (srow >= src_rows) {  // offsets or row_token outside the source tensor
-    if (j == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
-    srow = -1;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int owner = 4 * it + (lane >> 3);  // the thread whose step these 8 lanes load
+    const long long so = __shfl_sync(0xffffffffu, srow, owner);
+    const int jo = __shfl_sync(0xffffffffu, j, owner);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (so >= 0)
+      v = __ldg(reinterpret_cast<const uint4*>(src + so * ld + jo * 64 + (lane & 7) * 8));
+    const int c = 32 * it + lane;  // vector c & 7 of thread c >> 3
+    stage[(c & ~7) | ((c & 7) ^ ((c >> 3) & 7))] = v;
   }
+  __syncwarp();
+  uint4 x[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) x[m] = stage[8 * lane + (m ^ (lane & 7))];
+  if (!valid) return;
   uint32_t* word = sf_word(sf, p, j, KS);
   uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + j * 32);
   if (srow < 0) {  // padding row of a segment
@@ -323,8 +360,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     return;
   }
   uint4 out[2];
-  *word = quant64(reinterpret_cast<const uint4*>(src + srow * ld + j * 64), global_scale(amax),
-                  out);
+  *word = quant64_regs(x, global_scale(amax), out);
   dst[0] = out[0];
   dst[1] = out[1];
 }
@@ -378,8 +414,9 @@ int launch_quant_act(const uint16_t* src, long long ld, long long src_rows,
   if (n <= 0) return MOE_OK;
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
+  const size_t smem = (kQuantThreads / 32) * 256 * sizeof(uint4) + static_cast<size_t>(E + 1) * 4;
   return launch_pdl(k_quant_act, dim3(static_cast<unsigned>((n + kQuantThreads - 1) / kQuantThreads)),
-                    dim3(kQuantThreads), static_cast<size_t>(E + 1) * 4, s, src, ld, src_rows,
+                    dim3(kQuantThreads), smem, s, src, ld, src_rows,
                     row_token, offsets, poff, E, K, P_max, amax, codes, sf, status);
 }
 
