@@ -18,7 +18,7 @@ Sources, by page and section:
          混合Mamba Transformer MoE架构: a learned router picks 6 of 128 routable
          experts per token; MoE layers replace the FFN layers.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * Scores are sigmoid(logits). The per-expert bias is added for SELECTION only (the
     aux-loss-free scheme [NANO]). Gates are the unbiased scores of the chosen experts,
     renormalised to sum to one, with no extra scale factor.
