@@ -66,6 +66,24 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(values, device, world: int):
+    """Element-wise maximum of per-rank timings (ms) over all ranks; unchanged on one rank.
+    Replicas run the same workload, so the slowest rank sets the job's time."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job throughput of `world` replicas that each process tokens_per_rank tokens per
+    step, timed by the slowest rank."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 # ------------------------------------------------------------------- algorithmic counts ----
 
 def counts_from_routing(idx: np.ndarray, E: int) -> np.ndarray:
@@ -355,10 +373,7 @@ def run_ours(args, w: moe_synth.Workload):
                 "after_bracket": statistics.mean(b.elapsed_time(e) for b, e in zip(f1, e_ev))}
     ms = statistics.mean(step_ms)
     ffn = statistics.mean(ffn_ms)
-    if world > 1:
-        t = torch.tensor([ms, ffn], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ffn = float(t[0]), float(t[1])
+    ms, ffn = max_over_ranks([ms, ffn], dev, world)
     assert moe.get_device_status() == 0
 
     # ---- end to end through the C ABI: pinned host x in, host y out, every step
@@ -390,10 +405,7 @@ def run_ours(args, w: moe_synth.Workload):
         if i >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
     e2e = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t[0])
+    e2e = max_over_ranks([e2e], dev, world)[0]
     assert moe.get_device_status() == 0
 
     routing = idx.cpu().numpy()
@@ -453,7 +465,7 @@ def run_ours(args, w: moe_synth.Workload):
     traffic = None if args.gathered else read_traffic(w.name, alg["touched"])
     out = {
         "metric": METRIC,
-        "value": world * T / (ms / 1e3),
+        "value": job_tokens_per_s(world, T, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
@@ -487,7 +499,7 @@ def run_ours(args, w: moe_synth.Workload):
                            "tflops": alg["flops"] / (ms / 1e3) / 1e12,
                            "hbm_gbs": alg["bytes"] / (ms / 1e3) / 1e9,
                            "touched_experts": alg["touched"], "peak_source": peak_src},
-        "e2e": {"value": world * T / (e2e / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, T, e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
                 "ms_per_step": e2e},
         "gpu_launches": launches_per_step * K,
