@@ -6,63 +6,70 @@
 //   s = amax / 448,   q = E4M3(v / s)   (nearest, ties to even, saturating at +-448)
 // with each expert matrix, the whole routed-token tensor and the whole h as the tensors.
 // The division is correctly rounded (Markstein's FMA correction after a correctly rounded
-// reciprocal, as in nvfp4.cu), so the codes are those of an fp32 evaluation of the rule.
-#include <cuda_fp8.h>
-
+// reciprocal, on value pairs: quant.cuh), so the codes are those of an fp32 evaluation of
+// the rule.
 #include "internal.h"
+#include "quant.cuh"
 
 namespace moe {
 namespace {
 
-// v / s correctly rounded for 2^-100 < s < 2^100 and |v / s| < 2^100 (Markstein, IBM J. Res.
-// Dev. 34(1), 1990): y = RN(1/s), q = RN(v y), r = v - q s exact in one fma, RN(q + r y).
-__device__ __forceinline__ float div_markstein(float v, float s, float y) {
-  const float q = __fmul_rn(v, y);
-  const float r = fmaf(-q, s, v);
-  return fmaf(r, y, q);
+// Two E4M3 bytes, lo in the low byte (the conversion puts its first source in the high
+// byte): nearest, ties to even, saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
-__device__ __forceinline__ uint32_t e4m3_byte(float v) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
+constexpr int kFp8SegVec = 128;  // 16-byte vectors (8 values) per warp segment
 
-// One thread per 16 elements of a row: 32 bytes of bf16 in, 16 bytes of E4M3 out.
+// One warp per (row, 1024-value segment): lane t converts the vectors t, t+32, t+64, t+96
+// of the segment, so each 16-byte load and each 8-byte code store of the warp is contiguous.
+// The quantisation is elementwise, so no lane needs its neighbours' values.
 __global__ void k_quant_fp8(const uint16_t* __restrict__ src, long long ld,
                             const int32_t* __restrict__ row_map, long long rows, int K,
                             long long rows_per_scale, const uint32_t* __restrict__ amax,
                             uint8_t* __restrict__ out) {
   griddep_wait();
   griddep_launch_dependents();
-  const int per_row = K / 16;
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= rows * per_row) return;
-  const long long r = i / per_row;
-  const int c = static_cast<int>(i - r * per_row);
+  const int nvec = K / 8;
+  const int segs = (nvec + kFp8SegVec - 1) / kFp8SegVec;
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= rows * segs) return;  // whole warps
+  const long long r = wid / segs;
+  const int seg = static_cast<int>(wid - r * segs);
   const long long srow = row_map ? row_map[r] : r;
   const uint32_t* am = amax + (rows_per_scale > 0 ? r / rows_per_scale : 0);
   const float s = __fdiv_rn(__uint_as_float(*am), kFp8Div);
-  const uint4* p = reinterpret_cast<const uint4*>(src + srow * ld + c * 16);
-  const uint4 a = __ldg(p), b = __ldg(p + 1);
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  uint32_t o[4] = {0u, 0u, 0u, 0u};
-  if (s > 0x1p-100f && s < 0x1p100f) {
-    const float y = __frcp_rn(s);
+  const bool fast = s > 0x1p-100f && s < 0x1p100f;
+  const float y = fast ? __frcp_rn(s) : 0.f;
+  const uint64_t y2 = f32x2_pack(y, y), ns2 = f32x2_pack(-s, -s);
+  const uint4* row = reinterpret_cast<const uint4*>(src + srow * ld);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
-      const uint32_t pair = e4m3_byte(div_markstein(lo, s, y)) |
-                            (e4m3_byte(div_markstein(hi, s, y)) << 8);
-      o[k >> 1] |= pair << (16 * (k & 1));
-    }
-  } else if (s > 0.f) {  // outside the range of the fast division
+  for (int m = 0; m < kFp8SegVec / 32; ++m) {
+    const int v = seg * kFp8SegVec + m * 32 + lane;
+    if (v >= nvec) break;
+    const uint4 a = __ldg(row + v);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t o[2] = {0u, 0u};
+    if (fast) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
-      const uint32_t pair = e4m3_byte(__fdiv_rn(lo, s)) | (e4m3_byte(__fdiv_rn(hi, s)) << 8);
-      o[k >> 1] |= pair << (16 * (k & 1));
+      for (int k = 0; k < 4; ++k) {
+        float lo, hi;
+        div2_markstein_bf16(w[k], y2, ns2, lo, hi);
+        o[k >> 1] |= e4m3x2(lo, hi) << (16 * (k & 1));
+      }
+    } else if (s > 0.f) {  // outside the range of the fast division
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
+        o[k >> 1] |= e4m3x2(__fdiv_rn(lo, s), __fdiv_rn(hi, s)) << (16 * (k & 1));
+      }
     }
+    *reinterpret_cast<uint2*>(out + r * K + static_cast<long long>(v) * 8) = make_uint2(o[0], o[1]);
   }
-  *reinterpret_cast<uint4*>(out + r * K + c * 16) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __global__ void k_finalize_fp8_scale(float* s, int G) {
@@ -77,7 +84,7 @@ __global__ void k_finalize_fp8_scale(float* s, int G) {
 int launch_quant_fp8(const uint16_t* src, long long ld, const int32_t* row_map, long long rows,
                      int K, long long rows_per_scale, const uint32_t* amax, uint8_t* out,
                      cudaStream_t s) {
-  const long long n = rows * (K / 16);
+  const long long n = rows * ((K / 8 + kFp8SegVec - 1) / kFp8SegVec) * 32;  // one warp per segment
   if (n <= 0) return MOE_OK;
   return launch_pdl(k_quant_fp8, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, s,
                     src, ld, row_map, rows, K, rows_per_scale, amax, out);

@@ -20,6 +20,7 @@
 #include <cuda_fp8.h>
 
 #include "internal.h"
+#include "quant.cuh"
 #include "scan.cuh"
 
 namespace moe {
@@ -64,15 +65,17 @@ __device__ __forceinline__ float global_scale(const uint32_t* amax) {
   return __fdiv_rn(__uint_as_float(*amax), kNvfp4GlobalDiv);
 }
 
-// Quantise 64 consecutive bf16 values held as eight 16-byte vectors. Writes 32 code bytes
-// and returns the four block-scale bytes packed little-endian (block 0 in the low byte).
-__device__ __forceinline__ uint32_t quant64_regs(const uint4 (&x)[8], float g, uint4* dst) {
+// Quantise 64 consecutive bf16 values, eight 16-byte vectors that load(m) returns for
+// m = 0..7 (each fetched when its block is quantised). Writes 32 code bytes and returns the
+// four block-scale bytes packed little-endian (block 0 in the low byte).
+template <class Load>
+__device__ __forceinline__ uint32_t quant64_from(Load load, float g, uint4* dst) {
   uint32_t sf = 0u;
   uint32_t q[8];
   const float six_g = __fmul_rn(6.0f, g);
 #pragma unroll
   for (int blk = 0; blk < 4; ++blk) {
-    const uint4 a = x[2 * blk], b = x[2 * blk + 1];
+    const uint4 a = load(2 * blk), b = load(2 * blk + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float v[16];
 #pragma unroll
@@ -93,8 +96,9 @@ __device__ __forceinline__ uint32_t quant64_regs(const uint4 (&x)[8], float g, u
     float s[16];
     if (denom > 0x1p-100f && denom < 0x1p100f) {
       const float y = __frcp_rn(denom);
+      const uint64_t y2 = f32x2_pack(y, y), nd2 = f32x2_pack(-denom, -denom);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) s[i] = div_markstein(v[i], denom, y);
+      for (int i = 0; i < 8; ++i) div2_markstein_bf16(w[i], y2, nd2, s[2 * i], s[2 * i + 1]);
     } else if (denom > 0.f) {  // outside the range of the fast division
 #pragma unroll
       for (int i = 0; i < 16; ++i) s[i] = __fdiv_rn(v[i], denom);
@@ -115,10 +119,7 @@ __device__ __forceinline__ uint32_t quant64_regs(const uint4 (&x)[8], float g, u
 
 // The same from global memory (src 16-byte aligned).
 __device__ __forceinline__ uint32_t quant64(const uint4* __restrict__ src, float g, uint4* dst) {
-  uint4 x[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) x[i] = __ldg(src + i);
-  return quant64_regs(x, g, dst);
+  return quant64_from([src](int m) { return __ldg(src + m); }, g, dst);
 }
 
 // Codes of 16 values with block divisor denom = sb * g (0 gives zero codes): two words,
@@ -293,7 +294,7 @@ constexpr int kQuantThreads = 256;
 // four whole 128-byte lines, and the vectors go through a per-warp shared-memory buffer,
 // XOR-swizzled so that neither the stores nor the per-thread reads conflict on banks.
 // (Each thread reading its own 128 bytes directly costs eight L1 wavefronts per line.)
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kQuantThreads, 4)
     k_quant_act(const uint16_t* __restrict__ src, long long ld, long long src_rows,
                 const int32_t* __restrict__ row_token, const int32_t* __restrict__ offsets,
                 const int32_t* __restrict__ poff, int E, int K, int P_max,
@@ -347,9 +348,6 @@ __global__ void __launch_bounds__(kQuantThreads)
     stage[(c & ~7) | ((c & 7) ^ ((c >> 3) & 7))] = v;
   }
   __syncwarp();
-  uint4 x[8];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) x[m] = stage[8 * lane + (m ^ (lane & 7))];
   if (!valid) return;
   uint32_t* word = sf_word(sf, p, j, KS);
   uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + j * 32);
@@ -360,7 +358,9 @@ __global__ void __launch_bounds__(kQuantThreads)
     return;
   }
   uint4 out[2];
-  *word = quant64_regs(x, global_scale(amax), out);
+  const uint4* mine = stage + 8 * lane;
+  const int sw = lane & 7;
+  *word = quant64_from([mine, sw](int m) { return mine[m ^ sw]; }, global_scale(amax), out);
   dst[0] = out[0];
   dst[1] = out[1];
 }
