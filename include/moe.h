@@ -63,7 +63,8 @@ int moe_get_device_status(cudaStream_t stream, int* status_out);
  * router, top-6 of 128). The sigmoid/bias/renormalisation details are this library's
  * reading of the aux-loss-free scheme.
  * Layout: x [T,D] bf16, w_router [E,D] bf16, bias [E] fp32; topk_idx [T,k] int32,
- * gates [T,k] fp32, tie_flag [T] uint8. Workspace: moe_route_workspace_size().
+ * gates [T,k] fp32, tie_flag [T] uint8. Workspace: moe_route_workspace_size(); its contents
+ * at entry do not matter, and two calls in flight at once must not share it.
  * ------------------------------------------------------------------------------------- */
 size_t moe_route_workspace_size(int T, int D, int E, int k);
 int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias,
@@ -95,7 +96,9 @@ int moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int H, int E,
  * calls (topk_idx, gates, tie_flag; counts, offsets, row_token, slot_row, x_perm; D plays
  * the role of H). For small batches (T <= 256, E <= 256, D <= 6144) the router logits, the
  * top-k and the dispatch maps run as one kernel, followed by the row copy.
- * Workspace: moe_route_dispatch_workspace_size().
+ * Workspace: moe_route_dispatch_workspace_size(). Its contents at entry do not matter (the
+ * fused kernel's CTAs signal one another through flag words tagged with a per-launch
+ * value). Two calls in flight at once must not share a workspace.
  * ------------------------------------------------------------------------------------- */
 size_t moe_route_dispatch_workspace_size(int T, int D, int E, int k);
 int moe_route_dispatch(const uint16_t* x, const uint16_t* w_router, const float* bias, int T,
