@@ -7,7 +7,9 @@
 // own 128 activation rows and its half (128 rows) of the weight tile, and one MMA of M = 256,
 // N = 256 reads both CTAs' shared memory and writes 128 accumulator rows into each CTA's TMEM.
 // Per SM that is 32 KB of operands per 512 MMA-cycles, half the weight bytes of a one-CTA
-// 128 x 256 tile.
+// 128 x 256 tile. F8: E4M3 operands (kind::f8f6f4), 128 K-elements per 128-byte slice, the
+// per-tensor scales (a_amax / 448) * w_scale[group] applied in the epilogue, and the maximum
+// of the stored squared-ReLU outputs reported for the next quantisation.
 //
 // Roles (192 threads per CTA):
 //   warp 0 lane 0   TMA producer in both CTAs (6-stage ring, 128-byte swizzle). Each CTA
@@ -24,8 +26,6 @@
 // CTAs always reach the two cluster barriers (set-up and teardown).
 #include <cuda.h>
 #include <cuda_bf16.h>
-
-#include <mutex>
 
 #include "internal.h"
 #include "tc.cuh"
@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t full0 = mapa_shared(full, 0);
       int stage = 0;
       uint32_t phase = 0;
+      long long armed = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < total; tile += npairs) {
         int e, rt, ct;
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // the odd CTA's bytes may land before this arming: the barrier's transaction count
           // then dips below zero, but the phase cannot complete without this arrival
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
+          ++armed;
           const int kc = kb * a.kpe;
           tma2_load_2d(sA + stage * A_BYTES, &tm_act, full0 + stage * 8, kc, row0, pol);
           tma2_load_3d(sB + stage * B_BYTES, &tm_w, full0 + stage * 8, kc, col0, e, pol);
@@ -214,6 +216,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 1;
         record2(a.status, MOE_ERR_TIMEOUT);
       }
+      // the even CTA's stage barriers count both CTAs' copies: once they have landed, no copy
+      // of the pair writes shared memory (the odd CTA waits at the closing cluster barrier)
+      if (leader && !drain_stages(full, STAGES, stage, phase, armed))
+        record2(a.status, MOE_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
