@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
     const uint64_t pol_a = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
+    long long armed = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       int e, rt, ct;
@@ -326,6 +327,7 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+          ++armed;
           const int kc = kb * BKE;
           uint8_t* dst = sA + stage * A_BYTES;
 #pragma unroll 4
@@ -345,6 +347,8 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
       *abort_flag = 1;
       record(a.status, MOE_ERR_TIMEOUT);
     }
+    if (lane == 0 && !drain_stages(full, STAGES, stage, phase, armed))
+      record(a.status, MOE_ERR_TIMEOUT);
   } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
@@ -352,6 +356,7 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
       const uint64_t pol_a = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
+      long long armed = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, rt, ct;
@@ -364,6 +369,7 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+          ++armed;
           const int kc = kb * BKE;
           const int kw = a.k_wrap ? (kc % a.k_wrap) : kc;
           if (!SWAP) {
@@ -383,6 +389,7 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
         *abort_flag = 1;
         record(a.status, MOE_ERR_TIMEOUT);
       }
+      if (!drain_stages(full, STAGES, stage, phase, armed)) record(a.status, MOE_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
     if (lane == 0) {

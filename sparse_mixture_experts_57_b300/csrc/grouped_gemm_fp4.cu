@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t pol = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
+      long long armed = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, rt, ct;
@@ -231,6 +232,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t sf_bytes = nsteps * ATOM;
           mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + (two ? 3u : 2u) * sf_bytes);
+          ++armed;
           tma_load_2d(sA + stage * A_BYTES, &tm_a, &full[stage], kb * BKB, row0, pol);
           tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kb * BKB, col0, e, pol);
           const long long so = static_cast<long long>(kb) * STEPS_PER_STAGE * ATOM;
@@ -249,6 +251,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 1;
         record(a.status, MOE_ERR_TIMEOUT);
       }
+      if (!drain_stages(full, STAGES, stage, phase, armed)) record(a.status, MOE_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
     if (lane == 0) {

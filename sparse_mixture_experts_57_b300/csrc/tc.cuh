@@ -63,6 +63,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Producer exit: wait (at most kDrainLimitNs per stage, whatever the abort flag says) until
+// the most recent arming of every stage has landed, so that no copy this CTA issued is still
+// writing its shared memory when it exits. (stage, phase) is the producer's next slot and
+// `armed` the number of stage armings so far. In a run without errors every stage has landed
+// already and this returns at once.
+constexpr unsigned long long kDrainLimitNs = 100000000ull;
+__device__ __forceinline__ bool drain_stages(uint64_t* full, int stages, int stage,
+                                             uint32_t phase, long long armed) {
+  bool ok = true;
+  const int n = armed < stages ? static_cast<int>(armed) : stages;
+  for (int i = 1; i <= n; ++i) {
+    int s = stage - i;
+    uint32_t p = phase;
+    if (s < 0) {
+      s += stages;
+      p ^= 1u;
+    }
+    if (mbar_try_wait(&full[s], p)) continue;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(&full[s], p)) {
+      if (global_timer_ns() - t0 > kDrainLimitNs) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  return ok;
+}
+
 // ----------------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
