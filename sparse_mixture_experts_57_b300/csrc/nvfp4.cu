@@ -327,9 +327,12 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
       }
       const int local = static_cast<int>(p - s_poff[lo]);
       const int base = offsets[lo];
-      srow = local < offsets[lo + 1] - base
-                 ? (row_token ? row_token[base + local] : base + local)
-                 : -1;
+      if (local < offsets[lo + 1] - base) {
+        srow = row_token ? row_token[base + local] : base + local;
+        if (srow < 0) srow = src_rows;  // a negative token id is as invalid as a large one
+      } else {
+        srow = -1;  // padding row of the segment
+      }
     }
     if (srow >= src_rows) {  // offsets or row_token outside the source tensor
       if (j == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
