@@ -699,7 +699,7 @@ def main():
     ap.add_argument("--T", type=int, default=None,
                     help="override the token count (a scaled case, e.g. for profiling)")
     ap.add_argument("--E", type=int, default=None,
-                    help="override the expert count of a standard layer (scaled case)")
+                    help="override the expert count (E, or E' of the latent layer; scaled case)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--gathered", action="store_true",
                     help="standard layer: time moe_forward_gathered (whole-layer bracket)")
@@ -710,8 +710,6 @@ def main():
         ap.error("--gathered applies to the bf16 standard layer")
     if args.T is not None or args.E is not None:
         import dataclasses
-        if w.latent and args.E is not None:
-            ap.error("--E applies to the standard layer only")
         T = args.T if args.T is not None else w.T
         E = args.E if args.E is not None else w.E
         w = dataclasses.replace(w, T=T, E=E, name=f"{w.name}[T={T},E={E}]")

@@ -28,9 +28,9 @@ Readings where the pages are silent:
   * LatentMoE applies W_out once, after the combine. W_out is linear, so this equals
     applying it per expert.
 
-Parity status: the routing, permutation, FFN, combine and LatentMoE functions are pinned
-by the CPU tests in tests/test_oracle_pins.py (brute force, closed forms, invariants,
-special cases). The NVFP4 and FP8 functions are pinned by exhaustive format tables, error
+Parity status: the bf16 widening, routing, permutation, FFN, combine, per-token and
+LatentMoE functions are pinned by the CPU tests in tests/test_oracle_pins.py (brute force,
+closed forms, invariants, special cases, a full table of bf16 bit patterns). The NVFP4 and FP8 functions are pinned by exhaustive format tables, error
 bounds and brute force.
 """
 from __future__ import annotations

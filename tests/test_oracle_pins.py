@@ -571,13 +571,97 @@ def check_nvfp4_2d(o):
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
 
 
+def _brute_tokens(x, idx, gates, wu, wd):
+    """y[t] = sum_j gates[t, j] * FFN_{idx[t, j]}(x[t]) by scalar loops (given routing)."""
+    n, H = x.shape
+    F = wu.shape[1]
+    y = np.zeros((n, wd.shape[1]))
+    for t in range(n):
+        for j in range(idx.shape[1]):
+            e = int(idx[t, j])
+            hid = [max(math.fsum(x[t, i] * wu[e, f, i] for i in range(H)), 0.0) ** 2
+                   for f in range(F)]
+            for i in range(wd.shape[1]):
+                y[t, i] += gates[t, j] * math.fsum(wd[e, i, f] * hid[f] for f in range(F))
+    return y
+
+
+def _brute_route(x, wr, b, k):
+    """Routing by scalar loops: sigmoid scores, brute-force top-k, renormalised gates."""
+    T, H = x.shape
+    E = wr.shape[0]
+    idx = np.zeros((T, k), dtype=np.int64)
+    gates = np.zeros((T, k))
+    for t in range(T):
+        s = np.array([1.0 / (1.0 + math.exp(-math.fsum(x[t, i] * wr[e, i] for i in range(H))))
+                      for e in range(E)])
+        chosen = _brute_topk(s + b, k)
+        tot = math.fsum(s[e] for e in chosen)
+        idx[t] = chosen
+        gates[t] = [s[e] / tot for e in chosen]
+    return idx, gates
+
+
+def check_moe_tokens(o):
+    """The per-token evaluator used for sampled parity at full size equals the scalar-loop
+    layer on every token (k = 1, 1 < k < E and k = E), and weights each (token, slot)
+    by that slot's own gate when the gates are arbitrary and a sample is out of order."""
+    for seed, (T, H, E, k, F) in enumerate([(6, 4, 5, 1, 3), (7, 5, 6, 3, 2), (5, 3, 4, 4, 2)]):
+        x, wr, b, wu, wd, _ = _tiny_layer(20 + seed, T=T, H=H, E=E, k=k, F=F)
+        idx, gates = _brute_route(x, wr, b, k)
+        got = o.moe_tokens(x, idx, gates, wu, wd)
+        np.testing.assert_allclose(got, _brute_moe(x, wr, b, wu, wd, k), rtol=1e-11,
+                                   atol=1e-11)
+        # the full layer's output on every token is the per-token evaluation
+        np.testing.assert_allclose(got, o.moe_layer(x, wr, b, wu, wd, k)["y"], rtol=1e-11,
+                                   atol=1e-11)
+    rng = np.random.default_rng(31)
+    x, _, _, wu, wd, _ = _tiny_layer(31, T=6, H=4, E=5, F=3)
+    # a sample in no particular order; slot order not sorted by expert; distinct gates that
+    # do not sum to one, so a gate taken from the wrong slot or token changes the result
+    sample = np.array([4, 0, 5, 2])
+    idx = np.array([[3, 0, 4], [1, 4, 2], [0, 2, 1], [4, 3, 0]])
+    gates = rng.uniform(0.1, 2.0, size=idx.shape)
+    got = o.moe_tokens(x[sample], idx, gates, wu, wd)
+    np.testing.assert_allclose(got, _brute_tokens(x[sample], idx, gates, wu, wd), rtol=1e-11,
+                               atol=1e-11)
+
+
+def check_widen_bf16(o):
+    """bfloat16 is the upper half of an IEEE binary32 word: decode hand-picked patterns from
+    the bit fields, then every one of the 65536 patterns through struct's binary32 reader."""
+    import struct
+    cases = {0x3F80: 1.0, 0xC000: -2.0, 0x0001: 2.0 ** -133, 0x0080: 2.0 ** -126,
+             0x7F7F: (2.0 - 2.0 ** -7) * 2.0 ** 127, 0x3EAB: 0.333984375, 0x4049: 3.140625,
+             0x7F80: math.inf, 0xFF80: -math.inf}
+    got = o.widen_bf16(np.array(list(cases), dtype=np.uint16))
+    assert got.dtype == np.float64
+    assert got.tolist() == list(cases.values())
+    z = o.widen_bf16(np.array([0x0000, 0x8000], dtype=np.uint16))
+    assert z.tolist() == [0.0, 0.0] and not math.copysign(1, z[0]) < 0 \
+        and math.copysign(1, z[1]) < 0
+    assert math.isnan(o.widen_bf16(np.array([0x7FC0], dtype=np.uint16))[0])
+    allbits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):          # signalling NaN patterns widen to NaN
+        w = o.widen_bf16(allbits)
+    ref = np.array([struct.unpack(">f", int(b).to_bytes(2, "big") + b"\0\0")[0]
+                    for b in range(1 << 16)])
+    nan = np.isnan(ref)
+    assert (np.isnan(w) == nan).all()
+    assert (w[~nan] == ref[~nan]).all()
+    assert (np.signbit(w[~nan]) == np.signbit(ref[~nan])).all()
+    # shape is kept
+    assert o.widen_bf16(allbits[:12].reshape(3, 4)).shape == (3, 4)
+
+
 ALL_CHECKS = [check_route_closed_form, check_topk_brute_force, check_layer_brute_force,
               check_ffn_closed_form, check_single_expert_is_dense_ffn, check_identical_experts,
               check_k_equals_E, check_forced_expert, check_gate_and_count_invariants,
               check_latent_identity, check_latent_brute_force, check_combine_weights,
               check_e2m1_table, check_e4m3_table, check_nvfp4_block, check_nvfp4_bounds,
               check_nvfp4_brute_force, check_grouped_ffn_nvfp4, check_nvfp4_layer_paths,
-              check_fp8_quantize, check_fp8_layer_paths, check_shared_expert, check_nvfp4_2d]
+              check_fp8_quantize, check_fp8_layer_paths, check_shared_expert, check_nvfp4_2d,
+              check_moe_tokens, check_widen_bf16]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -665,6 +749,53 @@ def _fp8_scale_e2m1_max(amax):            # mistake: NVFP4's element maximum in 
     return np.float32(np.float32(amax) / np.float32(6.0))
 
 
+def _tokens_first_slot_gate(x_rows, idx_rows, gates_rows, w_up, w_down):
+    # mistake: every (token, slot) takes the token's first gate
+    xr = _f64(x_rows)
+    n, k = np.asarray(idx_rows).shape
+    out = np.zeros((n, np.asarray(w_down).shape[1]))
+    g = np.asarray(gates_rows, dtype=np.float64)
+    for i in range(n):
+        for j in range(k):
+            e = int(idx_rows[i][j])
+            out[i] += g[i, 0] * expert_ffn(xr[i:i + 1], w_up[e], w_down[e])[0]
+    return out
+
+
+def _tokens_overwrite(x_rows, idx_rows, gates_rows, w_up, w_down):
+    # mistake: a later expert's output replaces the earlier ones instead of adding to them
+    xr = _f64(x_rows)
+    n, k = np.asarray(idx_rows).shape
+    out = np.zeros((n, np.asarray(w_down).shape[1]))
+    g = np.asarray(gates_rows, dtype=np.float64)
+    for e in sorted({int(v) for v in np.asarray(idx_rows).reshape(-1)}):
+        ii, jj = np.nonzero(np.asarray(idx_rows) == e)
+        out[ii] = g[ii, jj][:, None] * expert_ffn(xr[ii], w_up[e], w_down[e])
+    return out
+
+
+def _tokens_gate_by_position(x_rows, idx_rows, gates_rows, w_up, w_down):
+    # mistake: gates read by the row's position inside its expert group, not by (token, slot)
+    xr = _f64(x_rows)
+    n, k = np.asarray(idx_rows).shape
+    out = np.zeros((n, np.asarray(w_down).shape[1]))
+    g = np.asarray(gates_rows, dtype=np.float64)
+    for e in sorted({int(v) for v in np.asarray(idx_rows).reshape(-1)}):
+        ii, jj = np.nonzero(np.asarray(idx_rows) == e)
+        o_e = expert_ffn(xr[ii], w_up[e], w_down[e])
+        np.add.at(out, ii, g.reshape(-1)[np.arange(len(ii))][:, None] * o_e)
+    return out
+
+
+def _widen_as_fp16(bits):                 # mistake: the 16 bits read as IEEE half precision
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def _widen_shift_15(bits):                # mistake: off-by-one shift into the binary32 word
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(15)
+    return u.view(np.float32).astype(np.float64)
+
+
 _f64 = moe_oracle._f64
 
 MUTANTS = {
@@ -678,6 +809,11 @@ MUTANTS = {
     "sigmoid_sign": ({"sigmoid": _sigmoid_sign}, check_route_closed_form),
     "e2m1_ties_away": ({"e2m1_round": _e2m1_ties_away}, check_e2m1_table),
     "fp8_scale_wrong_max": ({"fp8_scale": _fp8_scale_e2m1_max}, check_fp8_quantize),
+    "tokens_first_slot_gate": ({"moe_tokens": _tokens_first_slot_gate}, check_moe_tokens),
+    "tokens_overwrite": ({"moe_tokens": _tokens_overwrite}, check_moe_tokens),
+    "tokens_gate_by_position": ({"moe_tokens": _tokens_gate_by_position}, check_moe_tokens),
+    "widen_as_fp16": ({"widen_bf16": _widen_as_fp16}, check_widen_bf16),
+    "widen_shift_15": ({"widen_bf16": _widen_shift_15}, check_widen_bf16),
 }
 
 
