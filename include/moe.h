@@ -344,6 +344,82 @@ int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bi
                     int32_t* topk_idx_out, float* gates_out, void* workspace,
                     size_t workspace_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Quantised activation views. The NVFP4 and FP8 FFN calls quantise their activations into
+ * the caller's workspace: the routed tokens entering the up-projection (x) and the hidden
+ * activations h entering the down-projection, each with one global scale over the whole
+ * tensor (NVIDIA Nemotron 3 notes §2.4 for NVFP4; per-tensor E4M3 for FP8). These calls
+ * return where those buffers sit inside a workspace laid out by the named call with the
+ * same sizes, so a caller can read what the call actually fed the tensor cores.
+ * They make no CUDA call and touch no memory: they only compute addresses. The contents
+ * are those of the last call that used the workspace, valid once that call has completed
+ * on its stream and until the workspace is used again.
+ *
+ * Fields (NULL where the call has no such buffer):
+ *  - offsets [E+1], row_token [rows]: the forward calls' dispatch maps (moe_permute's).
+ *  - padded_offsets [E+1] (NVFP4): start row of each expert's segment in the padded
+ *    buffers; every segment is rounded up to whole 128-row tiles, rows past the expert's
+ *    count are padding (zero codes and zero scales).
+ *  - amax [2]: fp32 bit patterns of amax(|x|) over the whole token tensor (all of x for the
+ *    forward calls, all of x_perm for the grouped-FFN calls) and of amax(|h|) over the
+ *    stored bf16 h. Global scales: g = amax / (6 * 448) (NVFP4), s = amax / 448 (FP8).
+ *  - x_codes, x_scales: the quantised routed tokens. NVFP4: codes [buffer_rows, H/2] and
+ *    scale atoms of [buffer_rows, H] (the formats above), padded segment order; row
+ *    padded_offsets[e] + r holds permuted row offsets[e] + r. FP8: E4M3 bytes
+ *    [buffer_rows, H] in permuted row order; x_scales is NULL.
+ *  - h [buffer_rows, F] bf16: max(0, x_q . w_up_q[e]^T)^2 as stored by the up-projection
+ *    (NVFP4: padded order, padding rows zero).
+ *  - h_codes, h_scales: h quantised for the down-projection, as x_codes / x_scales.
+ *  - buffer_rows: rows of the x / h buffers (NVFP4: the padded-row bound
+ *    rows + 127 E rounded up to 128; FP8: rows).
+ * Return: MOE_ERR_INVALID_ARG for sizes the named call rejects or a NULL out;
+ * MOE_ERR_WORKSPACE if the workspace is smaller than the call needs.
+ * ------------------------------------------------------------------------------------- */
+typedef struct moe_quant_view {
+  const int32_t* offsets;
+  const int32_t* row_token;
+  const int32_t* padded_offsets;
+  const uint32_t* amax;
+  const uint8_t* x_codes;
+  const uint8_t* x_scales;
+  const uint16_t* h;
+  const uint8_t* h_codes;
+  const uint8_t* h_scales;
+  long long buffer_rows;
+} moe_quant_view;
+
+int moe_grouped_ffn_nvfp4_view(int rows, int H, int F, int E, const void* workspace,
+                               size_t workspace_bytes, moe_quant_view* out);
+int moe_forward_nvfp4_view(int T, int H, int E, int k, int F, const void* workspace,
+                           size_t workspace_bytes, moe_quant_view* out);
+int moe_grouped_ffn_fp8_view(int rows, int H, int F, int E, const void* workspace,
+                             size_t workspace_bytes, moe_quant_view* out);
+int moe_forward_fp8_view(int T, int H, int E, int k, int F, const void* workspace,
+                         size_t workspace_bytes, moe_quant_view* out);
+
+/* ---------------------------------------------------------------------------------------
+ * moe_selftest_wait_timeout: runs the failure path that every tensor-core pipeline kernel of
+ * this library shares, on purpose, so a caller can check it on a live GPU. Every wait of a
+ * kernel pipeline is bounded; when one gives up the kernel records MOE_ERR_TIMEOUT on the
+ * device status word, stops its other roles through a per-CTA abort flag, waits (bounded)
+ * for its copies in flight to land, releases its tensor memory and returns, so the GPU
+ * stays usable. Each of the `blocks` CTAs here allocates tensor memory, issues one 4 KB bulk
+ * copy from `src`, and then waits on barriers that nothing arrives on: the producer role
+ * with a limit of limit_us microseconds, the other roles with the pipelines' normal limit,
+ * which only the abort flag can cut short.
+ *   src     device, 16-byte aligned, at least 4096 bytes (read only);
+ *   report  device int [blocks * 8], written per CTA: [0] 1 if the producer's wait gave
+ *           up, [1] and [2] 1 if the MMA and epilogue roles left through the abort flag,
+ *           [3] 1 if the copy in flight landed before the CTA exited, [4] microseconds from
+ *           the first wait to the release of tensor memory; [5..7] unused.
+ * By design the call leaves MOE_ERR_TIMEOUT on the device status word (read and clear it
+ * with moe_get_device_status). Returns MOE_ERR_INVALID_ARG for a null pointer, limit_us
+ * outside [1, 10^6] or blocks outside [1, 1024]; MOE_ERR_UNSUPPORTED for an unaligned src.
+ * Asynchronous on `stream`.
+ * ------------------------------------------------------------------------------------- */
+int moe_selftest_wait_timeout(const void* src, int limit_us, int blocks, int* report,
+                              cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

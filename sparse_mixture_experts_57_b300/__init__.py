@@ -31,5 +31,6 @@ from ._binding import (  # noqa: F401
     moe_quantize_nvfp4_weights,
     moe_route,
     moe_route_dispatch,
+    quant_view,
     status_string,
 )

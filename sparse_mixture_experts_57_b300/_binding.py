@@ -19,6 +19,17 @@ _LIB = None
 
 _VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 
+
+
+class QuantView(ctypes.Structure):
+    """struct moe_quant_view of include/moe.h."""
+    _fields_ = [("offsets", _VP), ("row_token", _VP), ("padded_offsets", _VP), ("amax", _VP),
+                ("x_codes", _VP), ("x_scales", _VP), ("h", _VP), ("h_codes", _VP),
+                ("h_scales", _VP), ("buffer_rows", ctypes.c_longlong)]
+
+
+_QV = ctypes.POINTER(QuantView)
+
 # name -> (restype, argtypes); mirrors include/moe.h
 SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -58,6 +69,11 @@ SIGNATURES = {
     "moe_forward_fp8_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP,
                              _VP, _VP, _SZ, _VP]),
+    "moe_grouped_ffn_nvfp4_view": (_I, [_I, _I, _I, _I, _VP, _SZ, _QV]),
+    "moe_forward_nvfp4_view": (_I, [_I, _I, _I, _I, _I, _VP, _SZ, _QV]),
+    "moe_grouped_ffn_fp8_view": (_I, [_I, _I, _I, _I, _VP, _SZ, _QV]),
+    "moe_forward_fp8_view": (_I, [_I, _I, _I, _I, _I, _VP, _SZ, _QV]),
+    "moe_selftest_wait_timeout": (_I, [_VP, _I, _I, _VP, _VP]),
     "moe_forward_shared_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_shared": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP,
                                 _VP, _VP, _VP, _SZ, _VP]),
@@ -432,6 +448,31 @@ def moe_forward_fp8(x, w_router, bias, w_up: Fp8Weights, w_down: Fp8Weights, k: 
                              T, H, E, k, F, _ptr(y), _ptr(topk_idx_out), _ptr(gates_out),
                              _ptr(ws), ws.numel(), _stream(stream)), "moe_forward_fp8")
     return y
+
+
+# ------------------------------------------------------------ quantised activation views ----
+
+_VIEW_CALLS = {"grouped_ffn_nvfp4": "moe_grouped_ffn_nvfp4_view",
+               "forward_nvfp4": "moe_forward_nvfp4_view",
+               "grouped_ffn_fp8": "moe_grouped_ffn_fp8_view",
+               "forward_fp8": "moe_forward_fp8_view"}
+
+
+def quant_view(call: str, dims, workspace) -> dict:
+    """Where the quantised activations of `call` sit inside `workspace` (a uint8 CUDA tensor
+    used by that call with the same sizes). dims: (rows, H, F, E) for the grouped-FFN calls,
+    (T, H, E, k, F) for the forward calls. Returns byte offsets into the workspace (None where
+    the call has no such buffer) and "buffer_rows"."""
+    _cuda_tensor(workspace, torch.uint8, "workspace")
+    v = QuantView()
+    _check(getattr(lib(), _VIEW_CALLS[call])(*[int(d) for d in dims], _ptr(workspace),
+                                             workspace.numel(), ctypes.byref(v)),
+           _VIEW_CALLS[call])
+    base = workspace.data_ptr()
+    out = {name: (None if getattr(v, name) is None else getattr(v, name) - base)
+           for name, _ in QuantView._fields_ if name != "buffer_rows"}
+    out["buffer_rows"] = int(v.buffer_rows)
+    return out
 
 
 # ---------------------------------------------------------------------- shared expert ----

@@ -391,6 +391,56 @@ int ffn_fp8(const uint16_t* src, long long ld, long long amax_rows, const int32_
   return launch_grouped_gemm(d, s);
 }
 
+// Routing and dispatch buffers at the head of the moe_forward_nvfp4 / moe_forward_fp8
+// workspaces, followed by y_perm.
+struct QuantFwdWs {
+  float* logits;
+  int32_t* idx;
+  float* gates;
+  uint8_t* tie;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_token;
+  int32_t* slot_row;
+  int* sync;
+  void* perm_scratch;
+  uint16_t* y_perm;
+};
+
+QuantFwdWs carve_quant_fwd(Carver& c, int T, int H, int E, int k) {
+  QuantFwdWs w;
+  const size_t rows = static_cast<size_t>(T) * k;
+  w.logits = c.take<float>(static_cast<size_t>(T) * E);
+  w.idx = c.take<int32_t>(rows);
+  w.gates = c.take<float>(rows);
+  w.tie = c.take<uint8_t>(T > 0 ? T : 1);
+  w.counts = c.take<int32_t>(E);
+  w.offsets = c.take<int32_t>(E + 1);
+  w.row_token = c.take<int32_t>(rows);
+  w.slot_row = c.take<int32_t>(rows);
+  w.sync = c.take<int>(route_fused_sync_ints(T));
+  w.perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
+  w.y_perm = c.take<uint16_t>(rows * H);
+  return w;
+}
+
+// Routing, dispatch maps and permutation of the quantised layers (no bf16 x_perm).
+int quant_fwd_route(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H,
+                    int E, int k, const QuantFwdWs& w, int32_t* idx, float* gates,
+                    cudaStream_t stream) {
+  int st;
+  if (route_fused_ok(T, H, E, k, 1)) {  // small batches: routing and maps in one kernel
+    return launch_route_fused(x, H, w_router, bias, T, H, E, k, 1, w.logits, idx, gates, w.tie,
+                              w.counts, w.offsets, w.row_token, w.slot_row, w.sync, stream);
+  }
+  st = router_logits(x, H, w_router, T, H, E, 1, w.logits, stream);
+  if (st) return st;
+  st = launch_topk(w.logits, bias, T, E, k, idx, gates, w.tie, stream);
+  if (st) return st;
+  return launch_permute(idx, x, H, T, H, E, k, w.counts, w.offsets, w.row_token, w.slot_row,
+                        nullptr, w.perm_scratch, stream);
+}
+
 bool nvfp4_weights_ok(const uint8_t* codes, const uint8_t* scales, const float* g) {
   return codes && scales && g && aligned16(codes) && aligned16(scales);
 }
@@ -753,19 +803,8 @@ int moe_grouped_ffn_nvfp4(const uint16_t* x_perm, const int32_t* offsets,
 size_t moe_forward_nvfp4_workspace_size(int T, int H, int E, int k, int F) {
   if (!dims_ok(T, H, E, k) || F <= 0) return 0;
   Carver c(nullptr, 0);
-  const size_t rows = static_cast<size_t>(T) * k;
-  c.take<float>(static_cast<size_t>(T) * E);                     // logits
-  c.take<int32_t>(rows);                                        // idx
-  c.take<float>(rows);                                          // gates
-  c.take<uint8_t>(T > 0 ? T : 1);                               // tie
-  c.take<int32_t>(E);                                           // counts
-  c.take<int32_t>(E + 1);                                       // offsets
-  c.take<int32_t>(rows);                                        // row_token
-  c.take<int32_t>(rows);                                        // slot_row
-  c.take<int>(route_fused_sync_ints(T));
-  c.take<char>(permute_scratch_bytes(T, E));
-  c.take<uint16_t>(rows * H);                                   // y_perm
-  carve_fp4(c, static_cast<int>(rows), H, F, E);
+  carve_quant_fwd(c, T, H, E, k);
+  carve_fp4(c, T * k, H, F, E);
   return c.used + 256;
 }
 
@@ -785,42 +824,19 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
   if (H % 64 || F % 64 || !aligned16(x) || !aligned16(w_router) || !aligned16(y))
     return MOE_ERR_UNSUPPORTED;
   Carver c(workspace, workspace_bytes);
-  const size_t rows = static_cast<size_t>(T) * k;
-  float* logits = c.take<float>(static_cast<size_t>(T) * E);
-  int32_t* idx = c.take<int32_t>(rows);
-  float* gates = c.take<float>(rows);
-  uint8_t* tie = c.take<uint8_t>(T);
-  int32_t* counts = c.take<int32_t>(E);
-  int32_t* offsets = c.take<int32_t>(E + 1);
-  int32_t* row_token = c.take<int32_t>(rows);
-  int32_t* slot_row = c.take<int32_t>(rows);
-  int* sync = c.take<int>(route_fused_sync_ints(T));
-  void* perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
-  uint16_t* y_perm = c.take<uint16_t>(rows * H);
-  const Fp4Ws w = carve_fp4(c, static_cast<int>(rows), H, F, E);
+  const int rows = T * k;
+  const QuantFwdWs f = carve_quant_fwd(c, T, H, E, k);
+  const Fp4Ws w = carve_fp4(c, rows, H, F, E);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
-  if (topk_idx_out) idx = topk_idx_out;
-  if (gates_out) gates = gates_out;
+  int32_t* idx = topk_idx_out ? topk_idx_out : f.idx;
+  float* gates = gates_out ? gates_out : f.gates;
   // routing and dispatch stay in bf16/fp32; the expert FFNs run in NVFP4
-  int st;
-  if (route_fused_ok(T, H, E, k, 1)) {  // small batches: routing and maps in one kernel
-    st = launch_route_fused(x, H, w_router, bias, T, H, E, k, 1, logits, idx, gates, tie, counts,
-                            offsets, row_token, slot_row, sync, stream);
-    if (st) return st;
-  } else {
-    st = router_logits(x, H, w_router, T, H, E, 1, logits, stream);
-    if (st) return st;
-    st = launch_topk(logits, bias, T, E, k, idx, gates, tie, stream);
-    if (st) return st;
-    st = launch_permute(idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, nullptr,
-                        perm_scratch, stream);
-    if (st) return st;
-  }
-  st = ffn_nvfp4(x, H, T, row_token, offsets, {up_codes, up_scales, up_gscale},
-                 {down_codes, down_scales, down_gscale}, static_cast<int>(rows), H, F, E, y_perm,
-                 w, stream);
+  int st = quant_fwd_route(x, w_router, bias, T, H, E, k, f, idx, gates, stream);
   if (st) return st;
-  return launch_combine(y_perm, static_cast<int>(rows), slot_row, gates, T, H, k, y, stream);
+  st = ffn_nvfp4(x, H, T, f.row_token, f.offsets, {up_codes, up_scales, up_gscale},
+                 {down_codes, down_scales, down_gscale}, rows, H, F, E, f.y_perm, w, stream);
+  if (st) return st;
+  return launch_combine(f.y_perm, rows, f.slot_row, gates, T, H, k, y, stream);
 }
 
 int moe_quantize_fp8_weights(const uint16_t* w, int G, int N, int K, uint8_t* codes,
@@ -867,19 +883,8 @@ int moe_grouped_ffn_fp8(const uint16_t* x_perm, const int32_t* offsets, const ui
 size_t moe_forward_fp8_workspace_size(int T, int H, int E, int k, int F) {
   if (!dims_ok(T, H, E, k) || F <= 0) return 0;
   Carver c(nullptr, 0);
-  const size_t rows = static_cast<size_t>(T) * k;
-  c.take<float>(static_cast<size_t>(T) * E);
-  c.take<int32_t>(rows);
-  c.take<float>(rows);
-  c.take<uint8_t>(T > 0 ? T : 1);
-  c.take<int32_t>(E);
-  c.take<int32_t>(E + 1);
-  c.take<int32_t>(rows);
-  c.take<int32_t>(rows);
-  c.take<int>(route_fused_sync_ints(T));
-  c.take<char>(permute_scratch_bytes(T, E));
-  c.take<uint16_t>(rows * H);
-  carve_fp8(c, static_cast<int>(rows), H, F);
+  carve_quant_fwd(c, T, H, E, k);
+  carve_fp8(c, T * k, H, F);
   return c.used + 256;
 }
 
@@ -896,41 +901,19 @@ int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bi
       !aligned16(up_codes) || !aligned16(down_codes))
     return MOE_ERR_UNSUPPORTED;
   Carver c(workspace, workspace_bytes);
-  const size_t rows = static_cast<size_t>(T) * k;
-  float* logits = c.take<float>(static_cast<size_t>(T) * E);
-  int32_t* idx = c.take<int32_t>(rows);
-  float* gates = c.take<float>(rows);
-  uint8_t* tie = c.take<uint8_t>(T);
-  int32_t* counts = c.take<int32_t>(E);
-  int32_t* offsets = c.take<int32_t>(E + 1);
-  int32_t* row_token = c.take<int32_t>(rows);
-  int32_t* slot_row = c.take<int32_t>(rows);
-  int* sync = c.take<int>(route_fused_sync_ints(T));
-  void* perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
-  uint16_t* y_perm = c.take<uint16_t>(rows * H);
-  const Fp8Ws w = carve_fp8(c, static_cast<int>(rows), H, F);
+  const int rows = T * k;
+  const QuantFwdWs f = carve_quant_fwd(c, T, H, E, k);
+  const Fp8Ws w = carve_fp8(c, rows, H, F);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
-  if (topk_idx_out) idx = topk_idx_out;
-  if (gates_out) gates = gates_out;
-  int st;
-  if (route_fused_ok(T, H, E, k, 1)) {  // small batches: routing and maps in one kernel
-    st = launch_route_fused(x, H, w_router, bias, T, H, E, k, 1, logits, idx, gates, tie, counts,
-                            offsets, row_token, slot_row, sync, stream);
-    if (st) return st;
-  } else {
-    st = router_logits(x, H, w_router, T, H, E, 1, logits, stream);
-    if (st) return st;
-    st = launch_topk(logits, bias, T, E, k, idx, gates, tie, stream);
-    if (st) return st;
-    st = launch_permute(idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, nullptr,
-                        perm_scratch, stream);
-    if (st) return st;
-  }
-  // the tokens are quantised straight from x in expert order (row_token), no bf16 x_perm
-  st = ffn_fp8(x, H, T, row_token, offsets, up_codes, up_scale, down_codes, down_scale,
-               static_cast<int>(rows), H, F, E, y_perm, w, stream);
+  int32_t* idx = topk_idx_out ? topk_idx_out : f.idx;
+  float* gates = gates_out ? gates_out : f.gates;
+  int st = quant_fwd_route(x, w_router, bias, T, H, E, k, f, idx, gates, stream);
   if (st) return st;
-  return launch_combine(y_perm, static_cast<int>(rows), slot_row, gates, T, H, k, y, stream);
+  // the tokens are quantised straight from x in expert order (row_token), no bf16 x_perm
+  st = ffn_fp8(x, H, T, f.row_token, f.offsets, up_codes, up_scale, down_codes, down_scale, rows,
+               H, F, E, f.y_perm, w, stream);
+  if (st) return st;
+  return launch_combine(f.y_perm, rows, f.slot_row, gates, T, H, k, y, stream);
 }
 
 size_t moe_forward_shared_workspace_size(int T, int H, int E, int k, int F, int Fs) {
@@ -1038,6 +1021,82 @@ int latent_moe_shared(const uint16_t* x, const uint16_t* w_in, const uint16_t* w
   o.add = y_s;
   o.ld_add = H;
   return launch_grouped_gemm(o, stream);
+}
+
+// ------------------------------------------------------------ quantised activation views ----
+
+int moe_grouped_ffn_nvfp4_view(int rows, int H, int F, int E, const void* workspace,
+                               size_t workspace_bytes, moe_quant_view* out) {
+  if (rows < 0 || H <= 0 || F <= 0 || E < 1 || E > 1024 || !out) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(rows) + 127LL * E + 127 > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+  Carver c(const_cast<void*>(workspace), workspace_bytes);
+  const Fp4Ws w = carve_fp4(c, rows, H, F, E);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  *out = moe_quant_view{};
+  out->padded_offsets = w.poff;
+  out->amax = w.amax;
+  out->x_codes = w.xq;
+  out->x_scales = w.xsf;
+  out->h = w.h;
+  out->h_codes = w.hq;
+  out->h_scales = w.hsf;
+  out->buffer_rows = w.P;
+  return MOE_OK;
+}
+
+int moe_forward_nvfp4_view(int T, int H, int E, int k, int F, const void* workspace,
+                           size_t workspace_bytes, moe_quant_view* out) {
+  if (!dims_ok(T, H, E, k) || F <= 0 || !out) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * k + 127LL * E + 127 > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+  Carver c(const_cast<void*>(workspace), workspace_bytes);
+  const QuantFwdWs f = carve_quant_fwd(c, T, H, E, k);
+  const Fp4Ws w = carve_fp4(c, T * k, H, F, E);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  *out = moe_quant_view{};
+  out->offsets = f.offsets;
+  out->row_token = f.row_token;
+  out->padded_offsets = w.poff;
+  out->amax = w.amax;
+  out->x_codes = w.xq;
+  out->x_scales = w.xsf;
+  out->h = w.h;
+  out->h_codes = w.hq;
+  out->h_scales = w.hsf;
+  out->buffer_rows = w.P;
+  return MOE_OK;
+}
+
+int moe_grouped_ffn_fp8_view(int rows, int H, int F, int E, const void* workspace,
+                             size_t workspace_bytes, moe_quant_view* out) {
+  if (rows < 0 || H <= 0 || F <= 0 || E < 1 || E > 1024 || !out) return MOE_ERR_INVALID_ARG;
+  Carver c(const_cast<void*>(workspace), workspace_bytes);
+  const Fp8Ws w = carve_fp8(c, rows, H, F);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  *out = moe_quant_view{};
+  out->amax = w.amax;
+  out->x_codes = w.xq;
+  out->h = w.h;
+  out->h_codes = w.hq;
+  out->buffer_rows = rows;
+  return MOE_OK;
+}
+
+int moe_forward_fp8_view(int T, int H, int E, int k, int F, const void* workspace,
+                         size_t workspace_bytes, moe_quant_view* out) {
+  if (!dims_ok(T, H, E, k) || F <= 0 || !out) return MOE_ERR_INVALID_ARG;
+  Carver c(const_cast<void*>(workspace), workspace_bytes);
+  const QuantFwdWs f = carve_quant_fwd(c, T, H, E, k);
+  const Fp8Ws w = carve_fp8(c, T * k, H, F);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  *out = moe_quant_view{};
+  out->offsets = f.offsets;
+  out->row_token = f.row_token;
+  out->amax = w.amax;
+  out->x_codes = w.xq;
+  out->h = w.h;
+  out->h_codes = w.hq;
+  out->buffer_rows = T * k;
+  return MOE_OK;
 }
 
 }  // extern "C"

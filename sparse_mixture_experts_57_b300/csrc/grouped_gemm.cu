@@ -61,7 +61,7 @@ struct KArgs {
   long long ld_add;
   const uint32_t* a_amax;  // E4M3 kernels: activation amax (fp32 bits)
   const float* w_scale;    // E4M3 kernels: per-group weight scale
-  uint32_t* out_amax;      // max of the stored squared-ReLU outputs, or null
+  uint32_t* out_amax;      // max of the stored (bf16) squared-ReLU outputs, or null
 };
 
 template <int BN>
@@ -569,8 +569,7 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
     if (F8 && a.out_amax) {
 #pragma unroll
       for (int d = 16; d > 0; d >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, d));
-      // squared-ReLU outputs are >= 0: their fp32 bit patterns order like their values
-      if (lane == 0 && vmax > 0.f) atomicMax(a.out_amax, __float_as_uint(vmax));
+      if (lane == 0) record_stored_amax(a.out_amax, vmax);
     }
   }
 

@@ -466,8 +466,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (a.out_amax) {
 #pragma unroll
       for (int d = 16; d > 0; d >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, d));
-      // squared ReLU outputs are >= 0: their fp32 bit patterns order like their values
-      if (lane == 0 && vmax > 0.f) atomicMax(a.out_amax, __float_as_uint(vmax));
+      if (lane == 0) record_stored_amax(a.out_amax, vmax);
     }
   }
 

@@ -21,6 +21,17 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// Record the amax of a tile's stored squared-ReLU outputs: `vmax` is the max of the fp32
+// values before their rounding to bf16. Rounding to nearest is monotonic, so the max of the
+// stored bf16 values is the rounded max. Outputs are >= 0, so fp32 bit patterns order like
+// the values and an integer atomicMax keeps the largest.
+__device__ __forceinline__ void record_stored_amax(uint32_t* amax, float vmax) {
+  uint16_t b;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(b) : "f"(vmax));
+  const uint32_t bits = static_cast<uint32_t>(b) << 16;
+  if (bits != 0u) atomicMax(amax, bits);
+}
+
 // ------------------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -48,10 +59,11 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity
       : "memory");
   return done;
 }
-// Bounded wait for the phase with the given parity. Returns false after kWaitLimitNs, or
-// as soon as *abort_flag is set by another role of the same CTA.
+// Bounded wait for the phase with the given parity. Returns false after limit_ns, or as
+// soon as *abort_flag is set by another role of the same CTA.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort_flag) {
+                                          const volatile int* abort_flag,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
@@ -59,7 +71,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -81,3 +81,87 @@ def gates_by_expert(idx: np.ndarray, gates: np.ndarray) -> np.ndarray:
 
 def to_dev(a, device="cuda"):
     return moe_synth.to_torch(a, device)
+
+
+# ------------------------------------------------------------------ format decoding ----
+# Plain decoders of the library's documented NVFP4 and FP8 storage formats (include/moe.h).
+
+E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def decode_codes(codes: np.ndarray) -> np.ndarray:
+    """uint8 [..., K/2] -> E2M1 values [..., K]; element 2i in the low nibble."""
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(*codes.shape[:-1], -1)
+    mag = E2M1_MAG[nib & 7]
+    return np.where(nib & 8, -mag, mag)
+
+
+def decode_e4m3_scale(b: np.ndarray) -> np.ndarray:
+    """Non-negative E4M3 scale bytes (exponent bias 7, 3 mantissa bits) -> values."""
+    b = b.astype(np.int64)
+    e, m = (b >> 3) & 15, b & 7
+    return np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * np.exp2(e - 7.0))
+
+
+def scale_rows(buf: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Scale atoms of one matrix -> E4M3 bytes [ceil(rows/128)*128, K/16] in row order."""
+    nb, ks = (rows + 127) // 128, K // 64
+    a = buf.reshape(nb, ks, 32, 4, 4)          # block, K step, r0, r1, kb
+    return a.transpose(0, 3, 2, 1, 4).reshape(nb * 128, ks * 4)
+
+
+def decode_e4m3(b: np.ndarray) -> np.ndarray:
+    """E4M3 bytes (sign bit 7, exponent bias 7, 3 mantissa bits) -> values."""
+    b = np.asarray(b).astype(np.int64)
+    mag = decode_e4m3_scale(b & 0x7F)
+    return np.where(b & 0x80, -mag, mag)
+
+
+def tie_matrix(N, K):
+    """Values exactly on every E2M1 rounding boundary of their block, and one bf16 step to
+    either side. The matrix amax is 168 = 2688 / 16, so g = 1/16 exactly; every other block
+    has amax 6 g s for a block scale s with few mantissa bits, so its divisor is s g exactly
+    and the boundaries t s g are exact bf16 values."""
+    g = 1.0 / 16
+    scales = [1.0, 1.25, 1.5, 1.75, 0.5625, 3.0, 0.75, 2.5]
+    bounds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    w = np.zeros((N, K), np.float32)
+    for r in range(N):
+        for b in range(K // 16):
+            sc = scales[(r + b) % len(scales)]
+            d = sc * g
+            blk = [6 * g * sc]
+            for i in range(15):
+                t = bounds[(r * 3 + b + i) % len(bounds)]
+                v = np.float32(t * d)
+                side = (i + r) % 3                  # on, below, above the boundary
+                if side:
+                    bits = moe_synth.bf16_bits(np.array([v], np.float32)).astype(np.int32)
+                    bits += 1 if side == 2 else -1
+                    v = O.widen_bf16(bits.astype(np.uint16))[0]
+                blk.append(v if (i + b) % 2 else -v)
+            w[r, 16 * b:16 * b + 16] = blk
+    w[0, 0] = 2688 * g                             # the matrix amax
+    return w
+
+
+def tie_matrix_e4m3(N, K):
+    """Values exactly halfway between neighbouring E4M3 values (times s = 2^-4), and one bf16
+    step to either side. amax = 448 / 16, so s = 1/16 exactly."""
+    s = 1.0 / 16
+    rng = np.random.default_rng(7)
+    w = np.zeros((N, K), np.float32)
+    for r in range(N):
+        for c in range(K):
+            ex = int(rng.integers(-6, 8))                # binade of the E4M3 value
+            m = int(rng.integers(0, 7))
+            lo = (1 + m / 8) * 2.0 ** ex
+            v = np.float32((lo + 2.0 ** (ex - 3) / 2) * s)   # midpoint to the next value
+            side = (r + c) % 3
+            if side:
+                bits = moe_synth.bf16_bits(np.array([v], np.float32)).astype(np.int32)
+                bits += 1 if side == 2 else -1
+                v = O.widen_bf16(bits.astype(np.uint16))[0]
+            w[r, c] = v if (r + c) % 2 else -v
+    w[0, 0] = 448 * s
+    return w

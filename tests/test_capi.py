@@ -72,3 +72,58 @@ def test_unaligned_sizes_are_unsupported():
     assert r == 2
     r = L.moe_linear(16, 16, 4, 96, 64, 16, None)
     assert r == 2
+
+
+@pytest.mark.parametrize("call,dims,size_fn", [
+    ("moe_forward_nvfp4_view", (300, 256, 64, 4, 192), "moe_forward_nvfp4_workspace_size"),
+    ("moe_grouped_ffn_nvfp4_view", (1200, 256, 192, 64), "moe_grouped_ffn_nvfp4_workspace_size"),
+    ("moe_forward_fp8_view", (300, 256, 64, 4, 192), "moe_forward_fp8_workspace_size"),
+    ("moe_grouped_ffn_fp8_view", (1200, 256, 192, 64), "moe_grouped_ffn_fp8_workspace_size"),
+])
+def test_quant_views_are_disjoint_slices_of_the_workspace(call, dims, size_fn):
+    """The views only compute addresses (no CUDA call): every buffer lies inside the
+    workspace the matching size query asks for, 256-byte aligned, and no two overlap."""
+    from sparse_mixture_experts_57_b300._binding import QuantView
+    L = moe.lib()
+    size = getattr(L, size_fn)(*dims)
+    base = 1 << 40                     # a fake device address: never dereferenced
+    v = QuantView()
+    assert getattr(L, call)(*dims, base, size, ctypes.byref(v)) == 0
+    nvfp4 = "nvfp4" in call
+    fwd = "forward" in call
+    if fwd:
+        T, H, E, k, F = dims
+        rows = T * k
+    else:
+        rows, H, F, E = dims
+    P = v.buffer_rows
+    if nvfp4:
+        assert P >= rows + 127 * E and P % 128 == 0
+        sf = lambda K: (P + 127) // 128 * (K // 64) * 512  # noqa: E731
+    else:
+        assert P == rows
+    ext = {"amax": 8, "x_codes": P * H // (2 if nvfp4 else 1), "h": P * F * 2,
+           "h_codes": P * F // (2 if nvfp4 else 1)}
+    if nvfp4:
+        ext.update(padded_offsets=(E + 1) * 4, x_scales=sf(H), h_scales=sf(F))
+    if fwd:
+        ext.update(offsets=(E + 1) * 4, row_token=rows * 4)
+    spans = []
+    for name, _ in QuantView._fields_:
+        if name == "buffer_rows":
+            continue
+        p = getattr(v, name)
+        if name not in ext:
+            assert p is None, name
+            continue
+        off = p - base
+        assert off % 256 == 0 and 0 <= off and off + ext[name] <= size, name
+        spans.append((off, off + ext[name], name))
+    spans.sort()
+    for a, b in zip(spans, spans[1:]):
+        assert a[1] <= b[0], (a, b)
+    # a workspace one byte short of what the call needs, and sizes the call rejects
+    assert getattr(L, call)(*dims, base, spans[-1][1] - 1, ctypes.byref(v)) == 3
+    bad = (dims[0], -1) + tuple(dims[2:])
+    assert getattr(L, call)(*bad, base, size, ctypes.byref(v)) == 1
+    assert getattr(L, call)(*dims, base, size, None) == 1

@@ -16,7 +16,7 @@ import pytest
 
 import moe_synth
 from oracle import moe_oracle as O
-from helpers import bf16_out, check_selection, to_dev
+from helpers import bf16_out, check_selection, decode_e4m3, tie_matrix_e4m3, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -40,14 +40,6 @@ def _status_ok(moe):
     assert moe.get_device_status() == 0
 
 
-def decode_e4m3(b: np.ndarray) -> np.ndarray:
-    """E4M3 bytes (sign bit 7, exponent bias 7, 3 mantissa bits) -> values."""
-    b = b.astype(np.int64)
-    e, m = (b >> 3) & 15, b & 7
-    mag = np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * np.exp2(e - 7.0))
-    return np.where(b & 0x80, -mag, mag)
-
-
 def _rel_checks(got, ref, what):
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     assert np.isfinite(got).all(), what
@@ -61,28 +53,6 @@ def _rel_checks(got, ref, what):
     assert worst <= ROW_REL_FP8, f"{what}: worst row relative error {worst:.3e}"
 
 
-def _tie_matrix(N, K):
-    """Values exactly halfway between neighbouring E4M3 values (times s = 2^-4), and one bf16
-    step to either side. amax = 448 / 16, so s = 1/16 exactly."""
-    s = 1.0 / 16
-    rng = np.random.default_rng(7)
-    w = np.zeros((N, K), np.float32)
-    for r in range(N):
-        for c in range(K):
-            ex = int(rng.integers(-6, 8))                # binade of the E4M3 value
-            m = int(rng.integers(0, 7))
-            lo = (1 + m / 8) * 2.0 ** ex
-            v = np.float32((lo + 2.0 ** (ex - 3) / 2) * s)   # midpoint to the next value
-            side = (r + c) % 3
-            if side:
-                bits = moe_synth.bf16_bits(np.array([v], np.float32)).astype(np.int32)
-                bits += 1 if side == 2 else -1
-                v = O.widen_bf16(bits.astype(np.uint16))[0]
-            w[r, c] = v if (r + c) % 2 else -v
-    w[0, 0] = 448 * s
-    return w
-
-
 def test_quantize_fp8_weights_bit_exact(moe):
     G, N, K = 5, 200, 320
     rng = np.random.default_rng(41)
@@ -90,7 +60,7 @@ def test_quantize_fp8_weights_bit_exact(moe):
     w[1] *= np.exp2(-(np.arange(N) % 24))[:, None].astype(np.float32)   # E4M3 subnormals
     w[2] = 0.0                                                          # zero matrix
     w[3, :, :40] = 0.0
-    w[4] = _tie_matrix(N, K)                                            # rounding ties
+    w[4] = tie_matrix_e4m3(N, K)                                            # rounding ties
     wb = moe_synth.bf16_bits(w)
     assert (O.widen_bf16(wb[4]) == w[4]).all()
     nv = moe.moe_quantize_fp8_weights(to_dev(wb))

@@ -17,13 +17,13 @@ import pytest
 
 import moe_synth
 from oracle import moe_oracle as O
-from helpers import REL_FROB_NVFP4, bf16_out, check_selection, to_dev
+from helpers import (REL_FROB_NVFP4, bf16_out, check_selection, decode_codes,
+                     decode_e4m3_scale as decode_e4m3, scale_rows, tie_matrix, to_dev)
 
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 ROW_REL_NVFP4 = 0.15
 
 
@@ -39,29 +39,6 @@ def moe():
 
 def _status_ok(moe):
     assert moe.get_device_status() == 0
-
-
-# -------------------------------------------------------------- format decoding ----
-# Plain decoders of the library's documented NVFP4 storage formats (include/moe.h).
-
-def decode_codes(codes: np.ndarray) -> np.ndarray:
-    """uint8 [..., K/2] -> E2M1 values [..., K]; element 2i in the low nibble."""
-    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(*codes.shape[:-1], -1)
-    mag = E2M1_MAG[nib & 7]
-    return np.where(nib & 8, -mag, mag)
-
-
-def decode_e4m3(b: np.ndarray) -> np.ndarray:
-    b = b.astype(np.int64)
-    e, m = (b >> 3) & 15, b & 7
-    return np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * np.exp2(e - 7.0))
-
-
-def scale_rows(buf: np.ndarray, rows: int, K: int) -> np.ndarray:
-    """Scale atoms of one matrix -> E4M3 bytes [ceil(rows/128)*128, K/16] in row order."""
-    nb, ks = (rows + 127) // 128, K // 64
-    a = buf.reshape(nb, ks, 32, 4, 4)          # block, K step, r0, r1, kb
-    return a.transpose(0, 3, 2, 1, 4).reshape(nb * 128, ks * 4)
 
 
 def _rel_checks(got, ref, what):
@@ -80,34 +57,6 @@ def _rel_checks(got, ref, what):
 
 # --------------------------------------------------------------------- quantiser ----
 
-def _tie_matrix(N, K):
-    """Values exactly on every E2M1 rounding boundary of their block, and one bf16 step to
-    either side. The matrix amax is 168 = 2688 / 16, so g = 1/16 exactly; every other block
-    has amax 6 g s for a block scale s with few mantissa bits, so its divisor is s g exactly
-    and the boundaries t s g are exact bf16 values."""
-    g = 1.0 / 16
-    scales = [1.0, 1.25, 1.5, 1.75, 0.5625, 3.0, 0.75, 2.5]
-    bounds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
-    w = np.zeros((N, K), np.float32)
-    for r in range(N):
-        for b in range(K // 16):
-            sc = scales[(r + b) % len(scales)]
-            d = sc * g
-            blk = [6 * g * sc]
-            for i in range(15):
-                t = bounds[(r * 3 + b + i) % len(bounds)]
-                v = np.float32(t * d)
-                side = (i + r) % 3                  # on, below, above the boundary
-                if side:
-                    bits = moe_synth.bf16_bits(np.array([v], np.float32)).astype(np.int32)
-                    bits += 1 if side == 2 else -1
-                    v = O.widen_bf16(bits.astype(np.uint16))[0]
-                blk.append(v if (i + b) % 2 else -v)
-            w[r, 16 * b:16 * b + 16] = blk
-    w[0, 0] = 2688 * g                             # the matrix amax
-    return w
-
-
 def test_quantize_weights_bit_exact(moe):
     G, N, K = 5, 200, 320                  # ragged last 128-row block, 5 K steps
     rng = np.random.default_rng(31)
@@ -116,7 +65,7 @@ def test_quantize_weights_bit_exact(moe):
     w[1] *= np.exp2(-(np.arange(N) % 24))[:, None].astype(np.float32)
     w[2] = 0.0                             # all-zero matrix: g = 0, every scale 0
     w[3, :, :16] = 0.0                     # all-zero blocks inside a live matrix
-    w[4] = _tie_matrix(N, K)               # rounding ties and their neighbours
+    w[4] = tie_matrix(N, K)               # rounding ties and their neighbours
     wb = moe_synth.bf16_bits(w)
     assert (O.widen_bf16(wb[4]) == w[4]).all()     # the tie values are exact in bf16
     nv = moe.moe_quantize_nvfp4_weights(to_dev(wb))
