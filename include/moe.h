@@ -124,6 +124,9 @@ int moe_route_dispatch(const uint16_t* x, const uint16_t* w_router, const float*
  *    start at zero: each call overwrites every word it reads.
  *  - The first call on each device looks up the array's device address with that device
  *    current. Make that first call before any stream capture.
+ *  - The library caches that address, and the device status word's, per device for the
+ *    life of the process. Do not keep using the library on a device after
+ *    cudaDeviceReset() there: the cached addresses belong to the destroyed context.
  * Arguments, layouts and device-side error reporting are those of moe_permute.
  * ------------------------------------------------------------------------------------- */
 size_t moe_permute_noalloc_max_scratch_bytes(void);

@@ -50,13 +50,13 @@ int sm_count() {
 
 int cuda_status(cudaError_t) { return MOE_ERR_CUDA; }
 
-namespace {
-
 bool dims_ok(int T, int D, int E, int k) {
   if (T < 0 || D <= 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return false;
   if (static_cast<long long>(T) * k > 0x7fffffffLL) return false;
   return true;
 }
+
+namespace {
 
 // Workspace of one routed MoE layer of width D: routing, permutation, FFN buffers.
 struct LayerWs {

@@ -15,6 +15,10 @@ int* status_word();
 // Streaming-multiprocessor count of the current device.
 int sm_count();
 
+// Sizes every routed-layer call accepts: T >= 0 tokens of width D > 0, 1 <= E <= 1024
+// experts, 1 <= k <= min(32, E) of them per token, T * k rows addressable by int32.
+bool dims_ok(int T, int D, int E, int k);
+
 // Record the first failing CUDA call and map it to a status code.
 int cuda_status(cudaError_t e);
 #define MOE_CUDA(call)                                \

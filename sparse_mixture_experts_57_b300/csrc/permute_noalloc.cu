@@ -59,8 +59,7 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_idx, const uint16_t* x, i
                                    int32_t* row_token, int32_t* slot_row, uint16_t* x_perm,
                                    cudaStream_t stream) {
   using namespace moe;
-  if (T < 0 || H <= 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return MOE_ERR_INVALID_ARG;
-  if (static_cast<long long>(T) * k > 0x7fffffffLL) return MOE_ERR_INVALID_ARG;
+  if (!dims_ok(T, H, E, k)) return MOE_ERR_INVALID_ARG;  // the limits moe_permute applies
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!topk_idx || !x || !row_token || !slot_row || !x_perm))
     return MOE_ERR_INVALID_ARG;

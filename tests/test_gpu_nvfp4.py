@@ -136,6 +136,10 @@ def _offsets(counts):
     ([128, 256, 127, 3], 256, 128),            # exact tile multiples and near misses
     ([40] * 30 + [700, 0], 512, 448),          # many small groups, one large, ragged N tiles
     ([90, 410, 5, 260], 2688, 1856),           # Nano widths: K tails of 2 and 1 MMA steps
+    # many rows per expert: several row tiles per group with a partial last one, a ragged
+    # single column tile (N = 192) and a K tail of one MMA step in a partial stage (K = 320)
+    ([300, 0, 1, 129, 1000, 600], 320, 192),
+    ([90, 410, 5, 700, 300], 2688, 1856),      # Nano widths, many row tiles per group
 ])
 def test_grouped_ffn_nvfp4(moe, counts, H, F):
     E = len(counts)
@@ -170,7 +174,7 @@ def _layer_nvfp4(moe, w):
 
 
 @pytest.mark.parametrize("T,H,E,k,F", [(256, 256, 16, 2, 128), (700, 320, 10, 3, 192),
-                                       (1, 64, 4, 1, 64)])
+                                       (1, 64, 4, 1, 64), (2048, 256, 8, 2, 192)])
 def test_layer_nvfp4(moe, T, H, E, k, F):
     w = moe_synth.Workload("nvfp4_small", T=T, H=H, E=E, k=k, F=F, seed=T + H, nvfp4=True)
     inp, gi, got = _layer_nvfp4(moe, w)

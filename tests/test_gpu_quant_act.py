@@ -146,6 +146,7 @@ def moe_nvfp4_sf_bytes(rows, K):
 @pytest.mark.parametrize("counts,H,F", [
     ([300, 0, 1, 127, 128, 129, 57, 3], 320, 192),
     ([0, 1, 0, 256, 2], 256, 128),
+    ([300, 0, 1, 600, 257], 256, 192),         # several row tiles per group
 ])
 def test_grouped_ffn_nvfp4_activation_bytes(moe, counts, H, F):
     E = len(counts)

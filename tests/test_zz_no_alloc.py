@@ -78,6 +78,37 @@ def test_no_alloc_permute_matches_workspace_permute_twice(lib):
     assert status.value == 0
 
 
+def test_no_alloc_permute_at_capacity_and_empty(lib):
+    """The largest problem the array holds (ceil(T/32) * E * 8 bytes = exactly 2 MiB:
+    T = 16384 tokens, E = 512 experts) is accepted and matches moe_permute bit for bit; a
+    call with T = 0 writes all-zero counts and offsets."""
+    stream = torch.cuda.current_stream().cuda_stream
+    T, E, k, H = 16384, 512, 2, 64
+    assert (T + 31) // 32 * E * 8 == lib.moe_permute_noalloc_max_scratch_bytes()
+    idx = moe_synth.to_torch(moe_synth.random_topk(13, T, E, k, 0.7), "cuda")
+    x = moe_synth.to_torch(moe_synth.normal_bf16(13, 50, (T, H), 1.0), "cuda")
+    ref = _call_with_workspace(lib, idx, x, T, H, E, k, stream)
+    got = _call_no_alloc(lib, idx, x, T, H, E, k, stream)
+    torch.cuda.synchronize()
+    for key in ("counts", "offsets", "row_token", "slot_row"):
+        assert torch.equal(got[key], ref[key]), key
+    assert torch.equal(got["x_perm"].view(torch.int16), ref["x_perm"].view(torch.int16))
+    # T = 0: counts and offsets are written (zeros), nothing else is touched
+    out = _buffers(0, H, E, k)
+    out["counts"].fill_(-7)
+    out["offsets"].fill_(-7)
+    rc = lib.moe_permute_noalloc(idx.data_ptr(), x.data_ptr(), 0, H, E, k,
+                                 out["counts"].data_ptr(), out["offsets"].data_ptr(),
+                                 out["row_token"].data_ptr(), out["slot_row"].data_ptr(),
+                                 out["x_perm"].data_ptr(), stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(out["counts"].abs().sum()) == 0 and int(out["offsets"].abs().sum()) == 0
+    status = ctypes.c_int(-1)
+    assert lib.moe_get_device_status(stream, ctypes.byref(status)) == 0
+    assert status.value == 0
+
+
 def test_no_alloc_permute_refuses_oversized_problems(lib):
     cap = lib.moe_permute_noalloc_max_scratch_bytes()
     assert cap == 2 << 20
