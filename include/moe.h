@@ -423,6 +423,24 @@ int moe_forward_fp8_view(int T, int H, int E, int k, int F, const void* workspac
 int moe_selftest_wait_timeout(const void* src, int limit_us, int blocks, int* report,
                               cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Debug build. The library also builds as libmoe_debug.so (compiled with MOE_DEBUG), with
+ * the same entry points and results plus checks that the release build leaves out:
+ *  - every workspace slice is followed by a 256-byte guard region (the *_workspace_size
+ *    queries of that build include them); each call fills its guards before its first kernel
+ *    and checks them after its last one, and a damaged guard (a kernel that wrote past its
+ *    slice) is reported as MOE_ERR_WORKSPACE on the device status word;
+ *  - device-side range checks of indices the library itself produced (row_token in the row
+ *    copy, slot_row in the combine), reported as MOE_ERR_INVALID_ARG on the status word.
+ * moe_debug_build() returns 1 in that build and 0 in the release build.
+ * moe_debug_guard_selftest() checks the guard detector: it carves two slices of `workspace`
+ * (at least 8 KiB, device), fills their guards, overwrites one guard byte with
+ * cudaMemsetAsync and runs the check, which must leave MOE_ERR_WORKSPACE on the status word.
+ * The release build returns MOE_ERR_UNSUPPORTED from it.
+ * ------------------------------------------------------------------------------------- */
+int moe_debug_build(void);
+int moe_debug_guard_selftest(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -8,6 +8,7 @@ There is no CPU fallback: without the built library or a CUDA device, every call
 from __future__ import annotations
 
 import ctypes
+import os
 import threading
 
 import torch
@@ -74,6 +75,8 @@ SIGNATURES = {
     "moe_grouped_ffn_fp8_view": (_I, [_I, _I, _I, _I, _VP, _SZ, _QV]),
     "moe_forward_fp8_view": (_I, [_I, _I, _I, _I, _I, _VP, _SZ, _QV]),
     "moe_selftest_wait_timeout": (_I, [_VP, _I, _I, _VP, _VP]),
+    "moe_debug_build": (_I, []),
+    "moe_debug_guard_selftest": (_I, [_VP, _SZ, _VP]),
     "moe_forward_shared_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_shared": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP,
                                 _VP, _VP, _VP, _SZ, _VP]),
@@ -93,11 +96,13 @@ class MoeError(RuntimeError):
 
 
 def lib() -> ctypes.CDLL:
-    """Load (building first if needed) the in-tree libmoe.so."""
+    """Load (building first if needed) the in-tree libmoe.so, or libmoe_debug.so (the
+    MOE_DEBUG build: workspace guards and extra device checks) when the environment variable
+    MOE_DEBUG is 1 at the first call."""
     global _LIB
     with _lock:
         if _LIB is None:
-            path = _build.ensure_built()
+            path = _build.ensure_built(debug=os.environ.get("MOE_DEBUG") == "1")
             L = ctypes.CDLL(path)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(L, name)

@@ -3,6 +3,10 @@
 The shared library is compiled from csrc/*.cu with the public header in include/. A
 sidecar file records a hash of the sources, flags and header; the library is rebuilt
 whenever they change, so a stale binary is never loaded.
+
+build(debug=True) builds libmoe_debug.so from the same sources with MOE_DEBUG defined:
+workspace guard regions checked after every call and device-side range checks of the
+library's own indices, reported on the device status word (include/moe.h).
 """
 from __future__ import annotations
 
@@ -19,7 +23,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmoe.so")
-STAMP = LIB + ".buildinfo"
+DEBUG_LIB = os.path.join(PKG, "libmoe_debug.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,9 +42,17 @@ def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _digest() -> str:
+def _flags(debug: bool) -> list[str]:
+    return FLAGS + (["-DMOE_DEBUG=1"] if debug else [])
+
+
+def lib_path(debug: bool = False) -> str:
+    return DEBUG_LIB if debug else LIB
+
+
+def _digest(debug: bool = False) -> str:
     h = hashlib.sha256()
-    h.update(" ".join(ARCH + FLAGS).encode())
+    h.update(" ".join(ARCH + _flags(debug)).encode())
     files = sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) +
                                glob.glob(os.path.join(CSRC, "*.h")) +
                                glob.glob(os.path.join(INCLUDE, "*.h")))
@@ -51,23 +63,27 @@ def _digest() -> str:
     return h.hexdigest()
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+def up_to_date(debug: bool = False) -> bool:
+    lib = lib_path(debug)
+    stamp = lib + ".buildinfo"
+    if not os.path.exists(lib) or not os.path.exists(stamp):
         return False
-    with open(STAMP) as f:
-        return f.read().strip() == _digest()
+    with open(stamp) as f:
+        return f.read().strip() == _digest(debug)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    lib = lib_path(debug)
+    if not force and up_to_date(debug):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    bdir = os.path.join(BUILD_DIR, "debug") if debug else BUILD_DIR
+    os.makedirs(bdir, exist_ok=True)
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *_flags(debug), "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -79,21 +95,22 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt",
            "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
-        f.write(_digest())
-    return LIB
+    os.replace(tmp, lib)
+    with open(lib + ".buildinfo", "w") as f:
+        f.write(_digest(debug))
+    return lib
 
 
-def ensure_built() -> str:
-    return build(force=False)
+def ensure_built(debug: bool = False) -> str:
+    return build(force=False, debug=debug)
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -177,7 +177,7 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
                             w.tie, w.counts, w.offsets, w.row_token, w.slot_row, w.sync, s);
     if (st) return st;
     if (!gather) {
-      st = launch_gather_rows(w.row_token, x, ldx, rows, D, w.x_perm, s);
+      st = launch_gather_rows(w.row_token, x, ldx, T, rows, D, w.x_perm, s);
       if (st) return st;
     }
   } else {
@@ -481,8 +481,10 @@ size_t moe_route_workspace_size(int T, int D, int E, int k) {
   (void)D;
   (void)k;
   if (T < 0 || E < 1) return 0;
-  return align_up(static_cast<size_t>(T) * E * sizeof(float), 256) +
-         align_up(route_fused_sync_ints(T) * sizeof(int), 256) + 256;
+  Carver c(nullptr, 0);
+  c.take<float>(static_cast<size_t>(T) * E);
+  c.take<int>(route_fused_sync_ints(T));
+  return c.used + 256;
 }
 
 int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int D, int E,
@@ -496,6 +498,7 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, in
   float* logits = c.take<float>(static_cast<size_t>(T) * E);
   int* sync = c.take<int>(route_fused_sync_ints(T));
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   if (route_fused_ok(T, D, E, k, 1))  // small batches: logits and top-k in one kernel
     return launch_route_fused(x, D, w_router, bias, T, D, E, k, 1, logits, topk_idx, gates,
                               tie_flag, nullptr, nullptr, nullptr, nullptr, sync, stream);
@@ -506,7 +509,11 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, in
 
 size_t moe_route_dispatch_workspace_size(int T, int D, int E, int k) {
   if (!dims_ok(T, D, E, k)) return 0;
-  return moe_route_workspace_size(T, D, E, k) + permute_scratch_bytes(T, E) + 512;
+  Carver c(nullptr, 0);
+  c.take<float>(static_cast<size_t>(T) * E);
+  c.take<int>(route_fused_sync_ints(T));
+  c.take<char>(permute_scratch_bytes(T, E));
+  return c.used + 256;
 }
 
 int moe_route_dispatch(const uint16_t* x, const uint16_t* w_router, const float* bias, int T,
@@ -530,13 +537,14 @@ int moe_route_dispatch(const uint16_t* x, const uint16_t* w_router, const float*
   int* sync = c.take<int>(route_fused_sync_ints(T));
   void* scratch = c.take<char>(permute_scratch_bytes(T, E));
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   if (route_fused_ok(T, D, E, k, 1)) {
     // small batches: logits, top-k and the dispatch maps in one kernel, then the row copy
     const int st = launch_route_fused(x, D, w_router, bias, T, D, E, k, 1, logits, topk_idx,
                                       gates, tie_flag, counts, offsets, row_token, slot_row,
                                       sync, stream);
     if (st) return st;
-    return launch_gather_rows(row_token, x, D, T * k, D, x_perm, stream);
+    return launch_gather_rows(row_token, x, D, T, T * k, D, x_perm, stream);
   }
   int st = router_logits(x, D, w_router, T, D, E, 1, logits, stream);
   if (st) return st;
@@ -549,7 +557,9 @@ int moe_route_dispatch(const uint16_t* x, const uint16_t* w_router, const float*
 size_t moe_permute_workspace_size(int T, int E, int k) {
   (void)k;
   if (T < 0 || E < 1) return 0;
-  return permute_scratch_bytes(T, E) + 256;
+  Carver c(nullptr, 0);
+  c.take<char>(permute_scratch_bytes(T, E));
+  return c.used + 256;
 }
 
 int moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int H, int E, int k,
@@ -563,6 +573,10 @@ int moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int H, int E,
   Carver c(workspace, workspace_bytes);
   void* scratch = c.take<char>(permute_scratch_bytes(T, E));
   if (T > 0 && !c.ok()) return MOE_ERR_WORKSPACE;
+  if (T == 0)
+    return launch_permute(topk_idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row,
+                          x_perm, scratch, stream);
+  const WsGuard guard(c, stream);
   return launch_permute(topk_idx, x, H, T, H, E, k, counts, offsets, row_token, slot_row, x_perm,
                         scratch, stream);
 }
@@ -571,7 +585,9 @@ size_t moe_grouped_ffn_workspace_size(int rows, int H, int F, int E) {
   (void)H;
   (void)E;
   if (rows < 0 || F < 0) return 0;
-  return align_up(static_cast<size_t>(rows) * F * 2, 256) + 256;
+  Carver c(nullptr, 0);
+  c.take<uint16_t>(static_cast<size_t>(rows) * F);
+  return c.used + 256;
 }
 
 int moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_up,
@@ -586,6 +602,7 @@ int moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16
   Carver c(workspace, workspace_bytes);
   uint16_t* h = c.take<uint16_t>(static_cast<size_t>(rows) * F);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   return ffn(x_perm, offsets, w_up, w_down, rows, H, F, E, h, y_perm, stream);
 }
 
@@ -639,6 +656,7 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* bias,
   Carver c(workspace, workspace_bytes);
   const LayerWs w = carve_layer(c, T, H, E, k, F);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   return layer(x, H, x, H, H, 1, w_router, bias, w_up, w_down, T, H, E, k, F, y, topk_idx_out,
                gates_out, w, stream);
 }
@@ -656,6 +674,7 @@ int moe_forward_gathered(const uint16_t* x, const uint16_t* w_router, const floa
   Carver c(workspace, workspace_bytes);
   const LayerWs w = carve_layer(c, T, H, E, k, F);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   return layer(x, H, x, H, H, 1, w_router, bias, w_up, w_down, T, H, E, k, F, y, topk_idx_out,
                gates_out, w, stream, nullptr, true);
 }
@@ -688,6 +707,7 @@ int latent_moe(const uint16_t* x, const uint16_t* w_in, const uint16_t* w_out,
   uint16_t* y_lat = c.take<uint16_t>(static_cast<size_t>(T) * L);
   const LayerWs w = carve_layer(c, T, L, Ep, kp, F);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
 
   // x_lat = x . w_in^T  (H -> L). With routing on the latent vector, the epilogue writes
   // x_lat as three bf16 planes hi | mid | lo (sum within about 2^-24 of the fp32 value):
@@ -796,6 +816,7 @@ int moe_grouped_ffn_nvfp4(const uint16_t* x_perm, const int32_t* offsets,
   Carver c(workspace, workspace_bytes);
   const Fp4Ws w = carve_fp4(c, rows, H, F, E);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   return ffn_nvfp4(x_perm, H, rows, nullptr, offsets, {up_codes, up_scales, up_gscale},
                    {down_codes, down_scales, down_gscale}, rows, H, F, E, y_perm, w, stream);
 }
@@ -828,6 +849,7 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
   const QuantFwdWs f = carve_quant_fwd(c, T, H, E, k);
   const Fp4Ws w = carve_fp4(c, rows, H, F, E);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   int32_t* idx = topk_idx_out ? topk_idx_out : f.idx;
   float* gates = gates_out ? gates_out : f.gates;
   // routing and dispatch stay in bf16/fp32; the expert FFNs run in NVFP4
@@ -876,6 +898,7 @@ int moe_grouped_ffn_fp8(const uint16_t* x_perm, const int32_t* offsets, const ui
   Carver c(workspace, workspace_bytes);
   const Fp8Ws w = carve_fp8(c, rows, H, F);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   return ffn_fp8(x_perm, H, rows, nullptr, offsets, up_codes, up_scale, down_codes, down_scale,
                  rows, H, F, E, y_perm, w, stream);
 }
@@ -905,6 +928,7 @@ int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bi
   const QuantFwdWs f = carve_quant_fwd(c, T, H, E, k);
   const Fp8Ws w = carve_fp8(c, rows, H, F);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   int32_t* idx = topk_idx_out ? topk_idx_out : f.idx;
   float* gates = gates_out ? gates_out : f.gates;
   int st = quant_fwd_route(x, w_router, bias, T, H, E, k, f, idx, gates, stream);
@@ -942,6 +966,7 @@ int moe_forward_shared(const uint16_t* x, const uint16_t* w_router, const float*
   uint16_t* h_s = c.take<uint16_t>(static_cast<size_t>(T) * Fs);
   uint16_t* y_s = c.take<uint16_t>(static_cast<size_t>(T) * H);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
   int st = shared_expert(x, H, T, H, Fs, w_up_shared, w_down_shared, h_s, y_s, stream);
   if (st) return st;
   // the combine adds the shared expert's output into its fp32 sum
@@ -951,10 +976,14 @@ int moe_forward_shared(const uint16_t* x, const uint16_t* w_router, const float*
 
 size_t latent_moe_shared_workspace_size(int T, int H, int L, int Ep, int kp, int F, int Fs,
                                         int router_on_latent) {
-  const size_t base = latent_moe_workspace_size(T, H, L, Ep, kp, F, router_on_latent);
-  if (!base || Fs <= 0) return 0;
-  return base + align_up(static_cast<size_t>(T) * Fs * 2, 256) +
-         align_up(static_cast<size_t>(T) * H * 2, 256) + 512;
+  if (!dims_ok(T, L, Ep, kp) || H <= 0 || F <= 0 || Fs <= 0) return 0;
+  Carver c(nullptr, 0);
+  c.take<uint16_t>(static_cast<size_t>(T) * L * (router_on_latent ? 3 : 1));  // x_lat planes
+  c.take<uint16_t>(static_cast<size_t>(T) * L);                               // y_lat
+  carve_layer(c, T, L, Ep, kp, F);
+  c.take<uint16_t>(static_cast<size_t>(T) * Fs);  // h of the shared expert
+  c.take<uint16_t>(static_cast<size_t>(T) * H);   // its output
+  return c.used + 256;
 }
 
 int latent_moe_shared(const uint16_t* x, const uint16_t* w_in, const uint16_t* w_out,
@@ -980,6 +1009,7 @@ int latent_moe_shared(const uint16_t* x, const uint16_t* w_in, const uint16_t* w
   uint16_t* h_s = c.take<uint16_t>(static_cast<size_t>(T) * Fs);
   uint16_t* y_s = c.take<uint16_t>(static_cast<size_t>(T) * H);
   if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
 
   // shared expert in H on the token itself (Nemotron 3 notes §2.2)
   int st = shared_expert(x, H, T, H, Fs, w_up_shared, w_down_shared, h_s, y_s, stream);

@@ -31,7 +31,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 __global__ void k_combine(const uint16_t* __restrict__ y_perm, int rows,
                           const int32_t* __restrict__ slot_row, const float* __restrict__ gates,
                           int T, int H, int k, const uint16_t* __restrict__ addend,
-                          uint16_t* __restrict__ y) {
+                          uint16_t* __restrict__ y, int* status) {
   griddep_wait();
   griddep_launch_dependents();
   const int nvec = H / 8;
@@ -48,7 +48,12 @@ __global__ void k_combine(const uint16_t* __restrict__ y_perm, int rows,
   for (int j = 0; j < k; ++j) {
     const int r = __ldg(sr + j);
     const float g = __ldg(gg + j);
-    if (r < 0 || r >= rows) continue;
+    if (r < 0 || r >= rows) {  // skipped; the MOE_DEBUG build also reports it
+      if constexpr (kDebugBuild) {
+        if (v == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+      }
+      continue;
+    }
     const uint4 yv =
         __ldg(reinterpret_cast<const uint4*>(y_perm + static_cast<long long>(r) * H) + v);
     acc8(a, yv, g);
@@ -64,8 +69,11 @@ int launch_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row, co
   if (T <= 0) return MOE_OK;
   const int threads = 256;
   const long long n = static_cast<long long>(T) * (H / 8);
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
   return launch_pdl(k_combine, dim3(static_cast<unsigned>((n + threads - 1) / threads)),
-                    dim3(threads), 0, s, y_perm, rows, slot_row, gates, T, H, k, addend, y);
+                    dim3(threads), 0, s, y_perm, rows, slot_row, gates, T, H, k, addend, y,
+                    status);
 }
 
 }  // namespace moe

@@ -65,10 +65,21 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Bump allocator over a caller-provided workspace (256-byte aligned slices).
+// In the MOE_DEBUG build every slice is followed by a 256-byte guard region; the entry
+// points fill the guards with a pattern before their first kernel and check them after the
+// last one (WsGuard), so a kernel that writes past its slice is reported on the status word
+// as MOE_ERR_WORKSPACE. The workspace-size queries carve the same way, so they include the
+// guards.
+constexpr int kMaxWsGuards = 64;
+constexpr size_t kWsGuardBytes = 256;
 struct Carver {
   char* base;
   size_t cap;
   size_t used = 0;
+#ifdef MOE_DEBUG
+  char* guards[kMaxWsGuards];
+  int nguards = 0;
+#endif
   Carver(void* b, size_t c) : base(static_cast<char*>(b)), cap(c) {}
   // Slices start on 256-byte device addresses whatever the alignment of `base`; the
   // workspace-size queries therefore add 256 bytes of slack.
@@ -78,10 +89,37 @@ struct Carver {
     used = align_up(b + used, 256) - b;
     T* p = base ? reinterpret_cast<T*>(base + used) : nullptr;
     used += count * sizeof(T);
+#ifdef MOE_DEBUG
+    used = align_up(b + used, 256) - b;
+    if (base && nguards < kMaxWsGuards) guards[nguards++] = base + used;
+    used += kWsGuardBytes;
+#endif
     return p;
   }
   bool ok() const { return base != nullptr && used <= cap; }
 };
+
+// MOE_DEBUG build: fills the workspace guards of `c` (stream-ordered) when constructed and
+// checks them when destroyed, i.e. after the entry point has enqueued its last kernel. The
+// release build compiles this to nothing.
+struct WsGuard {
+#ifdef MOE_DEBUG
+  WsGuard(const Carver& c, cudaStream_t s);
+  ~WsGuard();
+  const Carver& c_;
+  cudaStream_t s_;
+#else
+  WsGuard(const Carver&, cudaStream_t) {}
+#endif
+};
+
+// Whether this library was built with MOE_DEBUG (extra device-side checks, workspace guards).
+constexpr bool kDebugBuild =
+#ifdef MOE_DEBUG
+    true;
+#else
+    false;
+#endif
 
 // Epilogues of the grouped GEMM.
 enum Epilogue : int {
@@ -226,9 +264,10 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
                        int32_t* idx, float* gates, uint8_t* tie, int32_t* counts,
                        int32_t* offsets, int32_t* row_token, int32_t* slot_row, int* sync,
                        cudaStream_t s);
-// x_perm[r] = x[row_token[r]] for r < rows.
-int launch_gather_rows(const int32_t* row_token, const uint16_t* x, int64_t ldx, int rows, int H,
-                       uint16_t* x_perm, cudaStream_t s);
+// x_perm[r] = x[row_token[r]] for r < rows (x has src_rows rows; the MOE_DEBUG build checks
+// every row_token against it and reports MOE_ERR_INVALID_ARG on the status word).
+int launch_gather_rows(const int32_t* row_token, const uint16_t* x, int64_t ldx, int src_rows,
+                       int rows, int H, uint16_t* x_perm, cudaStream_t s);
 
 // Permutation pieces.
 size_t permute_scratch_bytes(int T, int E);

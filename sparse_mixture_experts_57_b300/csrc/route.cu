@@ -509,13 +509,20 @@ __global__ void __launch_bounds__(256)
 
 // x_perm[r, :] = x[row_token[r], :], one warp per row (16-byte vectors).
 __global__ void k_gather_rows(const int32_t* __restrict__ row_token, const uint16_t* __restrict__ x,
-                              long long ldx, int rows, int H, uint16_t* __restrict__ x_perm) {
+                              long long ldx, int rows, int H, uint16_t* __restrict__ x_perm,
+                              int src_rows, int* status) {
   griddep_wait();
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (r >= rows) return;
   const int t = row_token[r];
+  if constexpr (kDebugBuild) {  // the routing kernel wrote row_token: check it in debug builds
+    if (t < 0 || t >= src_rows) {
+      if (lane == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+      return;
+    }
+  }
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(t) * ldx);
   uint4* dst = reinterpret_cast<uint4*>(x_perm + r * H);
 #pragma unroll 4
@@ -618,12 +625,15 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
   return go(k_route_small<8, 1>);
 }
 
-int launch_gather_rows(const int32_t* row_token, const uint16_t* x, int64_t ldx, int rows, int H,
-                       uint16_t* x_perm, cudaStream_t s) {
+int launch_gather_rows(const int32_t* row_token, const uint16_t* x, int64_t ldx, int src_rows,
+                       int rows, int H, uint16_t* x_perm, cudaStream_t s) {
   if (rows <= 0) return MOE_OK;
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
   const long long threads = static_cast<long long>(rows) * 32;
   return launch_pdl(k_gather_rows, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
-                    0, s, row_token, x, static_cast<long long>(ldx), rows, H, x_perm);
+                    0, s, row_token, x, static_cast<long long>(ldx), rows, H, x_perm, src_rows,
+                    status);
 }
 
 }  // namespace moe

@@ -211,6 +211,26 @@ def test_grouped_ffn(moe, T, E, k, H, F, skew):
     _status_ok(moe)
 
 
+@pytest.mark.parametrize("counts,H,F", [
+    # >= 256 rows per group on average: 256-row CTA-pair tiles whose last tile per group holds
+    # 44, 1, 88, 128 or 129 rows (300, 1, 600, 384, 385), or none (512)
+    ([300, 0, 1, 600, 384, 385, 512], 320, 448),
+    ([1500, 700, 300, 129], 2688, 1856),       # Nano widths
+])
+def test_grouped_ffn_pair_partial_tiles(moe, counts, H, F):
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(off[-1])
+    xp = _bf(rows + 1, (rows, H))
+    wu = moe_synth.expert_stack(rows, moe_synth.TAG_UP, E, F, H)
+    wd = moe_synth.expert_stack(rows, moe_synth.TAG_DOWN, E, H, F)
+    y = moe.moe_grouped_ffn(to_dev(xp), to_dev(off), to_dev(wu), to_dev(wd))
+    torch.cuda.synchronize()
+    ref = O.grouped_ffn(xp, off, wu, wd)
+    assert_close(bf16_out(y), ref, "grouped ffn, partial CTA-pair tiles")
+    _status_ok(moe)
+
+
 # --------------------------------------------------------------------- whole layer ----
 
 def _layer_full(moe, w):
