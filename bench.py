@@ -639,6 +639,58 @@ def _oracle_sample(w, inp, toks):
     return O.moe_tokens(x, r["idx"], r["gates"], inp["w_up"], inp["w_down"]), r
 
 
+class _BlasThreads:
+    """Context manager that sets the BLAS thread count of numpy's OpenBLAS for its duration
+    (threadpoolctl when installed, else OpenBLAS's own setter found among the loaded
+    libraries; without either it does nothing)."""
+
+    def __init__(self, n: int):
+        self.n, self.ctx, self.setter, self.prev = n, None, None, None
+
+    @staticmethod
+    def _openblas():
+        import ctypes
+        try:
+            with open("/proc/self/maps") as f:
+                paths = {ln.split()[-1] for ln in f if "openblas" in ln.lower() and "/" in ln}
+        except OSError:
+            return None, None
+        for path in sorted(paths):
+            try:
+                lib = ctypes.CDLL(path)
+            except OSError:
+                continue
+            for pre in ("scipy_", ""):
+                for suf in ("64_", ""):
+                    set_fn = getattr(lib, f"{pre}openblas_set_num_threads{suf}", None)
+                    get_fn = getattr(lib, f"{pre}openblas_get_num_threads{suf}", None)
+                    if set_fn is not None and get_fn is not None:
+                        return set_fn, get_fn
+        return None, None
+
+    def __enter__(self):
+        try:
+            from threadpoolctl import threadpool_limits
+            self.ctx = threadpool_limits(self.n)
+            self.ctx.__enter__()
+            return self
+        except ImportError:
+            pass
+        set_fn, get_fn = self._openblas()
+        if set_fn is not None:
+            self.prev = int(get_fn())
+            set_fn(self.n)
+            self.setter = set_fn
+        return self
+
+    def __exit__(self, *exc):
+        if self.ctx is not None:
+            self.ctx.__exit__(*exc)
+        elif self.setter is not None:
+            self.setter(self.prev)
+        return False
+
+
 class OraclePool:
     """The oracle run on all host cores: one thread per core, each evaluating its own chunk
     of tokens with single-threaded BLAS (numpy releases the GIL in its array kernels)."""
@@ -651,8 +703,7 @@ class OraclePool:
 
     def run(self, chunks):
         """Evaluate the token chunks concurrently; returns ([(toks, y, routing)], wall s)."""
-        from threadpoolctl import threadpool_limits
-        with threadpool_limits(1):
+        with _BlasThreads(1):
             t0 = time.perf_counter()
             res = list(self.ex.map(lambda t: (t, *_oracle_sample(self.w, self.inp, t)), chunks))
             return res, time.perf_counter() - t0
