@@ -281,7 +281,9 @@ __device__ __forceinline__ void topk_token_select(const float* __restrict__ row,
       key[i] = 0u;  // below every valid key (the key of -inf is 0x007fffff)
     }
   }
-  // 1. kth = the k-th largest key
+  // 1. kth = the k-th largest key, found bit by bit from the top. Once exactly k keys are at
+  //    or above the candidate prefix, they are the k largest and the k-th is their minimum:
+  //    the search stops there instead of resolving the remaining low bits.
   uint32_t kth = 0u;
 #pragma unroll 1
   for (int b = 31; b >= 0; --b) {
@@ -289,7 +291,16 @@ __device__ __forceinline__ void topk_token_select(const float* __restrict__ row,
     uint32_t c = 0u;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) c += key[i] >= cand ? 1u : 0u;
-    if (__reduce_add_sync(0xffffffffu, c) >= static_cast<uint32_t>(k)) kth = cand;
+    const uint32_t total = __reduce_add_sync(0xffffffffu, c);
+    if (total == static_cast<uint32_t>(k)) {
+      uint32_t m = 0xffffffffu;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (key[i] >= cand) m = min(m, key[i]);
+      kth = __reduce_min_sync(0xffffffffu, m);
+      break;
+    }
+    if (total > static_cast<uint32_t>(k)) kth = cand;
   }
   uint32_t gt = 0u, eq = 0u, below = 0u;
 #pragma unroll

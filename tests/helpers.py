@@ -165,3 +165,15 @@ def tie_matrix_e4m3(N, K):
             w[r, c] = v if (r + c) % 2 else -v
     w[0, 0] = 448 * s
     return w
+
+
+def sample_tokens(T: int, idx: np.ndarray, same: np.ndarray, n: int, seed: int) -> np.ndarray:
+    """Tokens for sampled full-size parity: the first and last token, n random ones, and for
+    every expert that receives tokens the first token routed to it (so every touched
+    expert's FFN is evaluated), restricted to tokens whose selection equals the oracle's."""
+    rng = np.random.default_rng(seed)
+    idx = np.asarray(idx)
+    firsts = [int(np.nonzero((idx == e).any(axis=1))[0][0]) for e in np.unique(idx)]
+    toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, min(n, T), replace=False),
+                                     firsts]))
+    return toks[same[toks]]

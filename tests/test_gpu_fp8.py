@@ -16,7 +16,8 @@ import pytest
 
 import moe_synth
 from oracle import moe_oracle as O
-from helpers import bf16_out, check_selection, decode_e4m3, tie_matrix_e4m3, to_dev
+from helpers import (bf16_out, check_selection, decode_e4m3, sample_tokens, tie_matrix_e4m3,
+                     to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -137,9 +138,7 @@ def test_layer_fp8_prefill_sampled(moe):
     ref = O.route(inp["x"], inp["w_router"], inp["bias"], w.k)
     same = check_selection(gi, ref, inp["bias"], w.k)
     h_amax = O.fp8_hidden_amax(inp["x"], ref["idx"], inp["w_up"])
-    rng = np.random.default_rng(w.seed + 1)
-    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, 30, replace=False)]))
-    toks = toks[same[toks]]
+    toks = sample_tokens(w.T, ref["idx"], same, 100, w.seed + 1)
     ref_y = O.moe_tokens_fp8(inp["x"], inp["x"][toks], ref["idx"][toks], ref["gates"][toks],
                              inp["w_up"], inp["w_down"], h_amax)
     _rel_checks(got[toks], ref_y, "fp8 prefill sampled tokens")

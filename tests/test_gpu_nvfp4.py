@@ -17,7 +17,7 @@ import pytest
 
 import moe_synth
 from oracle import moe_oracle as O
-from helpers import (REL_FROB_NVFP4, bf16_out, check_selection, decode_codes,
+from helpers import (REL_FROB_NVFP4, bf16_out, check_selection, decode_codes, sample_tokens,
                      decode_e4m3_scale as decode_e4m3, scale_rows, tie_matrix, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -193,9 +193,7 @@ def test_layer_nvfp4_prefill_sampled(moe):
     ref = O.route(inp["x"], inp["w_router"], inp["bias"], w.k)
     same = check_selection(gi, ref, inp["bias"], w.k)
     h_amax = O.nvfp4_hidden_amax(inp["x"], ref["idx"], inp["w_up"])
-    rng = np.random.default_rng(w.seed)
-    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, 30, replace=False)]))
-    toks = toks[same[toks]]
+    toks = sample_tokens(w.T, ref["idx"], same, 100, w.seed)
     ref_y = O.moe_tokens_nvfp4(inp["x"], inp["x"][toks], ref["idx"][toks], ref["gates"][toks],
                                inp["w_up"], inp["w_down"], h_amax=h_amax)
     _rel_checks(got[toks], ref_y, "nvfp4 prefill sampled tokens")

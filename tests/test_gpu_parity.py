@@ -8,7 +8,8 @@ import pytest
 
 import moe_synth
 from oracle import moe_oracle as O
-from helpers import (assert_close, bf16_out, check_selection, gates_by_expert, to_dev)
+from helpers import (assert_close, bf16_out, check_selection, gates_by_expert, sample_tokens,
+                     to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -282,7 +283,7 @@ def test_layer_nano_decode_full(moe):
     _layer_full(moe, moe_synth.WORKLOADS["nano_decode"])
 
 
-def _sampled_layer(moe, w, n_sample=40):
+def _sampled_layer(moe, w, n_sample=200):
     inp = moe_synth.layer_inputs(w)
     dev = {k: to_dev(v) for k, v in inp.items()}
     idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
@@ -297,9 +298,7 @@ def _sampled_layer(moe, w, n_sample=40):
     if same.all():
         p = O.permute(ref["idx"], w.E)
         assert (np.bincount(gi.reshape(-1), minlength=w.E) == p["counts"]).all()
-    rng = np.random.default_rng(w.seed)
-    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n_sample, replace=False)]))
-    toks = toks[same[toks]]
+    toks = sample_tokens(w.T, ref["idx"], same, n_sample, w.seed)
     ref_y = O.moe_tokens(inp["x"][toks], ref["idx"][toks], ref["gates"][toks], inp["w_up"],
                          inp["w_down"])
     assert_close(bf16_out(y)[toks], ref_y, f"{w.name} sampled tokens")
@@ -312,7 +311,7 @@ def test_layer_nano_prefill_sampled(moe):
 
 # ------------------------------------------------------------------------- LatentMoE ----
 
-def _latent_case(moe, w, full=True, n_sample=24):
+def _latent_case(moe, w, full=True, n_sample=96):
     inp = moe_synth.layer_inputs(w)
     dev = {k: to_dev(v) for k, v in inp.items()}
     idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
@@ -329,8 +328,7 @@ def _latent_case(moe, w, full=True, n_sample=24):
     if full:
         toks = np.arange(w.T)
     else:
-        rng = np.random.default_rng(w.seed)
-        toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n_sample, replace=False)]))
+        toks = sample_tokens(w.T, ref["idx"], np.ones(w.T, bool), n_sample, w.seed)
     toks = toks[same[toks]]
     y_lat = O.moe_tokens(x_lat[toks], ref["idx"][toks], ref["gates"][toks], inp["w_up"],
                          inp["w_down"])
