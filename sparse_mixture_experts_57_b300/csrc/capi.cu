@@ -268,10 +268,19 @@ struct Nvfp4Weights {
   const float* gscale;
 };
 
-// NVFP4 expert FFNs. The rows entering the experts are gathered from `src` (row stride ld):
-// token row_token[offsets[e] + r] when row_token is given, else row offsets[e] + r. amax_rows
-// rows of src make up the activation tensor whose amax sets its global scale.
-int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const int32_t* row_token,
+// The routing of the tokens whose rows enter the experts (layer calls): token t's slot j
+// is expert topk_idx[t k + j], permuted row slot_row[t k + j].
+struct TokenSlots {
+  const int32_t* topk_idx;
+  const int32_t* slot_row;
+  int T, k;
+};
+
+// NVFP4 expert FFNs. The rows entering the experts are rows offsets[e] + r of `src` (row
+// stride ld), or, with `slots`, the routed tokens of src: each token is quantised once and
+// written to its k rows. amax_rows rows of src make up the activation tensor whose amax sets
+// its global scale.
+int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const TokenSlots* slots,
               const int32_t* offsets, const Nvfp4Weights& up, const Nvfp4Weights& down, int rows,
               int H, int F, int E, uint16_t* y_perm, const Fp4Ws& w, cudaStream_t s) {
   MOE_CUDA(cudaMemsetAsync(w.amax, 0, 2 * sizeof(uint32_t), s));
@@ -279,8 +288,12 @@ int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const int3
   if (st) return st;
   st = launch_pad_offsets(offsets, E, w.poff, s);
   if (st) return st;
-  st = launch_quant_act(src, ld, amax_rows, row_token, offsets, w.poff, E, H, w.P, w.amax, w.xq,
-                        w.xsf, s);
+  if (slots)
+    st = launch_quant_tokens(src, ld, slots->T, slots->k, slots->topk_idx, slots->slot_row,
+                             offsets, w.poff, E, H, w.P, w.amax, w.xq, w.xsf, s);
+  else
+    st = launch_quant_act(src, ld, amax_rows, nullptr, offsets, w.poff, E, H, w.P, w.amax, w.xq,
+                          w.xsf, s);
   if (st) return st;
   Fp4Gemm g{};
   g.a_codes = w.xq;
@@ -342,16 +355,21 @@ Fp8Ws carve_fp8(Carver& c, int rows, int H, int F) {
   return w;
 }
 
-// FP8 expert FFNs. The rows entering the experts are src rows row_token[r] (or r when
-// row_token is null); amax_rows rows of src make up the activation tensor of the scale.
-int ffn_fp8(const uint16_t* src, long long ld, long long amax_rows, const int32_t* row_token,
+// FP8 expert FFNs. The rows entering the experts are src rows r, or, with `slots`, the
+// routed tokens of src (each quantised once and written to its k permuted rows); amax_rows
+// rows of src make up the activation tensor of the scale.
+int ffn_fp8(const uint16_t* src, long long ld, long long amax_rows, const TokenSlots* slots,
             const int32_t* offsets, const uint8_t* up, const float* up_scale, const uint8_t* down,
             const float* down_scale, int rows, int H, int F, int E, uint16_t* y_perm,
             const Fp8Ws& w, cudaStream_t s) {
   MOE_CUDA(cudaMemsetAsync(w.amax, 0, 2 * sizeof(uint32_t), s));
   int st = launch_amax_bf16(src, amax_rows * ld, 1, w.amax, s);
   if (st) return st;
-  st = launch_quant_fp8(src, ld, row_token, rows, H, 0, w.amax, w.xq, s);
+  if (slots)
+    st = launch_quant_fp8_tokens(src, ld, slots->T, slots->k, slots->slot_row, rows, H, w.amax,
+                                 w.xq, s);
+  else
+    st = launch_quant_fp8(src, ld, nullptr, rows, H, 0, w.amax, w.xq, s);
   if (st) return st;
   GroupedGemm g{};
   g.act = w.xq;
@@ -855,7 +873,8 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
   // routing and dispatch stay in bf16/fp32; the expert FFNs run in NVFP4
   int st = quant_fwd_route(x, w_router, bias, T, H, E, k, f, idx, gates, stream);
   if (st) return st;
-  st = ffn_nvfp4(x, H, T, f.row_token, f.offsets, {up_codes, up_scales, up_gscale},
+  const TokenSlots slots{idx, f.slot_row, T, k};
+  st = ffn_nvfp4(x, H, T, &slots, f.offsets, {up_codes, up_scales, up_gscale},
                  {down_codes, down_scales, down_gscale}, rows, H, F, E, f.y_perm, w, stream);
   if (st) return st;
   return launch_combine(f.y_perm, rows, f.slot_row, gates, T, H, k, y, stream);
@@ -934,8 +953,9 @@ int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bi
   int st = quant_fwd_route(x, w_router, bias, T, H, E, k, f, idx, gates, stream);
   if (st) return st;
   // the tokens are quantised straight from x in expert order (row_token), no bf16 x_perm
-  st = ffn_fp8(x, H, T, f.row_token, f.offsets, up_codes, up_scale, down_codes, down_scale, rows,
-               H, F, E, f.y_perm, w, stream);
+  const TokenSlots slots{idx, f.slot_row, T, k};
+  st = ffn_fp8(x, H, T, &slots, f.offsets, up_codes, up_scale, down_codes, down_scale, rows, H,
+               F, E, f.y_perm, w, stream);
   if (st) return st;
   return launch_combine(f.y_perm, rows, f.slot_row, gates, T, H, k, y, stream);
 }

@@ -72,6 +72,68 @@ __global__ void k_quant_fp8(const uint16_t* __restrict__ src, long long ld,
   }
 }
 
+// Routed tokens, each quantised once and written to every one of its k permuted rows
+// slot_row[t k + j] (E4M3 bytes [rows, K]). A token's codes are the same in all its copies
+// (one scale for the whole token tensor), so this gives the bytes that quantising each
+// gathered row gives, with a sixth of the arithmetic and of the reads at top-6. One warp per
+// (token, 1024-value segment), as k_quant_fp8.
+__global__ void k_quant_fp8_tokens(const uint16_t* __restrict__ src, long long ld, int T, int k,
+                                   const int32_t* __restrict__ slot_row, long long rows, int K,
+                                   const uint32_t* __restrict__ amax, uint8_t* __restrict__ out,
+                                   int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int nvec = K / 8;
+  const int segs = (nvec + kFp8SegVec - 1) / kFp8SegVec;
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= static_cast<long long>(T) * segs) return;  // whole warps
+  const long long t = wid / segs;
+  const int seg = static_cast<int>(wid - t * segs);
+  const float s = __fdiv_rn(__uint_as_float(*amax), kFp8Div);
+  const bool fast = s > 0x1p-100f && s < 0x1p100f;
+  const float y = fast ? __frcp_rn(s) : 0.f;
+  const uint64_t y2 = f32x2_pack(y, y), ns2 = f32x2_pack(-s, -s);
+  const uint4* row = reinterpret_cast<const uint4*>(src + t * ld);
+  uint2 code[kFp8SegVec / 32];
+#pragma unroll
+  for (int m = 0; m < kFp8SegVec / 32; ++m) {
+    const int v = seg * kFp8SegVec + m * 32 + lane;
+    uint32_t o[2] = {0u, 0u};
+    if (v < nvec) {
+      const uint4 a = __ldg(row + v);
+      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+      if (fast) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float lo, hi;
+          div2_markstein_bf16(w[q], y2, ns2, lo, hi);
+          o[q >> 1] |= e4m3x2(lo, hi) << (16 * (q & 1));
+        }
+      } else if (s > 0.f) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
+          o[q >> 1] |= e4m3x2(__fdiv_rn(lo, s), __fdiv_rn(hi, s)) << (16 * (q & 1));
+        }
+      }
+    }
+    code[m] = make_uint2(o[0], o[1]);
+  }
+  for (int j = 0; j < k; ++j) {
+    const long long r = __ldg(slot_row + t * k + j);
+    if (r < 0 || r >= rows) {
+      if (lane == 0 && seg == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+      continue;
+    }
+#pragma unroll
+    for (int m = 0; m < kFp8SegVec / 32; ++m) {
+      const int v = seg * kFp8SegVec + m * 32 + lane;
+      if (v < nvec) *reinterpret_cast<uint2*>(out + r * K + static_cast<long long>(v) * 8) = code[m];
+    }
+  }
+}
+
 __global__ void k_finalize_fp8_scale(float* s, int G) {
   griddep_wait();
   griddep_launch_dependents();
@@ -88,6 +150,17 @@ int launch_quant_fp8(const uint16_t* src, long long ld, const int32_t* row_map, 
   if (n <= 0) return MOE_OK;
   return launch_pdl(k_quant_fp8, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, s,
                     src, ld, row_map, rows, K, rows_per_scale, amax, out);
+}
+
+int launch_quant_fp8_tokens(const uint16_t* src, long long ld, int T, int k,
+                            const int32_t* slot_row, long long rows, int K, const uint32_t* amax,
+                            uint8_t* out, cudaStream_t s) {
+  if (T <= 0) return MOE_OK;
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  const long long n = static_cast<long long>(T) * ((K / 8 + kFp8SegVec - 1) / kFp8SegVec) * 32;
+  return launch_pdl(k_quant_fp8_tokens, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
+                    s, src, ld, T, k, slot_row, rows, K, amax, out, status);
 }
 
 int launch_finalize_fp8_scale(float* s, int G, cudaStream_t stream) {

@@ -216,6 +216,15 @@ int launch_quant_act(const uint16_t* src, long long ld, long long src_rows,
                      cudaStream_t s);
 
 // ------------------------------------------------------------------------------- FP8 ----
+// Routed tokens in the padded layout, each token quantised once (global scale from *amax)
+// and written to its k rows: slot s of token t goes to row poff[e] + slot_row[t k + s] -
+// offsets[e], e = topk_idx[t k + s]; padding rows get zero codes and scales. The same bytes
+// as launch_quant_act in gather mode. Out-of-range maps are skipped and reported.
+int launch_quant_tokens(const uint16_t* src, long long ld, int T, int k, const int32_t* topk_idx,
+                        const int32_t* slot_row, const int32_t* offsets, const int32_t* poff,
+                        int E, int K, int P_max, const uint32_t* amax, uint8_t* codes,
+                        uint8_t* sf, cudaStream_t s);
+
 // Per-tensor E4M3: s = amax / 448, q = E4M3(v / s). Codes are one byte per element.
 constexpr float kFp8Div = 448.0f;
 // Quantise rows of src (bf16, row stride ld) into out [rows, K] E4M3 bytes. Row r reads src
@@ -224,6 +233,11 @@ constexpr float kFp8Div = 448.0f;
 int launch_quant_fp8(const uint16_t* src, long long ld, const int32_t* row_map, long long rows,
                      int K, long long rows_per_scale, const uint32_t* amax, uint8_t* out,
                      cudaStream_t s);
+// Routed tokens quantised once each and written to their k permuted rows slot_row[t k + j]
+// of out [rows, K]; the same bytes as launch_quant_fp8 with row_map = row_token.
+int launch_quant_fp8_tokens(const uint16_t* src, long long ld, int T, int k,
+                            const int32_t* slot_row, long long rows, int K, const uint32_t* amax,
+                            uint8_t* out, cudaStream_t s);
 // s[i] = amax[i] / 448 in place.
 int launch_finalize_fp8_scale(float* s, int G, cudaStream_t stream);
 

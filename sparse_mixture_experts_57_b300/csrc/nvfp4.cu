@@ -368,6 +368,94 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
   dst[1] = out[1];
 }
 
+// Routed tokens, each quantised once and written to every one of its k rows of the padded
+// expert order: slot j of token t goes to row poff[e] + (slot_row[t k + j] - offsets[e]) with
+// e = topk_idx[t k + j]. A token's codes and block scales are the same in all its copies (the
+// global scale is that of the whole token tensor), so this gives the bytes that quantising
+// each gathered row (k_quant_act) gives, with a sixth of the arithmetic and of the reads at
+// top-6. One thread per (token, 64-element K step); a warp loads its 32 steps cooperatively
+// as k_quant_act does. The padding rows of each segment are written by k_zero_padding_rows.
+__global__ void __launch_bounds__(kQuantThreads, 4)
+    k_quant_tokens(const uint16_t* __restrict__ src, long long ld, int T, int k,
+                   const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_row,
+                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ poff, int E,
+                   int K, int P_max, const uint32_t* __restrict__ amax,
+                   uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ uint4 s_dyn[];  // [8 warps][256 vectors]
+  const int lane = threadIdx.x & 31;
+  uint4* stage = s_dyn + (threadIdx.x >> 5) * 256;
+  const int KS = K / 64;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long t = i / KS;
+  const int j = static_cast<int>(i - t * KS);
+  const bool valid = t < T;
+  const long long srow = valid ? t : -1;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int owner = 4 * it + (lane >> 3);  // the thread whose step these 8 lanes load
+    const long long so = __shfl_sync(0xffffffffu, srow, owner);
+    const int jo = __shfl_sync(0xffffffffu, j, owner);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (so >= 0)
+      v = __ldg(reinterpret_cast<const uint4*>(src + so * ld + jo * 64 + (lane & 7) * 8));
+    const int c = 32 * it + lane;  // vector c & 7 of thread c >> 3
+    stage[(c & ~7) | ((c & 7) ^ ((c >> 3) & 7))] = v;
+  }
+  __syncwarp();
+  if (!valid) return;
+  uint4 out[2];
+  const uint4* mine = stage + 8 * lane;
+  const int sw = lane & 7;
+  const uint32_t word = quant64_from([mine, sw](int m) { return mine[m ^ sw]; },
+                                     global_scale(amax), out);
+  for (int s = 0; s < k; ++s) {
+    const int e = __ldg(topk_idx + t * k + s);
+    const int r = __ldg(slot_row + t * k + s);
+    bool ok = e >= 0 && e < E;
+    long long p = -1;
+    if (ok) {
+      const int o0 = __ldg(offsets + e), o1 = __ldg(offsets + e + 1);
+      ok = r >= o0 && r < o1;
+      if (ok) p = static_cast<long long>(__ldg(poff + e)) + (r - o0);
+      ok = ok && p < P_max;
+    }
+    if (!ok) {
+      if (j == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+      continue;
+    }
+    *sf_word(sf, p, j, KS) = word;
+    uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + j * 32);
+    dst[0] = out[0];
+    dst[1] = out[1];
+  }
+}
+
+// The padding rows of every expert segment (rows past the expert's count up to the next
+// 128-row boundary): zero codes and zero block scales. One block per expert.
+__global__ void k_zero_padding_rows(const int32_t* __restrict__ offsets,
+                                    const int32_t* __restrict__ poff, int E, int K, int P_max,
+                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int e = blockIdx.x;
+  if (e >= E) return;
+  const int KS = K / 64;
+  const long long p0 = static_cast<long long>(__ldg(poff + e)) +
+                       (__ldg(offsets + e + 1) - __ldg(offsets + e));
+  const long long p1 = min(static_cast<long long>(__ldg(poff + e + 1)), static_cast<long long>(P_max));
+  const long long n = (p1 - p0) * KS;
+  for (long long q = threadIdx.x; q < n; q += blockDim.x) {
+    const long long p = p0 + q / KS;
+    const int j = static_cast<int>(q % KS);
+    *sf_word(sf, p, j, KS) = 0u;
+    uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + j * 32);
+    dst[0] = make_uint4(0u, 0u, 0u, 0u);
+    dst[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 }  // namespace
 
 int launch_amax_bf16(const uint16_t* src, long long elems_per_matrix, int G, uint32_t* amax,
@@ -421,6 +509,24 @@ int launch_quant_act(const uint16_t* src, long long ld, long long src_rows,
   return launch_pdl(k_quant_act, dim3(static_cast<unsigned>((n + kQuantThreads - 1) / kQuantThreads)),
                     dim3(kQuantThreads), smem, s, src, ld, src_rows,
                     row_token, offsets, poff, E, K, P_max, amax, codes, sf, status);
+}
+
+int launch_quant_tokens(const uint16_t* src, long long ld, int T, int k, const int32_t* topk_idx,
+                        const int32_t* slot_row, const int32_t* offsets, const int32_t* poff,
+                        int E, int K, int P_max, const uint32_t* amax, uint8_t* codes,
+                        uint8_t* sf, cudaStream_t s) {
+  if (T <= 0) return MOE_OK;
+  int* status = status_word();
+  if (!status) return MOE_ERR_CUDA;
+  const long long n = static_cast<long long>(T) * (K / 64);
+  const size_t smem = (kQuantThreads / 32) * 256 * sizeof(uint4);
+  int st = launch_pdl(k_quant_tokens,
+                      dim3(static_cast<unsigned>((n + kQuantThreads - 1) / kQuantThreads)),
+                      dim3(kQuantThreads), smem, s, src, ld, T, k, topk_idx, slot_row, offsets,
+                      poff, E, K, P_max, amax, codes, sf, status);
+  if (st) return st;
+  return launch_pdl(k_zero_padding_rows, dim3(E), dim3(256), 0, s, offsets, poff, E, K, P_max,
+                    codes, sf);
 }
 
 }  // namespace moe
