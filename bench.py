@@ -15,7 +15,8 @@ the 64-token decode layer. The NVFP4 prefill workload quantises the expert weigh
 runs moe_forward_nvfp4 (activation quantisation included in every step); the *_fp8
 workloads do the same with per-tensor E4M3 experts (moe_forward_fp8). Inputs and
 weights are resident in HBM before the timed region starts. L2 is
-flushed (a 512 MiB write) before every timed step. Each step is timed with CUDA events on
+flushed before every timed step: a 512 MiB write, then a 256 MiB read, so that the write's
+dirty lines are written back before the step starts rather than inside it. Each step is timed with CUDA events on
 the launching stream; the grouped expert FFN, the dominant kernel, is timed the same way.
 
 "e2e" is the same layer through the C ABI with the input coming from pinned host memory
@@ -62,6 +63,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 FP4_OVER_BF16 = 13.5 / 2.25
 FP8_OVER_BF16 = 4.5 / 2.25
 L2_FLUSH_BYTES = 512 << 20
+L2_EVICT_BYTES = 256 << 20
 
 
 def load_peaks():
@@ -126,7 +128,8 @@ def layer_algorithmic(w: moe_synth.Workload, counts: np.ndarray) -> dict:
             "ffn_bytes_per_launch": ffn_bytes_per_launch}
 
 
-def kernels_per_step(w: moe_synth.Workload, gathered: bool = False) -> int:
+def kernels_per_step(w: moe_synth.Workload, gathered: bool = False,
+                     fused_combine: bool = False) -> int:
     """Library kernels one timed step launches (memsets excluded), mirroring the C library's
     choices: the fused small-batch routing kernel (T <= 256, E <= 256, routing width <= 6144)
     or router logits + top-k + permutation (one small-batch block, or mark/count/scan)."""
@@ -142,6 +145,8 @@ def kernels_per_step(w: moe_synth.Workload, gathered: bool = False) -> int:
     route = 2 if fused else (2 + perm + 1)     # + the row copy
     if w.latent:  # projection in, routing in the latent space, FFN, combine, projection out
         return 1 + route + 2 + 1 + 1
+    if fused_combine:  # zero the fixed-point sums, FFN (combine in the epilogue), convert
+        return route + 1 + 2 + 1
     return route + 2 + 1
 
 
@@ -246,6 +251,13 @@ def run_ours(args, w: moe_synth.Workload):
     ws_ffn = torch.empty(L.moe_grouped_ffn_workspace_size(rows, D, F, E), dtype=torch.uint8,
                          device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    evict = torch.ones(L2_EVICT_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # the write leaves up to L2's size of dirty lines; the read replaces them with clean
+        # lines of another buffer, so their write-back to HBM happens here, untimed
+        flush.zero_()
+        evict.sum()
     if w.latent:
         ws_lat = torch.empty(L.latent_moe_workspace_size(T, H, w.latent, E, k, F,
                                                          int(w.router_on_latent)),
@@ -264,9 +276,17 @@ def run_ours(args, w: moe_synth.Workload):
         del d["w_up"], d["w_down"]
         ws_fp4 = torch.empty(L.moe_forward_nvfp4_workspace_size(T, H, E, k, F),
                              dtype=torch.uint8, device=dev)
+    elif args.fused_combine:
+        ws_fwd = torch.empty(L.moe_forward_fused_combine_workspace_size(T, H, E, k, F),
+                             dtype=torch.uint8, device=dev)
     else:
         ws_fwd = torch.empty(L.moe_forward_workspace_size(T, H, E, k, F), dtype=torch.uint8,
                              device=dev)
+    # the whole-layer entry point of the standard bf16 layer
+    fwd_name = ("moe_forward_gathered" if args.gathered else
+                "moe_forward_fused_combine" if args.fused_combine else "moe_forward")
+    fwd_fn = getattr(L, fwd_name)
+    whole_call = args.gathered or args.fused_combine
 
     def chk(code, what):
         if code != 0:
@@ -287,13 +307,14 @@ def run_ours(args, w: moe_synth.Workload):
                               P(ws_fp8), ws_fp8.numel(), sp), "moe_forward_fp8")
 
     def step(e_ffn0=None, e_ffn1=None):
-        if args.gathered:
+        if whole_call:
             # the whole layer through moe_forward_gathered (token rows gathered by the GEMM)
+            # or moe_forward_fused_combine (combine in the down-projection's epilogue)
             if e_ffn0 is not None:
                 e_ffn0.record(stream)
-            chk(L.moe_forward_gathered(P(d["x"]), P(d["w_router"]), P(d["bias"]), P(d["w_up"]),
-                                       P(d["w_down"]), T, H, E, k, F, P(y), P(idx), P(gates),
-                                       P(ws_fwd), ws_fwd.numel(), sp), "moe_forward_gathered")
+            chk(fwd_fn(P(d["x"]), P(d["w_router"]), P(d["bias"]), P(d["w_up"]), P(d["w_down"]),
+                       T, H, E, k, F, P(y), P(idx), P(gates), P(ws_fwd), ws_fwd.numel(), sp),
+                fwd_name)
             if e_ffn1 is not None:
                 e_ffn1.record(stream)
             return
@@ -337,10 +358,10 @@ def run_ours(args, w: moe_synth.Workload):
     # kernels per step: route 2, permutation 2-4, FFN 2, combine 1 (bf16); the latent layer
     # adds its two projections; the NVFP4 layer replaces the gather by amax, padding,
     # two quantisations and the two block-scaled GEMMs
-    launches_per_step = kernels_per_step(w, args.gathered)
+    launches_per_step = kernels_per_step(w, args.gathered, args.fused_combine)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     assert moe.get_device_status() == 0
@@ -367,7 +388,7 @@ def run_ours(args, w: moe_synth.Workload):
     clocks.mark("t0")
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.zero_()
+        flush_l2()
         s_ev[i].record(stream)
         step(f0[i], f1[i])
         e_ev[i].record(stream)
@@ -431,9 +452,8 @@ def run_ours(args, w: moe_synth.Workload):
                              T, H, w.latent, E, k, F, yp, None, None, P(ws_lat),
                              ws_lat.numel(), sp), "latent_moe")
         else:
-            chk(L.moe_forward(xp, P(d["w_router"]), P(d["bias"]), P(d["w_up"]),
-                              P(d["w_down"]), T, H, E, k, F, yp, None, None, P(ws_fwd),
-                              ws_fwd.numel(), sp), "moe_forward")
+            chk(fwd_fn(xp, P(d["w_router"]), P(d["bias"]), P(d["w_up"]), P(d["w_down"]), T, H,
+                       E, k, F, yp, None, None, P(ws_fwd), ws_fwd.numel(), sp), fwd_name)
         ev_comp[b].record(stream)
         with torch.cuda.stream(d2h):
             d2h.wait_event(ev_comp[b])
@@ -463,7 +483,7 @@ def run_ours(args, w: moe_synth.Workload):
 
     peaks, peak_src = load_peaks()
     alg = layer_algorithmic(w, counts_from_routing(routing, E))
-    launches = 1 if (w.latent or w.nvfp4 or w.fp8 or args.gathered) else 2  # calls bracketed
+    launches = 1 if (w.latent or w.nvfp4 or w.fp8 or whole_call) else 2  # calls bracketed
     p_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
     p_fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
     t_fp8_flops = alg["flops_experts"] / p_fp8 / 1e12
@@ -485,7 +505,7 @@ def run_ours(args, w: moe_synth.Workload):
         achieved = alg["flops_experts"] / (ffn / 1e3) / 1e12
         peak = p_fp4
         unit = "TFLOP/s"
-    elif w.latent or args.gathered:
+    elif w.latent or whole_call:
         # the whole layer call is bracketed; its tcgen05 GEMMs dominate
         bound = "tensor"
         dom_units = alg["flops"]
@@ -509,7 +529,7 @@ def run_ours(args, w: moe_synth.Workload):
     else:
         t_flops = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
     roof_ms = max(t_flops, alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
-    traffic = None if args.gathered else read_traffic(w.name, alg["touched"])
+    traffic = None if whole_call else read_traffic(w.name, alg["touched"])
     out = {
         "metric": METRIC,
         "value": job_tokens_per_s(world, T, ms),
@@ -525,7 +545,9 @@ def run_ours(args, w: moe_synth.Workload):
                   "e4m3 experts (per-tensor scales), bf16 router" if w.fp8 else "bf16"),
         "data": "synthetic (seeded, random-init weights of the named shape)",
         "config": {"workload": w.name, "T": T, "H": H, "E": E, "k": k, "F": F,
-                   "latent": w.latent or None, "bias": w.bias, "l2": "flushed before every step",
+                   "latent": w.latent or None, "bias": w.bias,
+                   "l2": "flushed before every step (512 MiB write, then 256 MiB read)",
+                   "layer_call": fwd_name if whole_call else None,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
@@ -536,6 +558,8 @@ def run_ours(args, w: moe_synth.Workload):
                      "kernel": ("whole latent layer (tcgen05 GEMMs dominate)" if w.latent
                                 else "whole layer, token rows gathered by the up-projection"
                                 if args.gathered
+                                else "whole layer, combine fused into the down-projection"
+                                if args.fused_combine
                                 else "whole NVFP4 layer (block-scaled tcgen05 GEMMs dominate)"
                                 if w.nvfp4
                                 else "whole FP8 layer (E4M3 tcgen05 grouped GEMMs dominate)"
@@ -838,11 +862,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--gathered", action="store_true",
                     help="standard layer: time moe_forward_gathered (whole-layer bracket)")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="standard layer: time moe_forward_fused_combine (whole-layer bracket)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = moe_synth.WORKLOADS[args.workload]
-    if args.gathered and (w.latent or w.nvfp4 or w.fp8):
-        ap.error("--gathered applies to the bf16 standard layer")
+    if (args.gathered or args.fused_combine) and (w.latent or w.nvfp4 or w.fp8):
+        ap.error("--gathered and --fused-combine apply to the bf16 standard layer")
+    if args.gathered and args.fused_combine:
+        ap.error("--gathered and --fused-combine select different entry points")
     if args.T is not None or args.E is not None:
         import dataclasses
         T = args.T if args.T is not None else w.T

@@ -194,6 +194,34 @@ int moe_forward_gathered(const uint16_t* x, const uint16_t* w_router, const floa
                          int F, uint16_t* y, int32_t* topk_idx_out, float* gates_out,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_forward_fused_combine: moe_forward with the combine (shd-paper.top summary 技术框架,
+ * the weighted combination of the chosen experts' outputs) fused into the down-projection's
+ * epilogue. Each routed row's output, times its gate, is rounded once to a multiple of 2^-32
+ * and added with 64-bit integer atomics to its token's accumulator [T,H] in the workspace;
+ * integer addition does not depend on the order in which the tiles finish, so the result
+ * is the same on every run. A last pass writes y = bf16(sum * 2^-32). y_perm is never
+ * written. Differences from moe_forward: the expert outputs are not rounded to bf16 before
+ * the combine (so y can differ from moe_forward's in the last bf16 place), and a term with
+ * |gate * output| >= 2^26 (or NaN) is not added and sets MOE_ERR_UNSUPPORTED on the device
+ * status word. Same arguments as moe_forward; workspace from
+ * moe_forward_fused_combine_workspace_size() (moe_forward's minus y_perm, plus 8*T*H bytes). */
+size_t moe_forward_fused_combine_workspace_size(int T, int H, int E, int k, int F);
+/* moe_fixed_to_bf16: the last pass of moe_forward_fused_combine on its own, for testing:
+ * out[i] = the bf16 nearest to q[i] * 2^-32 (ties to even; bit patterns as uint16), rounded
+ * once from the integer. on_device = 0: host pointers, computed on the calling thread (no
+ * CUDA call). on_device = 1: device pointers, the library's conversion kernel on `stream`
+ * (n a multiple of 8, both pointers 16-byte aligned, else MOE_ERR_UNSUPPORTED). The pages
+ * have no counterpart: the fixed-point sum is this library's way of making the fused
+ * combine independent of the order of its additions. MOE_ERR_INVALID_ARG for n < 0 or a
+ * NULL pointer with n > 0. */
+int moe_fixed_to_bf16(const int64_t* q, long long n, uint16_t* out, int on_device,
+                      cudaStream_t stream);
+int moe_forward_fused_combine(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                              const uint16_t* w_up, const uint16_t* w_down, int T, int H, int E,
+                              int k, int F, uint16_t* y, int32_t* topk_idx_out,
+                              float* gates_out, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * latent_moe: the LatentMoE layer (NVIDIA Nemotron 3 notes §2.2, Fig. 3b).
  *   x_lat = x . w_in^T                      (H -> L, bf16 projection)

@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     moe_forward_nvfp4_workspace_size,
     moe_forward_shared,
     moe_forward_workspace_size,
+    moe_forward_fused_combine_workspace_size,
     moe_grouped_ffn,
     moe_grouped_ffn_fp8,
     moe_grouped_ffn_nvfp4,

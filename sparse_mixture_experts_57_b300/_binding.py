@@ -53,6 +53,10 @@ SIGNATURES = {
                                   _VP, _SZ, _VP]),
     "moe_forward": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ,
                          _VP]),
+    "moe_forward_fused_combine_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_fixed_to_bf16": (_I, [_VP, ctypes.c_longlong, _VP, _I, _VP]),
+    "moe_forward_fused_combine": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP,
+                                       _VP, _VP, _SZ, _VP]),
     "moe_nvfp4_codes_bytes": (_SZ, [_I, _I, _I]),
     "moe_nvfp4_scales_bytes": (_SZ, [_I, _I, _I]),
     "moe_quantize_nvfp4_weights": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _VP]),
@@ -266,9 +270,18 @@ def moe_forward_workspace_size(T, H, E, k, F) -> int:
     return int(lib().moe_forward_workspace_size(T, H, E, k, F))
 
 
+def moe_forward_fused_combine_workspace_size(T, H, E, k, F) -> int:
+    return int(lib().moe_forward_fused_combine_workspace_size(T, H, E, k, F))
+
+
 def moe_forward(x, w_router, bias, w_up, w_down, k: int, *, out=None, topk_idx_out=None,
-                gates_out=None, workspace=None, stream=None, gathered: bool = False):
-    """gathered=True calls moe_forward_gathered (token rows gathered by the up-projection)."""
+                gates_out=None, workspace=None, stream=None, gathered: bool = False,
+                fused_combine: bool = False):
+    """gathered=True calls moe_forward_gathered (token rows gathered by the up-projection);
+    fused_combine=True calls moe_forward_fused_combine (combine in the down-projection's
+    epilogue, fixed-point sums)."""
+    if gathered and fused_combine:
+        raise ValueError("gathered and fused_combine select different entry points")
     bf = torch.bfloat16
     _cuda_tensor(x, bf, "x", 2)
     _cuda_tensor(w_router, bf, "w_router", 2)
@@ -279,8 +292,13 @@ def moe_forward(x, w_router, bias, w_up, w_down, k: int, *, out=None, topk_idx_o
     E, F, _ = w_up.shape
     y = out if out is not None else torch.empty((T, H), dtype=bf, device=x.device)
     L = lib()
-    ws = _workspace(L.moe_forward_workspace_size(T, H, E, k, F), x.device, workspace)
-    fn = L.moe_forward_gathered if gathered else L.moe_forward
+    if fused_combine:
+        ws = _workspace(L.moe_forward_fused_combine_workspace_size(T, H, E, k, F), x.device,
+                        workspace)
+        fn = L.moe_forward_fused_combine
+    else:
+        ws = _workspace(L.moe_forward_workspace_size(T, H, E, k, F), x.device, workspace)
+        fn = L.moe_forward_gathered if gathered else L.moe_forward
     _check(fn(_ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_up), _ptr(w_down), T, H, E,
               k, F, _ptr(y), _ptr(topk_idx_out), _ptr(gates_out), _ptr(ws),
               ws.numel(), _stream(stream)), "moe_forward")

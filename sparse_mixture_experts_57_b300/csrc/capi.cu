@@ -72,10 +72,12 @@ struct LayerWs {
   void* perm_scratch;
   uint16_t* x_perm;
   uint16_t* h;
-  uint16_t* y_perm;
+  uint16_t* y_perm;  // [rows, D] expert outputs, or null with the fused combine
+  int64_t* acc;      // fused combine: [T, D] fixed-point sums, else null
 };
 
-LayerWs carve_layer(Carver& c, int T, int D, int E, int k, int F) {
+// fused_combine: the down-projection adds into acc (fixed.cuh) instead of writing y_perm.
+LayerWs carve_layer(Carver& c, int T, int D, int E, int k, int F, bool fused_combine = false) {
   const size_t rows = static_cast<size_t>(T) * k;
   LayerWs w;
   w.logits = c.take<float>(static_cast<size_t>(T) * E);
@@ -90,7 +92,8 @@ LayerWs carve_layer(Carver& c, int T, int D, int E, int k, int F) {
   w.perm_scratch = c.take<char>(permute_scratch_bytes(T, E));
   w.x_perm = c.take<uint16_t>(rows * D);
   w.h = c.take<uint16_t>(rows * F);
-  w.y_perm = c.take<uint16_t>(rows * D);
+  w.y_perm = fused_combine ? nullptr : c.take<uint16_t>(rows * D);
+  w.acc = fused_combine ? c.take<int64_t>(static_cast<size_t>(T) * D) : nullptr;
   return w;
 }
 
@@ -122,10 +125,20 @@ int router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_router, int 
 
 // Expert FFNs. The up-projection reads x_perm [rows, D], or, when row_token is given, gathers
 // the rows from x_src (src_rows rows, row stride ld_src) by token: x_perm is never written.
+// With `fc`, the down-projection's epilogue adds each row's gated output into its token's
+// fixed-point sum fc->acc (EPI_COMBINE_I64) and y_perm is not written.
+struct FusedCombine {
+  int64_t* acc;
+  const int32_t* row_token;
+  const int32_t* slot_row;
+  const float* gates;
+  int T, k;
+};
+
 int ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_up,
         const uint16_t* w_down, int rows, int D, int F, int E, uint16_t* h, uint16_t* y_perm,
         cudaStream_t s, const int32_t* row_token = nullptr, const uint16_t* x_src = nullptr,
-        int64_t ld_src = 0, int src_rows = 0) {
+        int64_t ld_src = 0, int src_rows = 0, const FusedCombine* fc = nullptr) {
   GroupedGemm up{};
   up.act = row_token ? x_src : x_perm;
   up.act_ld = row_token ? ld_src : D;
@@ -154,6 +167,15 @@ int ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_up,
   dn.out = y_perm;
   dn.ldo = D;
   dn.epi = EPI_BF16;
+  if (fc) {
+    dn.out = fc->acc;
+    dn.epi = EPI_COMBINE_I64;
+    dn.comb_token = fc->row_token;
+    dn.comb_slot_row = fc->slot_row;
+    dn.comb_gates = fc->gates;
+    dn.comb_k = fc->k;
+    dn.comb_T = fc->T;
+  }
   return launch_grouped_gemm(dn, s);
 }
 
@@ -188,6 +210,17 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
     st = launch_permute(idx, x, ldx, T, D, E, k, w.counts, w.offsets, w.row_token, w.slot_row,
                         gather ? nullptr : w.x_perm, w.perm_scratch, s);
     if (st) return st;
+  }
+  if (w.acc) {  // combine fused into the down-projection (carve_layer with fused_combine)
+    st = launch_init_fixed(w.acc, T, D, addend, s);
+    if (st) return st;
+    const FusedCombine fc{w.acc, w.row_token, w.slot_row, gates, T, k};
+    st = gather ? ffn(nullptr, w.offsets, w_up, w_down, rows, D, F, E, w.h, nullptr, s,
+                      w.row_token, x, ldx, T, &fc)
+                : ffn(w.x_perm, w.offsets, w_up, w_down, rows, D, F, E, w.h, nullptr, s,
+                      nullptr, nullptr, 0, 0, &fc);
+    if (st) return st;
+    return launch_combine_fixed(w.acc, static_cast<long long>(T) * D, y, s);
   }
   if (gather)
     st = ffn(nullptr, w.offsets, w_up, w_down, rows, D, F, E, w.h, w.y_perm, s, w.row_token, x,
@@ -695,6 +728,32 @@ int moe_forward_gathered(const uint16_t* x, const uint16_t* w_router, const floa
   const WsGuard guard(c, stream);
   return layer(x, H, x, H, H, 1, w_router, bias, w_up, w_down, T, H, E, k, F, y, topk_idx_out,
                gates_out, w, stream, nullptr, true);
+}
+
+size_t moe_forward_fused_combine_workspace_size(int T, int H, int E, int k, int F) {
+  if (!dims_ok(T, H, E, k) || F <= 0) return 0;
+  Carver c(nullptr, 0);
+  carve_layer(c, T, H, E, k, F, true);
+  return c.used + 256;
+}
+
+int moe_forward_fused_combine(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                              const uint16_t* w_up, const uint16_t* w_down, int T, int H, int E,
+                              int k, int F, uint16_t* y, int32_t* topk_idx_out,
+                              float* gates_out, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+  if (!dims_ok(T, H, E, k) || F <= 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !bias || !w_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (H % 64 || F % 64 || !aligned16(x) || !aligned16(w_router) || !aligned16(w_up) ||
+      !aligned16(w_down) || !aligned16(y))
+    return MOE_ERR_UNSUPPORTED;
+  Carver c(workspace, workspace_bytes);
+  const LayerWs w = carve_layer(c, T, H, E, k, F, true);
+  if (!c.ok()) return MOE_ERR_WORKSPACE;
+  const WsGuard guard(c, stream);
+  return layer(x, H, x, H, H, 1, w_router, bias, w_up, w_down, T, H, E, k, F, y, topk_idx_out,
+               gates_out, w, stream);
 }
 
 size_t latent_moe_workspace_size(int T, int H, int L, int Ep, int kp, int F,

@@ -7,6 +7,7 @@
 // Deterministic (no atomics), fp32 accumulation, 16-byte loads and stores.
 #include <cuda_bf16.h>
 
+#include "fixed.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -62,7 +63,68 @@ __global__ void k_combine(const uint16_t* __restrict__ y_perm, int rows,
       make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
 }
 
+// The fused combine's accumulator starts at the addend in fixed point (exact for bf16 values
+// of magnitude 2^-24 and above), or at zero: one thread per 8 columns.
+__global__ void k_init_fixed(longlong2* __restrict__ acc, long long n8, int H,
+                             const uint16_t* __restrict__ addend) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += stride) {
+    longlong2* dst = acc + i * 4;
+    if (!addend) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) dst[u] = make_longlong2(0, 0);
+      continue;
+    }
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(addend) + i);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      dst[u] = make_longlong2(__float2ll_rn(__uint_as_float(w[u] << 16) * kFixedOne),
+                              __float2ll_rn(__uint_as_float(w[u] & 0xffff0000u) * kFixedOne));
+  }
+}
+
+// y[t, c] = bf16(acc[t, c] * 2^-32), one thread per 8 columns.
+__global__ void k_combine_fixed(const longlong2* __restrict__ acc, long long n8,
+                                uint4* __restrict__ y) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  uint32_t o[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const longlong2 q = __ldg(acc + i * 4 + u);
+    o[u] = static_cast<uint32_t>(fixed_to_bf16(q.x)) |
+           (static_cast<uint32_t>(fixed_to_bf16(q.y)) << 16);
+  }
+  y[i] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 }  // namespace
+
+int launch_init_fixed(int64_t* acc, int T, int H, const uint16_t* addend, cudaStream_t s) {
+  if (T <= 0) return MOE_OK;
+  const long long n8 = static_cast<long long>(T) * (H / 8);
+  const int threads = 256;
+  long long blocks = (n8 + threads - 1) / threads;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(k_init_fixed, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
+                    reinterpret_cast<longlong2*>(acc), n8, H, addend);
+}
+
+int launch_combine_fixed(const int64_t* acc, long long n, uint16_t* y, cudaStream_t s) {
+  if (n <= 0) return MOE_OK;
+  const int threads = 256;
+  const long long n8 = n / 8;
+  return launch_pdl(k_combine_fixed, dim3(static_cast<unsigned>((n8 + threads - 1) / threads)),
+                    dim3(threads), 0, s, reinterpret_cast<const longlong2*>(acc), n8,
+                    reinterpret_cast<uint4*>(y));
+}
 
 int launch_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row, const float* gates,
                    int T, int H, int k, uint16_t* y, cudaStream_t s, const uint16_t* addend) {
@@ -77,3 +139,14 @@ int launch_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row, co
 }
 
 }  // namespace moe
+
+extern "C" int moe_fixed_to_bf16(const int64_t* q, long long n, uint16_t* out, int on_device,
+                                 cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!q || !out))) return MOE_ERR_INVALID_ARG;
+  if (!on_device) {
+    for (long long i = 0; i < n; ++i) out[i] = moe::fixed_to_bf16(q[i]);
+    return MOE_OK;
+  }
+  if (n % 8 || !moe::aligned16(q) || !moe::aligned16(out)) return MOE_ERR_UNSUPPORTED;
+  return moe::launch_combine_fixed(q, n, out, stream);
+}

@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "fixed.cuh"
 #include "tc.cuh"
 
 namespace moe {
@@ -62,6 +63,10 @@ struct KArgs {
   const uint32_t* a_amax;  // E4M3 kernels: activation amax (fp32 bits)
   const float* w_scale;    // E4M3 kernels: per-group weight scale
   uint32_t* out_amax;      // max of the stored (bf16) squared-ReLU outputs, or null
+  const int32_t* comb_token;     // EPI_COMBINE_I64: token of each routed row,
+  const int32_t* comb_slot_row;  // the permuted rows of each token's k slots,
+  const float* comb_gates;       // and their gates
+  int comb_k, comb_T;
 };
 
 template <int BN>
@@ -161,6 +166,14 @@ __device__ __forceinline__ void store_row16(const KArgs& a, long long row, int c
     z[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     z[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
   }
+}
+
+// EPI_COMBINE_I64, rows-as-M: 16 consecutive columns of one row added to its token's sum.
+__device__ __forceinline__ void combine_row16(const KArgs& a, int t, float g, int col,
+                                              const float* v) {
+  unsigned long long* p = static_cast<unsigned long long*>(a.out) + static_cast<long long>(t) * a.ldo + col;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) fixed_add(p + i, g * v[i], a.status);
 }
 
 // One output element (weights-as-M epilogue: lanes hold consecutive features of a row).
@@ -521,6 +534,11 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
       if constexpr (F8) scale = __fdiv_rn(__uint_as_float(*a.a_amax), kFp8Div) * a.w_scale[e];
       if (!SWAP) {
         const int ncols = min(BN, a.N - col0);
+        int ctok = -1;  // EPI_COMBINE_I64: this row's token and gate
+        float cgate = 0.f;
+        if (a.epi == EPI_COMBINE_I64 && m < valid_rows)
+          fixed_row_gate(a.comb_token, a.comb_slot_row, a.comb_gates, a.comb_k, a.comb_T,
+                         row0 + m, a.status, ctok, cgate);
         for (int n0 = 0; n0 < ncols; n0 += 16) {
           uint32_t r[16];
           tmem_ld16(tb + n0, r);
@@ -536,7 +554,11 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
                 vmax = fmaxf(vmax, t * t);
               }
             }
-            store_row16(a, row0 + m, col0 + n0, v);
+            if (a.epi == EPI_COMBINE_I64) {
+              if (ctok >= 0) combine_row16(a, ctok, cgate, col0 + n0, v);
+            } else {
+              store_row16(a, row0 + m, col0 + n0, v);
+            }
           }
         }
       } else {
@@ -545,6 +567,24 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
           uint32_t r[16];
           tmem_ld16(tb + n0, r);
           tmem_ld_wait();
+          if (a.epi == EPI_COMBINE_I64) {
+            // lanes 0..15 look up rows n0..n0+15; each row's token and gate are then
+            // broadcast, and the warp adds 32 consecutive features of that token's sum
+            int ctok = -1;
+            float cgate = 0.f;
+            if (lane < 16 && n0 + lane < valid_rows)
+              fixed_row_gate(a.comb_token, a.comb_slot_row, a.comb_gates, a.comb_k, a.comb_T,
+                             row0 + n0 + lane, a.status, ctok, cgate);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int t = __shfl_sync(0xffffffffu, ctok, i);
+              const float g = __shfl_sync(0xffffffffu, cgate, i);
+              if (f < a.N && t >= 0)
+                fixed_add(static_cast<unsigned long long*>(a.out) + static_cast<long long>(t) * a.ldo + f,
+                          g * (__uint_as_float(r[i]) * scale), a.status);
+            }
+            continue;
+          }
           if (f < a.N) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -719,6 +759,10 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   if (g.fp8 && (g.k_wrap || g.precise || !g.a_amax || !g.w_scale || g.act_ld % 16))
     return MOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_ADD_BF16 && (!g.add || g.ld_add % 8 || g.precise)) return MOE_ERR_UNSUPPORTED;
+  if (g.epi == EPI_COMBINE_I64 &&
+      (g.precise || g.fp8 || g.row_token || g.k_wrap || !g.offsets || !g.comb_token ||
+       !g.comb_slot_row || !g.comb_gates || g.comb_k < 1 || g.comb_T < 1 || g.ldo % 2))
+    return MOE_ERR_UNSUPPORTED;
   if (g.row_token && (g.fp8 || g.precise || g.k_wrap || !g.offsets || g.src_rows <= 0 ||
                       g.force_mode == 2))
     return MOE_ERR_UNSUPPORTED;
@@ -742,6 +786,11 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   ka.a_amax = g.a_amax;
   ka.w_scale = g.w_scale;
   ka.out_amax = g.epi == EPI_SQRELU_BF16 ? g.out_amax : nullptr;
+  ka.comb_token = g.comb_token;
+  ka.comb_slot_row = g.comb_slot_row;
+  ka.comb_gates = g.comb_gates;
+  ka.comb_k = g.comb_k;
+  ka.comb_T = g.comb_T;
   ka.status = status_word();
   if (!ka.status) return MOE_ERR_CUDA;
   GroupedGemm gg = g;

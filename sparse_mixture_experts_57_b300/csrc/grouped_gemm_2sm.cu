@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "fixed.cuh"
 #include "tc.cuh"
 #include "tc2.cuh"
 
@@ -58,6 +59,10 @@ struct KArgs2 {
   const uint32_t* a_amax;
   const float* w_scale;
   uint32_t* out_amax;
+  const int32_t* comb_token;  // EPI_COMBINE_I64: the routing of the rows (fixed.cuh)
+  const int32_t* comb_slot_row;
+  const float* comb_gates;
+  int comb_k, comb_T;
   int* status;
 };
 
@@ -293,6 +298,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int ncols = min(PAIR_N, a.N - col0);
       float scale = 1.f;
       if constexpr (F8) scale = ascale * a.w_scale[e];
+      int ctok = -1;  // EPI_COMBINE_I64: this row's token and gate
+      float cgate = 0.f;
+      if (a.epi == EPI_COMBINE_I64 && valid)
+        fixed_row_gate(a.comb_token, a.comb_slot_row, a.comb_gates, a.comb_k, a.comb_T, row,
+                       a.status, ctok, cgate);
       if (!mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag)) {
         *abort_flag = 1;
         record2(a.status, MOE_ERR_TIMEOUT);
@@ -316,7 +326,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             vmax = fmaxf(vmax, v[i]);
           }
         }
-        if (a.epi == EPI_F32) {
+        if (a.epi == EPI_COMBINE_I64) {
+          if (ctok >= 0) {
+            unsigned long long* p = static_cast<unsigned long long*>(a.out) +
+                                    static_cast<long long>(ctok) * a.ldo + col0 + n0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) fixed_add(p + i, cgate * v[i], a.status);
+          }
+        } else if (a.epi == EPI_F32) {
           float4* p = reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * a.ldo + col0 + n0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
@@ -357,7 +374,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 bool grouped_gemm_2sm_ok(const GroupedGemm& g) {
   if (g.row_token || g.precise || g.k_wrap || g.force_mode == 2) return false;
-  if (g.epi != EPI_BF16 && g.epi != EPI_SQRELU_BF16 && g.epi != EPI_F32) return false;
+  if (g.epi != EPI_BF16 && g.epi != EPI_SQRELU_BF16 && g.epi != EPI_F32 &&
+      g.epi != EPI_COMBINE_I64)
+    return false;
   const int groups = g.offsets ? g.E : 1;
   // a pair tile holds 256 rows: worth it with enough rows per group
   return static_cast<double>(g.rows) / groups >= 256.0;
@@ -378,6 +397,11 @@ int launch_grouped_gemm_2sm(const GroupedGemm& g, cudaStream_t s) {
   ka.a_amax = g.a_amax;
   ka.w_scale = g.w_scale;
   ka.out_amax = (g.fp8 && g.epi == EPI_SQRELU_BF16) ? g.out_amax : nullptr;
+  ka.comb_token = g.comb_token;
+  ka.comb_slot_row = g.comb_slot_row;
+  ka.comb_gates = g.comb_gates;
+  ka.comb_k = g.comb_k;
+  ka.comb_T = g.comb_T;
   ka.status = status_word();
   if (!ka.status) return MOE_ERR_CUDA;
   const int E = g.offsets ? g.E : 1;

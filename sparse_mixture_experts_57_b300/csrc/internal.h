@@ -129,6 +129,8 @@ enum Epilogue : int {
   EPI_SPLIT_BF16 = 3,   // acc = hi + mid + lo, three bf16 planes at out, out + lo_offset,
                         // out + 2 * lo_offset (about fp32 accuracy for the router input)
   EPI_ADD_BF16 = 4,     // out = bf16(acc + add[row, col]) (add: bf16, row stride ld_add)
+  EPI_COMBINE_I64 = 5,  // combine fused into the epilogue: out is an int64 [T, ldo] sum,
+                        // out[token(row), col] += round(gate(row) * acc * 2^32) (fixed.cuh)
 };
 
 // One grouped GEMM: for every group e and every row r in [offsets[e], offsets[e+1]):
@@ -163,6 +165,13 @@ struct GroupedGemm {
   const uint32_t* a_amax = nullptr;
   const float* w_scale = nullptr;
   uint32_t* out_amax = nullptr;
+  // EPI_COMBINE_I64 only: row r belongs to token comb_token[r] (< comb_T); its gate is
+  // comb_gates[t k + j] for the slot j with comb_slot_row[t k + j] == r (k = comb_k).
+  const int32_t* comb_token = nullptr;
+  const int32_t* comb_slot_row = nullptr;
+  const float* comb_gates = nullptr;
+  int comb_k = 0;
+  int comb_T = 0;
 };
 int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s);
 // The rows-as-M GEMM on CTA pairs (cta_group::2, 256 x 256 pair tiles): used by
@@ -293,5 +302,10 @@ int launch_permute(const int32_t* idx, const uint16_t* x, int64_t ldx, int T, in
 int launch_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row,
                    const float* gates, int T, int H, int k, uint16_t* y, cudaStream_t s,
                    const uint16_t* addend = nullptr);
+// The fused combine's two passes: set the int64 accumulator [T, H] to the addend in fixed
+// point (or zero), and after the down-projection's EPI_COMBINE_I64 epilogue write the n
+// outputs y = bf16(acc * 2^-32) (n a multiple of 8).
+int launch_init_fixed(int64_t* acc, int T, int H, const uint16_t* addend, cudaStream_t s);
+int launch_combine_fixed(const int64_t* acc, long long n, uint16_t* y, cudaStream_t s);
 
 }  // namespace moe

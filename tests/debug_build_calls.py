@@ -46,6 +46,9 @@ def run_calls(moe) -> dict:
                                                d["w_down"], k))
         done(f"gathered.{tag}", moe.moe_forward(d["x"], d["w_router"], d["bias"], d["w_up"],
                                                 d["w_down"], k, gathered=True))
+        done(f"fused_combine.{tag}", moe.moe_forward(d["x"], d["w_router"], d["bias"],
+                                                     d["w_up"], d["w_down"], k,
+                                                     fused_combine=True))
         s = {n: moe_synth.to_torch(v, "cuda")
              for n, v in moe_synth.shared_expert_inputs(w, 128).items()}
         done(f"shared.{tag}", moe.moe_forward_shared(d["x"], d["w_router"], d["bias"],

@@ -50,6 +50,12 @@ def test_workspace_sizes_are_monotone():
     # x_perm + h + y_perm dominate: rows * (2H + F) * 2 bytes
     assert b >= 16384 * 6 * (2 * 2688 + 1856) * 2
     assert L.moe_forward_workspace_size(-1, 64, 4, 2, 64) == 0
+    # the fused combine drops y_perm (rows * H * 2 bytes) and adds the int64 sums (T * H * 8)
+    T, H, E, k, F = 16384, 2688, 128, 6, 1856
+    fused = L.moe_forward_fused_combine_workspace_size(T, H, E, k, F)
+    plain = L.moe_forward_workspace_size(T, H, E, k, F)
+    assert abs((plain - fused) - (T * k * H * 2 - T * H * 8)) <= 1024
+    assert L.moe_forward_fused_combine_workspace_size(-1, 64, 4, 2, 64) == 0
     assert L.latent_moe_workspace_size(8192, 4096, 1024, 512, 24, 1024, 1) > \
         L.latent_moe_workspace_size(8192, 4096, 1024, 512, 24, 1024, 0)
 
@@ -70,6 +76,14 @@ def test_unaligned_sizes_are_unsupported():
     # H not a multiple of 64 (pointers are fake but never dereferenced)
     r = L.moe_forward(16, 16, 16, 16, 16, 4, 100, 8, 2, 64, 16, None, None, 16, 1 << 20, None)
     assert r == 2
+    r = L.moe_forward_fused_combine(16, 16, 16, 16, 16, 4, 100, 8, 2, 64, 16, None, None, 16,
+                                    1 << 20, None)
+    assert r == 2
+    # null weights with T > 0, and k > E: rejected before any CUDA call
+    assert L.moe_forward_fused_combine(16, 16, 16, 0, 16, 4, 128, 8, 2, 64, 16, None, None, 16,
+                                       1 << 20, None) == 1
+    assert L.moe_forward_fused_combine(16, 16, 16, 16, 16, 4, 128, 8, 9, 64, 16, None, None, 16,
+                                       1 << 20, None) == 1
     r = L.moe_linear(16, 16, 4, 96, 64, 16, None)
     assert r == 2
 

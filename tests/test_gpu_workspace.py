@@ -77,6 +77,9 @@ def test_moe_forward_stays_in_bounds(moe, T, H, E, k, F):
     for gathered in (False, True):
         _run_guarded(moe, moe.moe_forward, n, (T, H), d["x"], d["w_router"], d["bias"],
                      d["w_up"], d["w_down"], k, gathered=gathered)
+    n = L.moe_forward_fused_combine_workspace_size(T, H, E, k, F)
+    _run_guarded(moe, moe.moe_forward, n, (T, H), d["x"], d["w_router"], d["bias"],
+                 d["w_up"], d["w_down"], k, fused_combine=True)
 
 
 @pytest.mark.parametrize("T,H,E,k,F", SHAPES)
