@@ -505,6 +505,13 @@ def run_ours(args, w: moe_synth.Workload):
         achieved = alg["flops_experts"] / (ffn / 1e3) / 1e12
         peak = p_fp4
         unit = "TFLOP/s"
+    elif whole_call and alg["bytes"] / peaks["hbm_gbs"] / 1e9 >= \
+            alg["flops"] / peaks["bf16_tflops"] / 1e12:
+        # the whole layer call is bracketed, and streaming the expert weights dominates
+        bound = "hbm"
+        achieved = alg["bytes"] / (ffn / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
     elif w.latent or whole_call:
         # the whole layer call is bracketed; its tcgen05 GEMMs dominate
         bound = "tensor"

@@ -186,6 +186,7 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
           const uint16_t* w_down, int T, int D, int E, int k, int F, uint16_t* y,
           int32_t* idx_out, float* gates_out, const LayerWs& w, cudaStream_t s,
           const uint16_t* addend = nullptr, bool gather_tokens = false) {
+  if (w.acc && addend) return MOE_ERR_UNSUPPORTED;  // no fused-combine call takes an addend
   int32_t* idx = idx_out ? idx_out : w.idx;
   float* gates = gates_out ? gates_out : w.gates;
   // gather_tokens: with the rows on the MMA's M side the up-projection gathers its token
@@ -212,7 +213,7 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
     if (st) return st;
   }
   if (w.acc) {  // combine fused into the down-projection (carve_layer with fused_combine)
-    st = launch_init_fixed(w.acc, T, D, addend, s);
+    st = launch_zero_fixed(w.acc, static_cast<long long>(T) * D, s);
     if (st) return st;
     const FusedCombine fc{w.acc, w.row_token, w.slot_row, gates, T, k};
     st = gather ? ffn(nullptr, w.offsets, w_up, w_down, rows, D, F, E, w.h, nullptr, s,

@@ -63,28 +63,15 @@ __global__ void k_combine(const uint16_t* __restrict__ y_perm, int rows,
       make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
 }
 
-// The fused combine's accumulator starts at the addend in fixed point (exact for bf16 values
-// of magnitude 2^-24 and above), or at zero: one thread per 8 columns.
-__global__ void k_init_fixed(longlong2* __restrict__ acc, long long n8, int H,
-                             const uint16_t* __restrict__ addend) {
+// The fused combine's accumulator starts at zero: consecutive threads store consecutive 16
+// bytes, grid-stride.
+__global__ void k_zero_fixed(longlong2* __restrict__ acc, long long n2) {
   griddep_wait();
   griddep_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += stride) {
-    longlong2* dst = acc + i * 4;
-    if (!addend) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) dst[u] = make_longlong2(0, 0);
-      continue;
-    }
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(addend) + i);
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      dst[u] = make_longlong2(__float2ll_rn(__uint_as_float(w[u] << 16) * kFixedOne),
-                              __float2ll_rn(__uint_as_float(w[u] & 0xffff0000u) * kFixedOne));
-  }
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n2;
+       i += stride)
+    acc[i] = make_longlong2(0, 0);
 }
 
 // y[t, c] = bf16(acc[t, c] * 2^-32), one thread per 8 columns.
@@ -106,15 +93,15 @@ __global__ void k_combine_fixed(const longlong2* __restrict__ acc, long long n8,
 
 }  // namespace
 
-int launch_init_fixed(int64_t* acc, int T, int H, const uint16_t* addend, cudaStream_t s) {
-  if (T <= 0) return MOE_OK;
-  const long long n8 = static_cast<long long>(T) * (H / 8);
+int launch_zero_fixed(int64_t* acc, long long n, cudaStream_t s) {
+  if (n <= 0) return MOE_OK;
+  const long long n2 = n / 2;  // n is a multiple of 8
   const int threads = 256;
-  long long blocks = (n8 + threads - 1) / threads;
-  const long long cap = static_cast<long long>(sm_count()) * 8;
+  long long blocks = (n2 + threads - 1) / threads;
+  const long long cap = static_cast<long long>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
-  return launch_pdl(k_init_fixed, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
-                    reinterpret_cast<longlong2*>(acc), n8, H, addend);
+  return launch_pdl(k_zero_fixed, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
+                    reinterpret_cast<longlong2*>(acc), n2);
 }
 
 int launch_combine_fixed(const int64_t* acc, long long n, uint16_t* y, cudaStream_t s) {

@@ -302,10 +302,9 @@ int launch_permute(const int32_t* idx, const uint16_t* x, int64_t ldx, int T, in
 int launch_combine(const uint16_t* y_perm, int rows, const int32_t* slot_row,
                    const float* gates, int T, int H, int k, uint16_t* y, cudaStream_t s,
                    const uint16_t* addend = nullptr);
-// The fused combine's two passes: set the int64 accumulator [T, H] to the addend in fixed
-// point (or zero), and after the down-projection's EPI_COMBINE_I64 epilogue write the n
-// outputs y = bf16(acc * 2^-32) (n a multiple of 8).
-int launch_init_fixed(int64_t* acc, int T, int H, const uint16_t* addend, cudaStream_t s);
+// The fused combine's two passes: zero the n int64 sums, and after the down-projection's
+// EPI_COMBINE_I64 epilogue write y = bf16(acc * 2^-32) (n a multiple of 8).
+int launch_zero_fixed(int64_t* acc, long long n, cudaStream_t s);
 int launch_combine_fixed(const int64_t* acc, long long n, uint16_t* y, cudaStream_t s);
 
 }  // namespace moe
