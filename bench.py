@@ -119,9 +119,10 @@ def layer_algorithmic(w: moe_synth.Workload, counts: np.ndarray) -> dict:
     b_router = w.E * (D if (w.latent and w.router_on_latent) else w.H) * 2.0
     b_proj = 2.0 * w.H * w.latent * 2 if w.latent else 0.0
     b_io = 2.0 * w.T * w.H * 2
-    # per grouped-GEMM launch (up and down alike): one expert matrix per touched expert,
-    # plus the permuted activations read and written
-    ffn_bytes_per_launch = touched * D * w.F * 2.0 + rows * (D + w.F) * 2.0
+    # per expert-GEMM launch (up and down alike): one expert matrix per touched expert, plus
+    # the routed activations read (bf16, E4M3, or NVFP4 codes and scales) and written (bf16)
+    a_in = (0.5 + 1.0 / 16) if w.nvfp4 else (1.0 if w.fp8 else 2.0)
+    ffn_bytes_per_launch = touched * D * w.F * w_bytes + rows * (D + w.F) * (a_in + 2.0) / 2
     return {"flops": f_router + f_experts + f_proj, "bytes": b_weights + b_router + b_proj + b_io,
             "flops_router": f_router, "flops_experts": f_experts, "flops_proj": f_proj,
             "touched": touched, "ffn_flops_per_launch": 2.0 * rows * D * w.F,
@@ -132,7 +133,9 @@ def kernels_per_step(w: moe_synth.Workload, gathered: bool = False,
                      fused_combine: bool = False) -> int:
     """Library kernels one timed step launches (memsets excluded), mirroring the C library's
     choices: the fused small-batch routing kernel (T <= 256, E <= 256, routing width <= 6144)
-    or router logits + top-k + permutation (one small-batch block, or mark/count/scan)."""
+    or router logits + top-k + permutation (one small-batch block, or mark/count/scan, then
+    the map writer / row copy). With gathered (moe_forward_gathered) the up-projection
+    gathers its token rows itself, so the fused routing needs no separate row copy."""
     T, E, k = w.T, w.E, w.k
     d_route = (w.latent * (3 if w.router_on_latent else 0) or w.H) if w.latent else w.H
     fused = T <= 256 and E <= 256 and d_route <= 6144 and k <= 32
@@ -142,7 +145,11 @@ def kernels_per_step(w: moe_synth.Workload, gathered: bool = False,
         return (1 if fused else 2 + perm) + 8   # quantise h, down, combine
     if w.fp8:     # route (1 or 2 + perm), amax x, quantise x, up, quantise h, down, combine
         return (1 if fused else 2 + perm) + 6
-    route = 2 if fused else (2 + perm + 1)     # + the row copy
+    gather_in_gemm = gathered
+    if fused:
+        route = 1 if gather_in_gemm else 2     # + the row copy
+    else:
+        route = 2 + perm + 1                   # + the map writer (and row copy)
     if w.latent:  # projection in, routing in the latent space, FFN, combine, projection out
         return 1 + route + 2 + 1 + 1
     if fused_combine:  # zero the fixed-point sums, FFN (combine in the epilogue), convert
@@ -239,17 +246,6 @@ def run_ours(args, w: moe_synth.Workload):
     y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     gates = torch.empty((T, k), dtype=torch.float32, device=dev)
-    tie = torch.empty((T,), dtype=torch.uint8, device=dev)
-    counts = torch.empty((E,), dtype=torch.int32, device=dev)
-    offsets = torch.empty((E + 1,), dtype=torch.int32, device=dev)
-    row_token = torch.empty((rows,), dtype=torch.int32, device=dev)
-    slot_row = torch.empty((rows,), dtype=torch.int32, device=dev)
-    x_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev)
-    y_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev)
-    ws_rd = torch.empty(L.moe_route_dispatch_workspace_size(T, D, E, k), dtype=torch.uint8,
-                        device=dev)
-    ws_ffn = torch.empty(L.moe_grouped_ffn_workspace_size(rows, D, F, E), dtype=torch.uint8,
-                         device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     evict = torch.ones(L2_EVICT_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -258,102 +254,80 @@ def run_ours(args, w: moe_synth.Workload):
         # lines of another buffer, so their write-back to HBM happens here, untimed
         flush.zero_()
         evict.sum()
-    if w.latent:
-        ws_lat = torch.empty(L.latent_moe_workspace_size(T, H, w.latent, E, k, F,
-                                                         int(w.router_on_latent)),
-                             dtype=torch.uint8, device=dev)
-    elif w.fp8:
-        # weight quantisation is a set-up step, outside the timed region
-        f8_up = moe.moe_quantize_fp8_weights(d["w_up"])
-        f8_down = moe.moe_quantize_fp8_weights(d["w_down"])
-        del d["w_up"], d["w_down"]
-        ws_fp8 = torch.empty(L.moe_forward_fp8_workspace_size(T, H, E, k, F),
-                             dtype=torch.uint8, device=dev)
-    elif w.nvfp4:
-        # weight quantisation is a set-up step, outside the timed region
-        nv_up = moe.moe_quantize_nvfp4_weights(d["w_up"])
-        nv_down = moe.moe_quantize_nvfp4_weights(d["w_down"])
-        del d["w_up"], d["w_down"]
-        ws_fp4 = torch.empty(L.moe_forward_nvfp4_workspace_size(T, H, E, k, F),
-                             dtype=torch.uint8, device=dev)
-    elif args.fused_combine:
-        ws_fwd = torch.empty(L.moe_forward_fused_combine_workspace_size(T, H, E, k, F),
-                             dtype=torch.uint8, device=dev)
-    else:
-        ws_fwd = torch.empty(L.moe_forward_workspace_size(T, H, E, k, F), dtype=torch.uint8,
-                             device=dev)
-    # the whole-layer entry point of the standard bf16 layer
-    fwd_name = ("moe_forward_gathered" if args.gathered else
-                "moe_forward_fused_combine" if args.fused_combine else "moe_forward")
-    fwd_fn = getattr(L, fwd_name)
-    whole_call = args.gathered or args.fused_combine
 
     def chk(code, what):
         if code != 0:
             raise moe.MoeError(code, what)
 
+    # Every workload runs as its whole-layer C call, the call a user makes. The expert GEMMs,
+    # the dominant kernels, are timed inside it with the library's profiling hook, which
+    # records caller-owned events around the up- and down-projection GEMMs on the stream.
+    if w.latent:
+        ws = torch.empty(L.latent_moe_workspace_size(T, H, w.latent, E, k, F,
+                                                     int(w.router_on_latent)),
+                         dtype=torch.uint8, device=dev)
+
+        def layer_call(xp, yp, ip, gp):
+            chk(L.latent_moe(xp, P(d["w_in"]), P(d["w_out"]), P(d["w_router"]), P(d["bias"]),
+                             int(w.router_on_latent), P(d["w_up"]), P(d["w_down"]), T, H,
+                             w.latent, E, k, F, yp, ip, gp, P(ws), ws.numel(), sp), "latent_moe")
+    elif w.fp8:
+        # weight quantisation is a set-up step, outside the timed region
+        f8_up = moe.moe_quantize_fp8_weights(d["w_up"])
+        f8_down = moe.moe_quantize_fp8_weights(d["w_down"])
+        del d["w_up"], d["w_down"]
+        ws = torch.empty(L.moe_forward_fp8_workspace_size(T, H, E, k, F), dtype=torch.uint8,
+                         device=dev)
+
+        def layer_call(xp, yp, ip, gp):
+            chk(L.moe_forward_fp8(xp, P(d["w_router"]), P(d["bias"]), *f8_up.ptrs(),
+                                  *f8_down.ptrs(), T, H, E, k, F, yp, ip, gp, P(ws), ws.numel(),
+                                  sp), "moe_forward_fp8")
+    elif w.nvfp4:
+        # weight quantisation is a set-up step, outside the timed region
+        nv_up = moe.moe_quantize_nvfp4_weights(d["w_up"])
+        nv_down = moe.moe_quantize_nvfp4_weights(d["w_down"])
+        del d["w_up"], d["w_down"]
+        ws = torch.empty(L.moe_forward_nvfp4_workspace_size(T, H, E, k, F), dtype=torch.uint8,
+                         device=dev)
+
+        def layer_call(xp, yp, ip, gp):
+            chk(L.moe_forward_nvfp4(xp, P(d["w_router"]), P(d["bias"]), *nv_up.ptrs(),
+                                    *nv_down.ptrs(), T, H, E, k, F, yp, ip, gp, P(ws),
+                                    ws.numel(), sp), "moe_forward_nvfp4")
+    else:
+        # the standard bf16 layer: moe_forward, or one of its opt-in forms
+        fwd_name = ("moe_forward_gathered" if args.gathered else
+                    "moe_forward_fused_combine" if args.fused_combine else "moe_forward")
+        size_fn = (L.moe_forward_fused_combine_workspace_size if args.fused_combine
+                   else L.moe_forward_workspace_size)
+        ws = torch.empty(size_fn(T, H, E, k, F), dtype=torch.uint8, device=dev)
+        fwd_fn = getattr(L, fwd_name)
+
+        def layer_call(xp, yp, ip, gp):
+            chk(fwd_fn(xp, P(d["w_router"]), P(d["bias"]), P(d["w_up"]), P(d["w_down"]), T, H,
+                       E, k, F, yp, ip, gp, P(ws), ws.numel(), sp), fwd_name)
+
+    call_name = ("latent_moe" if w.latent else "moe_forward_fp8" if w.fp8 else
+                 "moe_forward_nvfp4" if w.nvfp4 else fwd_name)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    # one step; for the standard layer the four calls are issued one by one so the grouped
-    # FFN can be bracketed by events on the launching stream
-    def nvfp4_call(x_ptr, idx_ptr, gates_ptr):
-        chk(L.moe_forward_nvfp4(x_ptr, P(d["w_router"]), P(d["bias"]), *nv_up.ptrs(),
-                                *nv_down.ptrs(), T, H, E, k, F, P(y), idx_ptr, gates_ptr,
-                                P(ws_fp4), ws_fp4.numel(), sp), "moe_forward_nvfp4")
+    def hook_events(n):
+        """n groups of the 4 profiling events, created (recorded once) so that their CUDA
+        handles exist."""
+        groups = [[ev() for _ in range(4)] for _ in range(n)]
+        for g in groups:
+            for e in g:
+                e.record(stream)
+        return groups
 
-    def fp8_call(x_ptr, idx_ptr, gates_ptr):
-        chk(L.moe_forward_fp8(x_ptr, P(d["w_router"]), P(d["bias"]), *f8_up.ptrs(),
-                              *f8_down.ptrs(), T, H, E, k, F, P(y), idx_ptr, gates_ptr,
-                              P(ws_fp8), ws_fp8.numel(), sp), "moe_forward_fp8")
-
-    def step(e_ffn0=None, e_ffn1=None):
-        if whole_call:
-            # the whole layer through moe_forward_gathered (token rows gathered by the GEMM)
-            # or moe_forward_fused_combine (combine in the down-projection's epilogue)
-            if e_ffn0 is not None:
-                e_ffn0.record(stream)
-            chk(fwd_fn(P(d["x"]), P(d["w_router"]), P(d["bias"]), P(d["w_up"]), P(d["w_down"]),
-                       T, H, E, k, F, P(y), P(idx), P(gates), P(ws_fwd), ws_fwd.numel(), sp),
-                fwd_name)
-            if e_ffn1 is not None:
-                e_ffn1.record(stream)
-            return
-        if w.fp8:
-            if e_ffn0 is not None:
-                e_ffn0.record(stream)
-            fp8_call(P(d["x"]), P(idx), P(gates))
-            if e_ffn1 is not None:
-                e_ffn1.record(stream)
-            return
-        if w.nvfp4:
-            if e_ffn0 is not None:
-                e_ffn0.record(stream)
-            nvfp4_call(P(d["x"]), P(idx), P(gates))
-            if e_ffn1 is not None:
-                e_ffn1.record(stream)
-            return
-        if w.latent:
-            if e_ffn0 is not None:
-                e_ffn0.record(stream)
-            chk(L.latent_moe(P(d["x"]), P(d["w_in"]), P(d["w_out"]), P(d["w_router"]),
-                             P(d["bias"]), int(w.router_on_latent), P(d["w_up"]), P(d["w_down"]),
-                             T, H, w.latent, E, k, F, P(y), P(idx), P(gates), P(ws_lat),
-                             ws_lat.numel(), sp), "latent_moe")
-            if e_ffn1 is not None:
-                e_ffn1.record(stream)
-            return
-        chk(L.moe_route_dispatch(P(d["x"]), P(d["w_router"]), P(d["bias"]), T, H, E, k, P(idx),
-                                 P(gates), P(tie), P(counts), P(offsets), P(row_token),
-                                 P(slot_row), P(x_perm), P(ws_rd), ws_rd.numel(), sp),
-            "moe_route_dispatch")
-        if e_ffn0 is not None:
-            e_ffn0.record(stream)
-        chk(L.moe_grouped_ffn(P(x_perm), P(offsets), P(d["w_up"]), P(d["w_down"]), rows, H, F, E,
-                              P(y_perm), P(ws_ffn), ws_ffn.numel(), sp), "moe_grouped_ffn")
-        if e_ffn1 is not None:
-            e_ffn1.record(stream)
-        chk(L.moe_combine(P(y_perm), rows, P(slot_row), P(gates), T, H, k, P(y), sp),
-            "moe_combine")
+    def step(evs=None):
+        if evs is not None:
+            handles = (ctypes.c_void_p * 4)(*[e.cuda_event for e in evs])
+            chk(L.moe_set_profile_events(handles, 4), "moe_set_profile_events")
+        layer_call(P(d["x"]), P(y), P(idx), P(gates))
+        if evs is not None:
+            chk(L.moe_set_profile_events(None, 0), "moe_set_profile_events")
 
     # kernels per step: route 2, permutation 2-4, FFN 2, combine 1 (bf16); the latent layer
     # adds its two projections; the NVFP4 layer replaces the gather by amax, padding,
@@ -380,8 +354,8 @@ def run_ours(args, w: moe_synth.Workload):
     K = args.steps
     s_ev = [ev() for _ in range(K)]
     e_ev = [ev() for _ in range(K)]
-    f0 = [ev() for _ in range(K)]
-    f1 = [ev() for _ in range(K)]
+    g_ev = hook_events(K)
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -390,7 +364,7 @@ def run_ours(args, w: moe_synth.Workload):
     for i in range(K):
         flush_l2()
         s_ev[i].record(stream)
-        step(f0[i], f1[i])
+        step(g_ev[i])
         e_ev[i].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -400,11 +374,17 @@ def run_ours(args, w: moe_synth.Workload):
     time.sleep(0.25)
     clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(s_ev, e_ev)]
-    ffn_ms = [a.elapsed_time(b) for a, b in zip(f0, f1)]
-    # phases of a step: before the bracketed call(s), inside them, after them
-    phase_ms = {"before_bracket": statistics.mean(s.elapsed_time(a) for s, a in zip(s_ev, f0)),
-                "bracket": statistics.mean(ffn_ms),
-                "after_bracket": statistics.mean(b.elapsed_time(e) for b, e in zip(f1, e_ev))}
+    # the dominant kernels: the up- and down-projection GEMMs, each bracketed by the hook
+    up_ms = [g[0].elapsed_time(g[1]) for g in g_ev]
+    down_ms = [g[2].elapsed_time(g[3]) for g in g_ev]
+    ffn_ms = [a + b for a, b in zip(up_ms, down_ms)]
+    # phases of a step: before the up-projection GEMM, from its start to the end of the
+    # down-projection GEMM, after it
+    phase_ms = {"before_up_gemm": statistics.mean(s.elapsed_time(g[0]) for s, g in zip(s_ev, g_ev)),
+                "up_gemm": statistics.mean(up_ms),
+                "between_gemms": statistics.mean(g[1].elapsed_time(g[2]) for g in g_ev),
+                "down_gemm": statistics.mean(down_ms),
+                "after_down_gemm": statistics.mean(g[3].elapsed_time(e) for g, e in zip(g_ev, e_ev))}
     ms = statistics.mean(step_ms)
     ffn = statistics.mean(ffn_ms)
     ms, ffn = max_over_ranks([ms, ffn], dev, world)
@@ -437,23 +417,7 @@ def run_ours(args, w: moe_synth.Workload):
         stream.wait_event(ev_in[b])
         if started[b]:
             stream.wait_event(ev_out[b])         # step i-2's output has left y_dev[b]
-        xp, yp = P(x_dev[b]), P(y_dev[b])
-        if w.fp8:
-            chk(L.moe_forward_fp8(xp, P(d["w_router"]), P(d["bias"]), *f8_up.ptrs(),
-                                  *f8_down.ptrs(), T, H, E, k, F, yp, None, None,
-                                  P(ws_fp8), ws_fp8.numel(), sp), "moe_forward_fp8")
-        elif w.nvfp4:
-            chk(L.moe_forward_nvfp4(xp, P(d["w_router"]), P(d["bias"]), *nv_up.ptrs(),
-                                    *nv_down.ptrs(), T, H, E, k, F, yp, None, None,
-                                    P(ws_fp4), ws_fp4.numel(), sp), "moe_forward_nvfp4")
-        elif w.latent:
-            chk(L.latent_moe(xp, P(d["w_in"]), P(d["w_out"]), P(d["w_router"]),
-                             P(d["bias"]), int(w.router_on_latent), P(d["w_up"]), P(d["w_down"]),
-                             T, H, w.latent, E, k, F, yp, None, None, P(ws_lat),
-                             ws_lat.numel(), sp), "latent_moe")
-        else:
-            chk(fwd_fn(xp, P(d["w_router"]), P(d["bias"]), P(d["w_up"]), P(d["w_down"]), T, H,
-                       E, k, F, yp, None, None, P(ws_fwd), ws_fwd.numel(), sp), fwd_name)
+        layer_call(P(x_dev[b]), P(y_dev[b]), None, None)
         ev_comp[b].record(stream)
         with torch.cuda.stream(d2h):
             d2h.wait_event(ev_comp[b])
@@ -483,51 +447,20 @@ def run_ours(args, w: moe_synth.Workload):
 
     peaks, peak_src = load_peaks()
     alg = layer_algorithmic(w, counts_from_routing(routing, E))
-    launches = 1 if (w.latent or w.nvfp4 or w.fp8 or whole_call) else 2  # calls bracketed
+    launches = 2  # the up- and down-projection GEMMs, each bracketed by the hook
     p_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
     p_fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
-    t_fp8_flops = alg["flops_experts"] / p_fp8 / 1e12
-    t_fp8_bytes = alg["bytes"] / peaks["hbm_gbs"] / 1e9
-    if w.fp8 and t_fp8_bytes >= t_fp8_flops:
-        # the whole FP8 layer call is bracketed; streaming the E4M3 weights dominates
-        bound = "hbm"
-        achieved = alg["bytes"] / (ffn / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-    elif w.fp8:
+    p_tensor = p_fp4 if w.nvfp4 else (p_fp8 if w.fp8 else peaks["bf16_tflops"])
+    gemm_flops = alg["ffn_flops_per_launch"] * launches
+    gemm_bytes = alg["ffn_bytes_per_launch"] * launches
+    if gemm_flops / p_tensor / 1e12 >= gemm_bytes / peaks["hbm_gbs"] / 1e9:
         bound = "tensor"
-        achieved = alg["flops_experts"] / (ffn / 1e3) / 1e12
-        peak = p_fp8
-        unit = "TFLOP/s"
-    elif w.nvfp4:
-        # the whole NVFP4 layer call is bracketed; its block-scaled GEMMs dominate
-        bound = "tensor"
-        achieved = alg["flops_experts"] / (ffn / 1e3) / 1e12
-        peak = p_fp4
-        unit = "TFLOP/s"
-    elif whole_call and alg["bytes"] / peaks["hbm_gbs"] / 1e9 >= \
-            alg["flops"] / peaks["bf16_tflops"] / 1e12:
-        # the whole layer call is bracketed, and streaming the expert weights dominates
-        bound = "hbm"
-        achieved = alg["bytes"] / (ffn / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-    elif w.latent or whole_call:
-        # the whole layer call is bracketed; its tcgen05 GEMMs dominate
-        bound = "tensor"
-        dom_units = alg["flops"]
-        achieved = dom_units / (ffn / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
-        unit = "TFLOP/s"
-    elif alg["ffn_flops_per_launch"] / peaks["bf16_tflops"] / 1e12 > \
-            alg["ffn_bytes_per_launch"] / peaks["hbm_gbs"] / 1e9:
-        bound = "tensor"
-        achieved = alg["ffn_flops_per_launch"] * launches / (ffn / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
+        achieved = gemm_flops / (ffn / 1e3) / 1e12
+        peak = p_tensor
         unit = "TFLOP/s"
     else:
         bound = "hbm"
-        achieved = alg["ffn_bytes_per_launch"] * launches / (ffn / 1e3) / 1e9
+        achieved = gemm_bytes / (ffn / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     if w.nvfp4 or w.fp8:
@@ -536,7 +469,8 @@ def run_ours(args, w: moe_synth.Workload):
     else:
         t_flops = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
     roof_ms = max(t_flops, alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
-    traffic = None if whole_call else read_traffic(w.name, alg["touched"])
+    traffic = None if (args.gathered or args.fused_combine) else \
+        read_traffic(w.name, alg["touched"])
     out = {
         "metric": METRIC,
         "value": job_tokens_per_s(world, T, ms),
@@ -554,7 +488,7 @@ def run_ours(args, w: moe_synth.Workload):
         "config": {"workload": w.name, "T": T, "H": H, "E": E, "k": k, "F": F,
                    "latent": w.latent or None, "bias": w.bias,
                    "l2": "flushed before every step (512 MiB write, then 256 MiB read)",
-                   "layer_call": fwd_name if whole_call else None,
+                   "layer_call": call_name,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
@@ -562,18 +496,16 @@ def run_ours(args, w: moe_synth.Workload):
                                         "from the committed ncu summary of this kernel source "
                                         "(profiles/), not measured in this run")
                      if traffic is not None else None,
-                     "kernel": ("whole latent layer (tcgen05 GEMMs dominate)" if w.latent
-                                else "whole layer, token rows gathered by the up-projection"
-                                if args.gathered
-                                else "whole layer, combine fused into the down-projection"
-                                if args.fused_combine
-                                else "whole NVFP4 layer (block-scaled tcgen05 GEMMs dominate)"
-                                if w.nvfp4
-                                else "whole FP8 layer (E4M3 tcgen05 grouped GEMMs dominate)"
-                                if w.fp8
-                                else "grouped expert GEMM (tcgen05), up + down launches"),
+                     "kernel": ("expert up- and down-projection GEMMs ("
+                                + ("block-scaled NVFP4 tcgen05" if w.nvfp4 else
+                                   "E4M3 tcgen05" if w.fp8 else "bf16 tcgen05")
+                                + (", the down-projection adding into the fixed-point sums"
+                                   if args.fused_combine else "")
+                                + (", the up-projection gathering token rows"
+                                   if args.gathered else "")
+                                + f"), timed inside {call_name} by moe_set_profile_events"),
                      "peak_source": (f"{peak_src} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16)"
-                                     if w.nvfp4 else
+                                     if (w.nvfp4 and bound == "tensor") else
                                      f"{peak_src} bf16 x {FP8_OVER_BF16:g} (nominal FP8/BF16)"
                                      if (w.fp8 and bound == "tensor") else peak_src),
                      "ffn_ms": ffn, "launches_timed": launches},

@@ -51,6 +51,16 @@ const char* moe_status_string(int status);
  * holds MOE_OK or the first error that a kernel recorded since it was last cleared. */
 int moe_get_device_status(cudaStream_t stream, int* status_out);
 
+/* moe_set_profile_events: a profiling hook with no counterpart in the pages. With n = 4, the
+ * layer and grouped-FFN calls made afterwards on the calling thread record events[0] and
+ * events[1] on their stream just before and just after the expert up-projection GEMM, and
+ * events[2] and events[3] around the down-projection GEMM (for the NVFP4 and FP8 calls the
+ * activation quantisers fall outside both brackets). The events belong to the caller
+ * (cudaEventCreate); the library keeps the four handles and only records them. n = 0 turns
+ * the hook off. MOE_ERR_INVALID_ARG for another n or a NULL handle. A failed record makes
+ * the layer call return MOE_ERR_CUDA. */
+int moe_set_profile_events(const cudaEvent_t* events, int n);
+
 /* ---------------------------------------------------------------------------------------
  * moe_route: the learned router with aux-loss-free, bias-corrected top-k.
  *   z[t,e] = sum_d x[t,d] * w_router[e,d]   (bf16 inputs, fp32 accumulation)
@@ -183,12 +193,13 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* bias,
                 int32_t* topk_idx_out, float* gates_out,
                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* moe_forward_gathered: moe_forward whose up-projection, when the rows sit on the MMA's M side
- * (more than 48 rows per expert on average), gathers the routed token rows straight from x
- * with TMA tile::gather4, so the permuted copy x_perm is never written; otherwise identical
- * to moe_forward. Same arguments and workspace (moe_forward_workspace_size()). On B300 the
- * 32 gather4 copies per 128-row K-slice make the up-projection slower than reading a
- * materialised x_perm, so moe_forward does not use it. */
+/* moe_forward_gathered: moe_forward whose up-projection gathers the routed token rows
+ * straight from x with TMA tile::gather4, so the permuted copy x_perm is never written.
+ * With more than 48 rows per expert on average the rows sit on the MMA's M side and a
+ * 128-row K-slice takes 32 gather4 copies; with fewer, the weights sit on M and a slice of
+ * BN token rows takes BN / 4. Same results as moe_forward, bit for bit (the same operands in
+ * the same order), same arguments and workspace (moe_forward_workspace_size()). On B300 both
+ * forms are slower than reading a materialised x_perm, so moe_forward does not use them. */
 int moe_forward_gathered(const uint16_t* x, const uint16_t* w_router, const float* bias,
                          const uint16_t* w_up, const uint16_t* w_down, int T, int H, int E, int k,
                          int F, uint16_t* y, int32_t* topk_idx_out, float* gates_out,

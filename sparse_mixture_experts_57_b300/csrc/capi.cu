@@ -125,6 +125,22 @@ int router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_router, int 
 
 // Expert FFNs. The up-projection reads x_perm [rows, D], or, when row_token is given, gathers
 // the rows from x_src (src_rows rows, row stride ld_src) by token: x_perm is never written.
+// Profiling hook (moe_set_profile_events): events recorded around the expert GEMMs of the
+// layer calls made on this thread.
+struct ProfileEvents {
+  cudaEvent_t ev[4];
+  bool on = false;
+};
+thread_local ProfileEvents g_profile;
+
+// Mark i: 0 before the up-projection GEMM, 1 after it, 2 before the down-projection GEMM,
+// 3 after it.
+int profile_mark(int i, cudaStream_t s) {
+  if (!g_profile.on) return MOE_OK;
+  MOE_CUDA(cudaEventRecord(g_profile.ev[i], s));
+  return MOE_OK;
+}
+
 // With `fc`, the down-projection's epilogue adds each row's gated output into its token's
 // fixed-point sum fc->acc (EPI_COMBINE_I64) and y_perm is not written.
 struct FusedCombine {
@@ -153,7 +169,11 @@ int ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_up,
   up.out = h;
   up.ldo = F;
   up.epi = EPI_SQRELU_BF16;
-  int st = launch_grouped_gemm(up, s);
+  int st = profile_mark(0, s);
+  if (st) return st;
+  st = launch_grouped_gemm(up, s);
+  if (st) return st;
+  st = profile_mark(1, s);
   if (st) return st;
   GroupedGemm dn{};
   dn.act = h;
@@ -176,7 +196,11 @@ int ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_up,
     dn.comb_k = fc->k;
     dn.comb_T = fc->T;
   }
-  return launch_grouped_gemm(dn, s);
+  st = profile_mark(2, s);
+  if (st) return st;
+  st = launch_grouped_gemm(dn, s);
+  if (st) return st;
+  return profile_mark(3, s);
 }
 
 // route -> permute -> grouped FFN -> combine for rows of width D read from x (row stride ldx).
@@ -192,7 +216,11 @@ int layer(const uint16_t* x, int64_t ldx, const uint16_t* xr, int64_t ldr, int D
   // gather_tokens: with the rows on the MMA's M side the up-projection gathers its token
   // rows itself (TMA gather4), so the permutation only builds the maps (no x_perm copy).
   const int rows = T * k;
-  const bool gather = gather_tokens && grouped_gemm_rows_as_m(rows, E);
+  // gather_tokens (moe_forward_gathered): the up-projection gathers its token rows itself
+  // with TMA gather4 (32 copies per K-slice with the rows on the MMA's M side, BN / 4 with
+  // the weights there), so x_perm is never written. Both forms measured slower than reading
+  // a materialised x_perm on B300, so moe_forward does not gather.
+  const bool gather = gather_tokens;
   int st;
   if (route_fused_ok(T, Dr, E, k, parts)) {
     // small batches: logits, top-k and the dispatch maps in one kernel, then the row copy
@@ -347,7 +375,11 @@ int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const Toke
   g.ldo = F;
   g.epi = EPI_SQRELU_BF16;
   g.out_amax = w.amax + 1;
+  st = profile_mark(0, s);
+  if (st) return st;
   st = launch_fp4_gemm(g, s);
+  if (st) return st;
+  st = profile_mark(1, s);
   if (st) return st;
   st = launch_quant_act(w.h, F, w.P, nullptr, nullptr, w.poff, E, F, w.P, w.amax + 1, w.hq,
                         w.hsf, s);
@@ -369,7 +401,11 @@ int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const Toke
   d.out = y_perm;
   d.ldo = H;
   d.epi = EPI_BF16;
-  return launch_fp4_gemm(d, s);
+  st = profile_mark(2, s);
+  if (st) return st;
+  st = launch_fp4_gemm(d, s);
+  if (st) return st;
+  return profile_mark(3, s);
 }
 
 // FP8 expert FFN buffers (unpadded: the E4M3 GEMM needs no scale atoms).
@@ -421,7 +457,11 @@ int ffn_fp8(const uint16_t* src, long long ld, long long amax_rows, const TokenS
   g.a_amax = w.amax;
   g.w_scale = up_scale;
   g.out_amax = w.amax + 1;
+  st = profile_mark(0, s);
+  if (st) return st;
   st = launch_grouped_gemm(g, s);
+  if (st) return st;
+  st = profile_mark(1, s);
   if (st) return st;
   st = launch_quant_fp8(w.h, F, nullptr, rows, F, 0, w.amax + 1, w.hq, s);
   if (st) return st;
@@ -440,7 +480,11 @@ int ffn_fp8(const uint16_t* src, long long ld, long long amax_rows, const TokenS
   d.fp8 = 1;
   d.a_amax = w.amax + 1;
   d.w_scale = down_scale;
-  return launch_grouped_gemm(d, s);
+  st = profile_mark(2, s);
+  if (st) return st;
+  st = launch_grouped_gemm(d, s);
+  if (st) return st;
+  return profile_mark(3, s);
 }
 
 // Routing and dispatch buffers at the head of the moe_forward_nvfp4 / moe_forward_fp8
@@ -503,6 +547,20 @@ bool nvfp4_weights_ok(const uint8_t* codes, const uint8_t* scales, const float* 
 using namespace moe;
 
 extern "C" {
+
+int moe_set_profile_events(const cudaEvent_t* events, int n) {
+  if (n == 0) {
+    g_profile.on = false;
+    return MOE_OK;
+  }
+  if (n != 4 || !events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+    g_profile.ev[i] = events[i];
+  }
+  g_profile.on = true;
+  return MOE_OK;
+}
 
 const char* moe_status_string(int status) {
   switch (status) {

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
   constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;
   constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
   static_assert(!(F8 && CHUNKED), "E4M3 kernels have no chunked variant");
-  static_assert(!GATHER || (!SWAP && !CHUNKED && !F8), "gathered rows: bf16 rows-as-M only");
+  static_assert(!GATHER || (!CHUNKED && !F8), "gathered rows: bf16 only");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
   static_assert(!CHUNKED || (!SWAP && BN % 128 == 0),
                 "chunked accumulation: rows-as-M, BN 128 or 256");
@@ -315,24 +315,41 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
 
   if (warp == 0 && GATHER) {
     // ------------------------------------------------------- TMA producer (gathered rows)
-    const uint64_t pol_w = policy_evict_last();
+    const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_last();
     const uint64_t pol_a = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
     long long armed = 0;
     bool ok = true;
+    // token ids of a tile's rows (rows past the group's end: an out-of-range row, read as
+    // zeros), one per lane and register; the next tile's ids load while lane 0 issues the
+    // current tile's copies
+    constexpr int TJ = (RT + 31) / 32;
+    int tok[TJ];
+    auto fetch_ids = [&](int tile) {
+      if (tile >= total) return;
+      int e, rt, ct;
+      decode_tile(tile, n_ct, s_pref, E, e, rt, ct);
+      const int rbeg = rt * RT;
+      const int valid_rows = min(RT, s_cnt[e] - rbeg);
+#pragma unroll
+      for (int j = 0; j < TJ; ++j) {
+        const int i = lane + 32 * j;
+        tok[j] = i < valid_rows ? __ldg(a.row_token + s_off[e] + rbeg + i) : a.src_rows;
+      }
+    };
+    fetch_ids(blockIdx.x);
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       int e, rt, ct;
       decode_tile(tile, n_ct, s_pref, E, e, rt, ct);
-      const int rbeg = rt * BM;
-      const int valid_rows = min(BM, s_cnt[e] - rbeg);
       const int col0 = ct * CT;
 #pragma unroll
-      for (int j = 0; j < BM / 32; ++j) {
+      for (int j = 0; j < TJ; ++j) {
         const int i = lane + 32 * j;
-        s_tok[i] = i < valid_rows ? __ldg(a.row_token + s_off[e] + rbeg + i) : a.src_rows;
+        if (i < RT) s_tok[i] = tok[j];
       }
       __syncwarp();
+      fetch_ids(tile + static_cast<int>(gridDim.x));
       if (lane == 0) {
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -342,12 +359,14 @@ __global__ void __launch_bounds__(kernel_threads(CHUNKED), 1)
           mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
           ++armed;
           const int kc = kb * BKE;
-          uint8_t* dst = sA + stage * A_BYTES;
+          // the activation rows: the A operand (rows-as-M) or the B operand (weights-as-M)
+          uint8_t* dst = SWAP ? sB + stage * B_BYTES : sA + stage * A_BYTES;
+          if (SWAP) tma_load_3d(sA + stage * A_BYTES, &tm_w, &full[stage], kc, col0, e, pol_w);
 #pragma unroll 4
-          for (int g4 = 0; g4 < BM / 4; ++g4)
+          for (int g4 = 0; g4 < RT / 4; ++g4)
             tma_gather4(dst + g4 * 512, &tm_act, &full[stage], kc, s_tok[4 * g4],
                         s_tok[4 * g4 + 1], s_tok[4 * g4 + 2], s_tok[4 * g4 + 3], pol_a);
-          tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kc, col0, e, pol_w);
+          if (!SWAP) tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kc, col0, e, pol_w);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -763,8 +782,7 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
       (g.precise || g.fp8 || g.row_token || g.k_wrap || !g.offsets || !g.comb_token ||
        !g.comb_slot_row || !g.comb_gates || g.comb_k < 1 || g.comb_T < 1 || g.ldo % 2))
     return MOE_ERR_UNSUPPORTED;
-  if (g.row_token && (g.fp8 || g.precise || g.k_wrap || !g.offsets || g.src_rows <= 0 ||
-                      g.force_mode == 2))
+  if (g.row_token && (g.fp8 || g.precise || g.k_wrap || !g.offsets || g.src_rows <= 0))
     return MOE_ERR_UNSUPPORTED;
   KArgs ka;
   ka.offsets = g.offsets;
@@ -803,7 +821,14 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   if (g.precise)
     return g.N > 128 ? launch_variant<256, 4, false, true>(gg, ka, s)
                      : launch_variant<128, 6, false, true>(gg, ka, s);
-  if (g.row_token) {  // gathered activation rows: always rows-as-M
+  if (g.row_token) {  // gathered activation rows
+    const double rows_per_group = static_cast<double>(g.rows) / gg.E;
+    if (g.force_mode == 2 || (g.force_mode == 0 && rows_per_group <= 48.0)) {
+      // weights on M: each K-slice gathers BN / 4 groups of four token rows for the B operand
+      if (rows_per_group <= 16.0) return launch_variant<16, 10, true, false, false, true>(gg, ka, s);
+      if (rows_per_group <= 32.0) return launch_variant<32, 8, true, false, false, true>(gg, ka, s);
+      return launch_variant<64, 8, true, false, false, true>(gg, ka, s);
+    }
     switch (pick_bn_rows_as_m(g.N)) {
       case 256: return launch_variant<256, 4, false, false, false, true>(gg, ka, s);
       case 224: return launch_variant<224, 4, false, false, false, true>(gg, ka, s);

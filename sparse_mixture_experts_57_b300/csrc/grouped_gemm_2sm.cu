@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(remote_tempty + acc * 8);
+      if (lane == 0) mbar_arrive_cluster_cta(remote_tempty + acc * 8);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;

@@ -17,6 +17,7 @@
 
 #include "internal.h"
 #include "scan.cuh"
+#include "tc2.cuh"
 
 namespace moe {
 namespace {
@@ -88,40 +89,19 @@ __global__ void k_router_logits(const uint16_t* __restrict__ x, long long ldx,
 constexpr int kSmallTok = 8, kSmallExp = 8;
 constexpr int kSmallMaxElems = 6144;  // staged elements per token row (all planes)
 
-// Router logits of the 8 tokens t0.. against expert e (one warp per expert): the tokens are
-// staged in shared memory (sx), then each lane takes every 32nd 16-byte vector of the
-// expert's row, in ascending order. The row is streamed through a ring of kAhead registers
-// refilled one vector per iteration, so kAhead loads stay in flight while the loop body stays
-// small (these kernels run once per layer with a cold instruction cache: unrolling the
-// 8-token x kAhead-vector product multiplies the code that every SM must fetch).
-// Every thread of the CTA must call this.
+// Router logits of 8 staged token rows against expert e, by one warp: each lane takes every
+// 32nd 16-byte vector of the expert's row, in ascending order. The row is streamed through
+// a ring of kAhead registers refilled one vector per iteration, so kAhead loads stay in
+// flight while the loop body stays small (these kernels run once per layer with a cold
+// instruction cache: unrolling the 8-token x kAhead-vector product multiplies the code that
+// every SM must fetch). Returns the logit of token t on lane t < 8.
 template <int PARTS>
-__device__ __forceinline__ void logits_tile(const uint16_t* __restrict__ x, long long ldx,
-                                            const uint16_t* __restrict__ w, int T, int D, int E,
-                                            int t0, uint4* sx, float* __restrict__ logits) {
+__device__ __forceinline__ float logits_warp(const uint4* sx, const uint16_t* __restrict__ w,
+                                             int D, int e) {
   constexpr int kAhead = 8;
-  const int nvec = D / 8, rowv = PARTS * nvec, n = kSmallTok * rowv;
-  const int nt = blockDim.x;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  auto xload = [&](int i) {
-    const int t = i / rowv, v = i - t * rowv;
-    return t0 + t < T ? __ldg(reinterpret_cast<const uint4*>(x + (t0 + t) * ldx) + v) : zero;
-  };
-  int i = threadIdx.x;
-#pragma unroll 1
-  for (; i + 3 * nt < n; i += 4 * nt) {
-    const uint4 a = xload(i), b = xload(i + nt), c = xload(i + 2 * nt), d = xload(i + 3 * nt);
-    sx[i] = a;
-    sx[i + nt] = b;
-    sx[i + 2 * nt] = c;
-    sx[i + 3 * nt] = d;
-  }
-#pragma unroll 1
-  for (; i < n; i += nt) sx[i] = xload(i);
-  __syncthreads();
+  const int nvec = D / 8, rowv = PARTS * nvec;
   const int lane = threadIdx.x & 31;
-  const int e = blockIdx.y * kSmallExp + (threadIdx.x >> 5);
-  if (e >= E) return;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   const uint4* wrow = reinterpret_cast<const uint4*>(w + static_cast<long long>(e) * D);
   uint4 ring[kAhead];
 #pragma unroll
@@ -147,13 +127,44 @@ __device__ __forceinline__ void logits_tile(const uint16_t* __restrict__ x, long
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
   }
-  if (lane < kSmallTok && t0 + lane < T) {
-    float v = acc[0];
+  float v = acc[0];
 #pragma unroll
-    for (int t = 1; t < kSmallTok; ++t)
-      if (lane == t) v = acc[t];
-    logits[static_cast<long long>(t0 + lane) * E + e] = v;
+  for (int t = 1; t < kSmallTok; ++t)
+    if (lane == t) v = acc[t];
+  return v;
+}
+
+// Router logits of the 8 tokens t0.. against expert e (one warp per expert): the tokens are
+// staged in shared memory (sx) with plain loads, then logits_warp. Every thread of the CTA
+// must call this.
+template <int PARTS>
+__device__ __forceinline__ void logits_tile(const uint16_t* __restrict__ x, long long ldx,
+                                            const uint16_t* __restrict__ w, int T, int D, int E,
+                                            int t0, uint4* sx, float* __restrict__ logits) {
+  const int nvec = D / 8, rowv = PARTS * nvec, n = kSmallTok * rowv;
+  const int nt = blockDim.x;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  auto xload = [&](int i) {
+    const int t = i / rowv, v = i - t * rowv;
+    return t0 + t < T ? __ldg(reinterpret_cast<const uint4*>(x + (t0 + t) * ldx) + v) : zero;
+  };
+  int i = threadIdx.x;
+#pragma unroll 1
+  for (; i + 3 * nt < n; i += 4 * nt) {
+    const uint4 a = xload(i), b = xload(i + nt), c = xload(i + 2 * nt), d = xload(i + 3 * nt);
+    sx[i] = a;
+    sx[i + nt] = b;
+    sx[i + 2 * nt] = c;
+    sx[i + 3 * nt] = d;
   }
+#pragma unroll 1
+  for (; i < n; i += nt) sx[i] = xload(i);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.y * kSmallExp + (threadIdx.x >> 5);
+  if (e >= E) return;
+  const float v = logits_warp<PARTS>(sx, w, D, e);
+  if (lane < kSmallTok && t0 + lane < T) logits[static_cast<long long>(t0 + lane) * E + e] = v;
 }
 
 template <int PARTS>
@@ -418,6 +429,66 @@ __device__ __forceinline__ bool flag_all_set(unsigned long long* flags, int mine
   return __all_sync(0xffffffffu, set);
 }
 
+// Dispatch maps of all T tokens, built by one CTA (every thread calls this) from their
+// top-k (idx, written by other CTAs of the kernel and read through L2): per-expert counts
+// and offsets, then row_token / slot_row, the rows of one expert in ascending token order (a
+// token-word x expert bit matrix, as moe_permute). scratch: W * E * 8 bytes of shared
+// memory, W = ceil(T / 32); warp_sums: 33 ints of shared memory.
+__device__ __noinline__ void dispatch_maps(const int32_t* __restrict__ idx, int T, int E, int k,
+                                           int32_t* __restrict__ counts,
+                                           int32_t* __restrict__ offsets,
+                                           int32_t* __restrict__ row_token,
+                                           int32_t* __restrict__ slot_row, uint32_t* scratch,
+                                           int* warp_sums, int* status) {
+  __shared__ int s_off[kFusedMaxE];
+  const int tid = threadIdx.x;
+  const int W = (T + 31) / 32;
+  uint32_t* bits = scratch;                           // [W][E]
+  int* wpref = reinterpret_cast<int*>(bits + W * E);  // [W][E]
+  for (int i = tid; i < W * E; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  bool bad = false;
+  for (int i = tid; i < T * k; i += blockDim.x) {
+    const int t = i / k;
+    const int e = __ldcg(idx + i);
+    if (e < 0 || e >= E) {
+      bad = true;
+      continue;
+    }
+    const uint32_t bit = 1u << (t & 31);
+    if (atomicOr(&bits[(t >> 5) * E + e], bit) & bit) bad = true;
+  }
+  if (__syncthreads_or(bad) && tid == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
+  int c = 0;
+  if (tid < E) {
+    for (int wd = 0; wd < W; ++wd) {
+      wpref[wd * E + tid] = c;
+      c += __popc(bits[wd * E + tid]);
+    }
+    counts[tid] = c;
+  }
+  int total;
+  const int excl = block_exclusive_scan(c, warp_sums, &total);
+  if (tid < E) {
+    offsets[tid] = excl;
+    s_off[tid] = excl;
+  }
+  if (tid == 0) offsets[E] = total;
+  __syncthreads();
+  for (int i = tid; i < T * k; i += blockDim.x) {
+    const int t = i / k;
+    const int e = __ldcg(idx + i);
+    if (e < 0 || e >= E) {
+      slot_row[i] = -1;
+      continue;
+    }
+    const int o = (t >> 5) * E + e;
+    const int row = s_off[e] + wpref[o] + __popc(bits[o] & ((1u << (t & 31)) - 1u));
+    row_token[row] = t;
+    slot_row[i] = row;
+  }
+}
+
 template <int VPL, int PARTS>
 __global__ void __launch_bounds__(256)
     k_route_small(const uint16_t* __restrict__ x, long long ldx, const uint16_t* __restrict__ w,
@@ -469,52 +540,114 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
-  const int W = (T + 31) / 32;
-  uint32_t* bits = reinterpret_cast<uint32_t*>(sx);  // [W][E]
-  int* wpref = reinterpret_cast<int*>(bits + W * E);  // [W][E]
-  for (int i = tid; i < W * E; i += blockDim.x) bits[i] = 0u;
+  dispatch_maps(idx, T, E, k, counts, offsets, row_token, slot_row,
+                reinterpret_cast<uint32_t*>(sx), warp_sums, status);
+  if (tid < static_cast<int>(gridDim.x)) __stcg(tflags + tid, 0ull);
+}
+
+// Small batches with E <= 128, the same three steps with a cluster per token group. Grid
+// (token groups of 8, C = ceil(E / 8) expert groups), cluster (1, C, 1), 256 threads:
+//  0. the CTA's 8 router-weight rows are prefetched into L2 before the kernel waits for its
+//     predecessor (they are layer parameters that no earlier kernel writes); the group's
+//     token rows are staged with one bulk copy each;
+//  1. every CTA computes its 8 x 8 tile of logits and stores each token's values straight
+//     into the shared memory of the CTA that ranks that token (token t: rank t % C);
+//  2. after a cluster barrier, each CTA runs the top-k of its tokens from shared memory,
+//     one warp per token;
+//  3. after a second cluster barrier, rank 0 of each group stores the group's flag, and the
+//     last group to finish builds the dispatch maps (dispatch_maps).
+// Compared with k_route_small, the logits never go through L2 and no CTA waits on flags of
+// its own group: the exchange is a hardware cluster barrier.
+constexpr int kClusterMaxE = 128;
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+template <int VPL, int PARTS>
+__global__ void __launch_bounds__(256)
+    k_route_cluster(const uint16_t* __restrict__ x, long long ldx,
+                    const uint16_t* __restrict__ w, const float* __restrict__ bias, int T, int D,
+                    int E, int k, int32_t* __restrict__ idx, float* __restrict__ gates,
+                    uint8_t* __restrict__ tie, int perm, int32_t* __restrict__ counts,
+                    int32_t* __restrict__ offsets, int32_t* __restrict__ row_token,
+                    int32_t* __restrict__ slot_row, unsigned long long* __restrict__ sync,
+                    unsigned long long gen, int* status) {
+  extern __shared__ uint4 sx[];  // [8][PARTS * D / 8] token rows; later the dispatch scratch
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ float s_lg[kSmallTok][kClusterMaxE];  // logits of the tokens this CTA ranks
+  __shared__ float s_bias[kClusterMaxE];
+  __shared__ int s_flag;
+  __shared__ int s_abort;
+  __shared__ int warp_sums[33];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = static_cast<int>(gridDim.y);
+  const uint32_t rank = cluster_ctarank();
+  const int t0 = blockIdx.x * kSmallTok;
+  const int nt = min(kSmallTok, T - t0);
+  const int e = blockIdx.y * kSmallExp + warp;
+  const int rowv = PARTS * (D / 8);
+  if (lane == 0 && e < E)
+    prefetch_l2(w + static_cast<long long>(e) * D, static_cast<uint32_t>(D) * 2u);
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  cluster_arrive_relaxed();  // this CTA has started: peers may write its shared memory
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int i = tid; i < E; i += blockDim.x) s_bias[i] = __ldg(bias + i);
   __syncthreads();
-  bool bad = false;
-  for (int i = tid; i < T * k; i += blockDim.x) {
-    const int t = i / k;
-    const int e = __ldcg(idx + i);
-    if (e < 0 || e >= E) {
-      bad = true;
-      continue;
-    }
-    const uint32_t bit = 1u << (t & 31);
-    if (atomicOr(&bits[(t >> 5) * E + e], bit) & bit) bad = true;
+  if (tid == 0) {
+    const uint32_t row_bytes = static_cast<uint32_t>(rowv) * 16u;
+    mbar_arrive_expect_tx(&s_bar, row_bytes * static_cast<uint32_t>(nt));
+    const uint64_t pol = policy_evict_first();
+    for (int t = 0; t < nt; ++t)
+      bulk_load(sx + t * rowv, x + static_cast<long long>(t0 + t) * ldx, row_bytes, &s_bar, pol);
   }
-  if (__syncthreads_or(bad) && tid == 0) atomicCAS(status, 0, MOE_ERR_INVALID_ARG);
-  int c = 0;
-  if (tid < E) {
-    for (int wd = 0; wd < W; ++wd) {
-      wpref[wd * E + tid] = c;
-      c += __popc(bits[wd * E + tid]);
-    }
-    counts[tid] = c;
+  for (int i = nt * rowv + tid; i < kSmallTok * rowv; i += blockDim.x)
+    sx[i] = make_uint4(0u, 0u, 0u, 0u);  // rows past T
+  if (!mbar_wait(&s_bar, 0, &s_abort)) {
+    if (tid == 0) atomicCAS(status, 0, MOE_ERR_TIMEOUT);
+    mbar_wait(&s_bar, 0, &s_abort, kDrainLimitNs);  // no copy may land after the CTA exits
   }
-  int total;
-  const int excl = block_exclusive_scan(c, warp_sums, &total);
-  __shared__ int s_off[kFusedMaxE];
-  if (tid < E) {
-    offsets[tid] = excl;
-    s_off[tid] = excl;
-  }
-  if (tid == 0) offsets[E] = total;
   __syncthreads();
-  for (int i = tid; i < T * k; i += blockDim.x) {
-    const int t = i / k;
-    const int e = __ldcg(idx + i);
-    if (e < 0 || e >= E) {
-      slot_row[i] = -1;
-      continue;
-    }
-    const int o = (t >> 5) * E + e;
-    const int row = s_off[e] + wpref[o] + __popc(bits[o] & ((1u << (t & 31)) - 1u));
-    row_token[row] = t;
-    slot_row[i] = row;
+  float v = 0.f;
+  if (e < E) v = logits_warp<PARTS>(sx, w, D, e);
+  cluster_wait();  // every CTA of the cluster has started
+  if (e < E && lane < nt)
+    st_cluster_f32(mapa_shared(&s_lg[lane][e], static_cast<uint32_t>(lane % C)), v);
+  cluster_sync();  // all logits of the group delivered
+  const int t = static_cast<int>(rank) + C * warp;
+  if (t < nt) {
+    if (use_select<VPL>(k))
+      topk_token_select<VPL, false>(s_lg[t], s_bias, t0 + t, E, k, idx, gates, tie);
+    else
+      topk_token<VPL, false>(s_lg[t], s_bias, t0 + t, E, k, idx, gates, tie);
   }
+  __threadfence();  // this thread's top-k results before the group's flag
+  cluster_sync();   // every top-k of the group is written; no CTA reads peers' memory after
+  if (!perm || rank != 0) return;
+  unsigned long long* tflags = sync + kFusedGroups * kFusedExpGroups;  // [grid.x]
+  if (warp == 0) {
+    const bool all = flag_all_set(tflags, blockIdx.x, gridDim.x, gen);
+    if (tid == 0) s_flag = all;
+  }
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  dispatch_maps(idx, T, E, k, counts, offsets, row_token, slot_row,
+                reinterpret_cast<uint32_t*>(sx), warp_sums, status);
   if (tid < static_cast<int>(gridDim.x)) __stcg(tflags + tid, 0ull);
 }
 
@@ -583,6 +716,12 @@ int launch_topk(const float* logits, const float* bias, int T, int E, int k, int
   return launch_pdl(k_topk<32>, b, th, 0, s, logits, bias, T, E, k, idx, gates, tie);
 }
 
+// The CUDA error of the last refused cluster launch of the small-batch routing (0: none).
+int& cluster_launch_error() {
+  static int e = 0;
+  return e;
+}
+
 bool route_fused_ok(int T, int D, int E, int k, int parts) {
   return T >= 1 && T <= kFusedMaxT && E >= 1 && E <= kFusedMaxE && k <= 32 &&
          (parts == 1 || parts == 3) &&
@@ -624,6 +763,67 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
                       row_token, slot_row, reinterpret_cast<unsigned long long*>(sync), gen,
                       status);
   };
+  // The cluster form: one cluster of C = ceil(E / 8) CTAs per token group (C <= 16; more
+  // than 8 is a non-portable cluster size). Returns 1 when it cannot run here (the caller
+  // then launches k_route_small).
+  auto go_cluster = [&](auto kern) -> int {
+    static int ready_device = -1, usable = 0;
+    int dev = 0;
+    MOE_CUDA(cudaGetDevice(&dev));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = grid.y;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (ready_device != dev) {
+      MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmallTok * kSmallMaxElems * 2));
+      MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+      // the largest cluster (16 CTAs) with the largest staging buffer must fit at least once
+      cudaLaunchConfig_t probe = cfg;
+      cudaLaunchAttribute pattr = attr[0];
+      pattr.val.clusterDim.y = kClusterMaxE / kSmallExp;
+      probe.gridDim = dim3(1, pattr.val.clusterDim.y);
+      probe.dynamicSmemBytes = kSmallTok * kSmallMaxElems * 2;
+      probe.attrs = &pattr;
+      int n = 0;
+      usable = cudaOccupancyMaxActiveClusters(&n, kern, &probe) == cudaSuccess && n > 0;
+      cudaGetLastError();  // a refused query is not an error of this call
+      ready_device = dev;
+    }
+    if (!usable) return 1;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, x, static_cast<long long>(ldx),
+                                             w_router, bias, T, D, E, k, idx, gates, tie, perm,
+                                             counts, offsets, row_token, slot_row,
+                                             reinterpret_cast<unsigned long long*>(sync), gen,
+                                             status);
+    if (e == cudaSuccess) return MOE_OK;
+    // a configuration this device refuses (nothing was launched): use k_route_small from now
+    cluster_launch_error() = static_cast<int>(e);
+    cudaGetLastError();
+    usable = 0;
+    return 1;
+  };
+  if (E <= kClusterMaxE && ldx % 8 == 0 && aligned16(x)) {
+    int st = 1;
+    if (parts == 3)
+      st = E <= 32 ? go_cluster(k_route_cluster<1, 3>)
+         : E <= 64 ? go_cluster(k_route_cluster<2, 3>) : go_cluster(k_route_cluster<4, 3>);
+    else
+      st = E <= 32 ? go_cluster(k_route_cluster<1, 1>)
+         : E <= 64 ? go_cluster(k_route_cluster<2, 1>) : go_cluster(k_route_cluster<4, 1>);
+    if (st != 1) return st;
+  }
   if (parts == 3) {
     if (E <= 32) return go(k_route_small<1, 3>);
     if (E <= 64) return go(k_route_small<2, 3>);

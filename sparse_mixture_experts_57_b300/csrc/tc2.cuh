@@ -36,6 +36,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// The same arrival with release semantics at CTA scope only: for a signal that orders no
+// memory the peer reads (the epilogue's "accumulator read" signal, issued after
+// tcgen05.wait::ld and tcgen05.fence::before_thread_sync), so the arriving thread does not
+// wait for its earlier global stores to become visible across the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster_cta(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(

@@ -262,9 +262,8 @@ def test_layer_shapes(moe, T, H, E, k, F):
 @pytest.mark.parametrize("T,H,E,k,F", [(513, 256, 32, 4, 192), (700, 512, 8, 3, 448),
                                        (64, 128, 16, 2, 64)])
 def test_layer_gathered_tokens(moe, T, H, E, k, F):
-    """moe_forward_gathered: the up-projection gathers the token rows itself (TMA gather4)
-    when the rows sit on the MMA's M side (first two shapes); the last shape falls back to a
-    materialised x_perm (weights on M)."""
+    """moe_forward_gathered: the up-projection gathers the token rows itself (TMA gather4),
+    with the rows on the MMA's M side (first two shapes) or the weights there (the last)."""
     w = moe_synth.Workload("gathered", T=T, H=H, E=E, k=k, F=F, seed=T + H + 3)
     inp = moe_synth.layer_inputs(w)
     dev = {key: to_dev(v) for key, v in inp.items()}
@@ -276,6 +275,29 @@ def test_layer_gathered_tokens(moe, T, H, E, k, F):
     ref = O.moe_layer(inp["x"], inp["w_router"], inp["bias"], inp["w_up"], inp["w_down"], k)
     same = check_selection(idx.cpu().numpy(), ref, inp["bias"], k)
     assert_close(bf16_out(y)[same], ref["y"][same], f"gathered layer T={T}")
+
+
+# rows per expert 3, 12.5 and 18.75 (16-row tiles), 25 (32), 46.9 (64); the last two shapes
+# route with the multi-kernel path (T > 256), the others with the fused small-batch kernel
+@pytest.mark.parametrize("T,H,E,k,F", [(64, 2688, 128, 6, 1856), (100, 512, 64, 8, 256),
+                                       (200, 256, 32, 4, 128), (600, 256, 256, 8, 128),
+                                       (300, 256, 32, 5, 128)])
+def test_layer_weights_on_m_gathers_exactly(moe, T, H, E, k, F):
+    """With at most 48 rows per expert moe_forward_gathered's up-projection gathers the token
+    rows itself (TMA gather4 into the B operand, the weights on the MMA's M side) instead of
+    reading x_perm. Its operands and accumulation order are the materialised path's, so the
+    layer output must equal route + permute (x_perm) + grouped FFN + combine bit for bit."""
+    w = moe_synth.Workload("gather_b", T=T, H=H, E=E, k=k, F=F, seed=T + E)
+    inp = moe_synth.layer_inputs(w)
+    dev = {key: to_dev(v) for key, v in inp.items()}
+    y = moe.moe_forward(dev["x"], dev["w_router"], dev["bias"], dev["w_up"], dev["w_down"], k,
+                        gathered=True)
+    idx, gates, tie, p = moe.moe_route_dispatch(dev["x"], dev["w_router"], dev["bias"], k)
+    yp = moe.moe_grouped_ffn(p["x_perm"], p["offsets"], dev["w_up"], dev["w_down"])
+    ys = moe.moe_combine(yp, p["slot_row"], gates, T, k)
+    torch.cuda.synchronize()
+    _status_ok(moe)
+    assert torch.equal(y.view(torch.int16), ys.view(torch.int16))
 
 
 def test_layer_nano_decode_full(moe):
