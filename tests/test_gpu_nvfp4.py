@@ -140,6 +140,12 @@ def _offsets(counts):
     # single column tile (N = 192) and a K tail of one MMA step in a partial stage (K = 320)
     ([300, 0, 1, 129, 1000, 600], 320, 192),
     ([90, 410, 5, 700, 300], 2688, 1856),      # Nano widths, many row tiles per group
+    # several row tiles per group, odd tile counts, a single-row and an empty group; N = 448
+    # gives a partial second weight block in the up-projection, N = 320 a last column tile
+    # with no second weight block in the down-projection
+    ([600, 520, 130, 900], 320, 448),
+    ([1200, 1, 800, 900, 0], 256, 448),
+    ([700, 900, 520, 1300], 2688, 1856),
 ])
 def test_grouped_ffn_nvfp4(moe, counts, H, F):
     E = len(counts)
