@@ -61,6 +61,13 @@ int moe_get_device_status(cudaStream_t stream, int* status_out);
  * the layer call return MOE_ERR_CUDA. */
 int moe_set_profile_events(const cudaEvent_t* events, int n);
 
+/* moe_route_cluster_refusal: a diagnostic with no counterpart in the pages. Small batches
+ * (T <= 256, E <= 128) route with one thread-block cluster per group of 8 tokens (up to 16
+ * CTAs, a non-portable cluster size). If the device refuses that launch configuration, the
+ * library falls back to its cluster-free routing kernel (same results) for the rest of the
+ * process; this returns the cudaError_t of the refusal, or 0 if none happened. */
+int moe_route_cluster_refusal(void);
+
 /* ---------------------------------------------------------------------------------------
  * moe_route: the learned router with aux-loss-free, bias-corrected top-k.
  *   z[t,e] = sum_d x[t,d] * w_router[e,d]   (bf16 inputs, fp32 accumulation)

@@ -56,6 +56,7 @@ SIGNATURES = {
     "moe_forward_fused_combine_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_fixed_to_bf16": (_I, [_VP, ctypes.c_longlong, _VP, _I, _VP]),
     "moe_set_profile_events": (_I, [_VP, _I]),
+    "moe_route_cluster_refusal": (_I, []),
     "moe_forward_fused_combine": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP,
                                        _VP, _VP, _SZ, _VP]),
     "moe_nvfp4_codes_bytes": (_SZ, [_I, _I, _I]),

@@ -848,3 +848,5 @@ int launch_gather_rows(const int32_t* row_token, const uint16_t* x, int64_t ldx,
 }
 
 }  // namespace moe
+
+extern "C" int moe_route_cluster_refusal(void) { return moe::cluster_launch_error(); }

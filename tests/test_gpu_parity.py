@@ -74,6 +74,9 @@ def _route_case(moe, T, D, E, k, seed, bias_kind="uniform"):
                                      (40, 128, 1000, 32)])
 def test_route(moe, T, D, E, k):
     _route_case(moe, T, D, E, k, seed=T + E)
+    # small batches route on thread-block clusters; a refused cluster launch would fall back
+    # to the cluster-free kernel silently
+    assert moe.lib().moe_route_cluster_refusal() == 0
 
 
 @pytest.mark.parametrize("T,D,E,k", [(64, 2688, 128, 6), (1, 256, 16, 2), (200, 512, 256, 8),
@@ -303,6 +306,7 @@ def test_layer_weights_on_m_gathers_exactly(moe, T, H, E, k, F):
 def test_layer_nano_decode_full(moe):
     """The whole decode workload (64 tokens, 128 experts, top-6) against the oracle."""
     _layer_full(moe, moe_synth.WORKLOADS["nano_decode"])
+    assert moe.lib().moe_route_cluster_refusal() == 0
 
 
 def _sampled_layer(moe, w, n_sample=200):
