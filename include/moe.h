@@ -362,12 +362,16 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
  * token tensor, and the whole h. Decisions in fp32 with correctly rounded division. The GEMMs
  * run on tcgen05 kind::f8f6f4 (E4M3 x E4M3, fp32 accumulation); routing, dispatch and the
  * combine stay bf16/fp32.
- * Formats: codes [G, N, K] bytes (E4M3), scale [G] fp32 (s of each matrix).
+ * Formats: codes [G, N, ldk] bytes (E4M3; row n of matrix g at (g N + n) ldk, K codes then
+ * padding), ldk = K rounded up to a multiple of 128 so that every 128-byte K-slice the GEMMs
+ * load starts on a 128-byte boundary; scale [G] fp32 (s of each matrix).
  * ------------------------------------------------------------------------------------- */
 
 /* moe_quantize_fp8_weights: quantise G bf16 matrices w [G, N, K] (K a multiple of 16; w and
- * codes 16-byte aligned) into codes and per-matrix scales. A set-up step; no workspace
- * (scale doubles as the amax accumulator). Asynchronous on `stream`. */
+ * codes 16-byte aligned) into codes ([G, N, ldk], moe_fp8_codes_bytes() bytes; the padding
+ * bytes of each row are left as they are) and per-matrix scales. A set-up step; no
+ * workspace (scale doubles as the amax accumulator). Asynchronous on `stream`. */
+size_t moe_fp8_codes_bytes(int G, int N, int K);
 int moe_quantize_fp8_weights(const uint16_t* w, int G, int N, int K, uint8_t* codes,
                              float* scale, cudaStream_t stream);
 
@@ -415,10 +419,13 @@ int moe_forward_fp8(const uint16_t* x, const uint16_t* w_router, const float* bi
  *  - x_codes, x_scales: the quantised routed tokens. NVFP4: codes [buffer_rows, H/2] and
  *    scale atoms of [buffer_rows, H] (the formats above), padded segment order; row
  *    padded_offsets[e] + r holds permuted row offsets[e] + r. FP8: E4M3 bytes
- *    [buffer_rows, H] in permuted row order; x_scales is NULL.
+ *    [buffer_rows, H] in permuted row order; x_scales is NULL. Code rows are x_codes_ld
+ *    bytes apart: H/2 (NVFP4) or H (FP8) rounded up to a multiple of 128, so every
+ *    128-byte K-slice the GEMM loads starts on a 128-byte boundary.
  *  - h [buffer_rows, F] bf16: max(0, x_q . w_up_q[e]^T)^2 as stored by the up-projection
  *    (NVFP4: padded order, padding rows zero).
- *  - h_codes, h_scales: h quantised for the down-projection, as x_codes / x_scales.
+ *  - h_codes, h_scales: h quantised for the down-projection, as x_codes / x_scales, code
+ *    rows h_codes_ld bytes apart (F/2 or F rounded up to a multiple of 128).
  *  - buffer_rows: rows of the x / h buffers (NVFP4: the padded-row bound
  *    rows + 127 E rounded up to 128; FP8: rows).
  * Return: MOE_ERR_INVALID_ARG for sizes the named call rejects or a NULL out;
@@ -435,6 +442,8 @@ typedef struct moe_quant_view {
   const uint8_t* h_codes;
   const uint8_t* h_scales;
   long long buffer_rows;
+  long long x_codes_ld;
+  long long h_codes_ld;
 } moe_quant_view;
 
 int moe_grouped_ffn_nvfp4_view(int rows, int H, int F, int E, const void* workspace,

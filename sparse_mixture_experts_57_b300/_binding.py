@@ -26,7 +26,8 @@ class QuantView(ctypes.Structure):
     """struct moe_quant_view of include/moe.h."""
     _fields_ = [("offsets", _VP), ("row_token", _VP), ("padded_offsets", _VP), ("amax", _VP),
                 ("x_codes", _VP), ("x_scales", _VP), ("h", _VP), ("h_codes", _VP),
-                ("h_scales", _VP), ("buffer_rows", ctypes.c_longlong)]
+                ("h_scales", _VP), ("buffer_rows", ctypes.c_longlong),
+                ("x_codes_ld", ctypes.c_longlong), ("h_codes_ld", ctypes.c_longlong)]
 
 
 _QV = ctypes.POINTER(QuantView)
@@ -56,6 +57,7 @@ SIGNATURES = {
     "moe_forward_fused_combine_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_fixed_to_bf16": (_I, [_VP, ctypes.c_longlong, _VP, _I, _VP]),
     "moe_set_profile_events": (_I, [_VP, _I]),
+    "moe_fp8_codes_bytes": (_SZ, [_I, _I, _I]),
     "moe_route_cluster_refusal": (_I, []),
     "moe_forward_fused_combine": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP,
                                        _VP, _VP, _SZ, _VP]),
@@ -413,7 +415,8 @@ def moe_forward_nvfp4(x, w_router, bias, w_up: Nvfp4Weights, w_down: Nvfp4Weight
 
 class Fp8Weights:
     """G expert matrices [N, K] quantised to per-tensor E4M3 on the device:
-    codes [G, N, K] uint8 and scale [G] fp32 (include/moe.h)."""
+    codes [G, N, ldk] uint8 (ldk = K rounded up to 128; columns past K are padding) and
+    scale [G] fp32 (include/moe.h)."""
 
     def __init__(self, codes, scale, G, N, K):
         self.codes, self.scale = codes, scale
@@ -426,7 +429,8 @@ class Fp8Weights:
 def moe_quantize_fp8_weights(w, *, stream=None) -> Fp8Weights:
     _cuda_tensor(w, torch.bfloat16, "w", 3)
     G, N, K = w.shape
-    codes = torch.empty((G, N, K), dtype=torch.uint8, device=w.device)
+    ldk = int(lib().moe_fp8_codes_bytes(G, N, K)) // (G * N)
+    codes = torch.zeros((G, N, ldk), dtype=torch.uint8, device=w.device)
     scale = torch.empty((G,), dtype=torch.float32, device=w.device)
     _check(lib().moe_quantize_fp8_weights(_ptr(w), G, N, K, _ptr(codes), _ptr(scale),
                                           _stream(stream)), "moe_quantize_fp8_weights")
@@ -494,9 +498,11 @@ def quant_view(call: str, dims, workspace) -> dict:
                                              workspace.numel(), ctypes.byref(v)),
            _VIEW_CALLS[call])
     base = workspace.data_ptr()
+    sizes = ("buffer_rows", "x_codes_ld", "h_codes_ld")
     out = {name: (None if getattr(v, name) is None else getattr(v, name) - base)
-           for name, _ in QuantView._fields_ if name != "buffer_rows"}
-    out["buffer_rows"] = int(v.buffer_rows)
+           for name, _ in QuantView._fields_ if name not in sizes}
+    for name in sizes:
+        out[name] = int(getattr(v, name))
     return out
 
 

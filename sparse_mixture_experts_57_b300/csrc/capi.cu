@@ -316,10 +316,10 @@ Fp4Ws carve_fp4(Carver& c, int rows, int H, int F, int E) {
   const size_t P = static_cast<size_t>(w.P);
   w.poff = c.take<int32_t>(E + 1);
   w.amax = c.take<uint32_t>(2);
-  w.xq = c.take<uint8_t>(P * H / 2);
+  w.xq = c.take<uint8_t>(P * fp4_act_pitch(H));
   w.xsf = c.take<uint8_t>(nvfp4_sf_bytes(w.P, H));
   w.h = c.take<uint16_t>(P * F);
-  w.hq = c.take<uint8_t>(P * F / 2);
+  w.hq = c.take<uint8_t>(P * fp4_act_pitch(F));
   w.hsf = c.take<uint8_t>(nvfp4_sf_bytes(w.P, F));
   return w;
 }
@@ -359,6 +359,7 @@ int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const Toke
   if (st) return st;
   Fp4Gemm g{};
   g.a_codes = w.xq;
+  g.a_ld = fp4_act_pitch(H);
   g.a_sf = w.xsf;
   g.a_amax = w.amax;
   g.P = w.P;
@@ -386,6 +387,7 @@ int ffn_nvfp4(const uint16_t* src, long long ld, long long amax_rows, const Toke
   if (st) return st;
   Fp4Gemm d{};
   d.a_codes = w.hq;
+  d.a_ld = fp4_act_pitch(F);
   d.a_sf = w.hsf;
   d.a_amax = w.amax + 1;
   d.P = w.P;
@@ -416,12 +418,13 @@ struct Fp8Ws {
   uint8_t* hq;
 };
 
+// xq and hq rows are fp8_act_pitch(H) and fp8_act_pitch(F) bytes apart.
 Fp8Ws carve_fp8(Carver& c, int rows, int H, int F) {
   Fp8Ws w;
   w.amax = c.take<uint32_t>(2);
-  w.xq = c.take<uint8_t>(static_cast<size_t>(rows) * H);
+  w.xq = c.take<uint8_t>(static_cast<size_t>(rows) * fp8_act_pitch(H));
   w.h = c.take<uint16_t>(static_cast<size_t>(rows) * F);
-  w.hq = c.take<uint8_t>(static_cast<size_t>(rows) * F);
+  w.hq = c.take<uint8_t>(static_cast<size_t>(rows) * fp8_act_pitch(F));
   return w;
 }
 
@@ -437,15 +440,16 @@ int ffn_fp8(const uint16_t* src, long long ld, long long amax_rows, const TokenS
   if (st) return st;
   if (slots)
     st = launch_quant_fp8_tokens(src, ld, slots->T, slots->k, slots->slot_row, rows, H, w.amax,
-                                 w.xq, s);
+                                 w.xq, fp8_act_pitch(H), s);
   else
-    st = launch_quant_fp8(src, ld, nullptr, rows, H, 0, w.amax, w.xq, s);
+    st = launch_quant_fp8(src, ld, nullptr, rows, H, 0, w.amax, w.xq, fp8_act_pitch(H), s);
   if (st) return st;
   GroupedGemm g{};
   g.act = w.xq;
-  g.act_ld = H;
+  g.act_ld = fp8_act_pitch(H);
   g.rows = rows;
   g.w = up;
+  g.w_ld = fp8_act_pitch(H);
   g.E = E;
   g.N = F;
   g.K = H;
@@ -463,13 +467,14 @@ int ffn_fp8(const uint16_t* src, long long ld, long long amax_rows, const TokenS
   if (st) return st;
   st = profile_mark(1, s);
   if (st) return st;
-  st = launch_quant_fp8(w.h, F, nullptr, rows, F, 0, w.amax + 1, w.hq, s);
+  st = launch_quant_fp8(w.h, F, nullptr, rows, F, 0, w.amax + 1, w.hq, fp8_act_pitch(F), s);
   if (st) return st;
   GroupedGemm d{};
   d.act = w.hq;
-  d.act_ld = F;
+  d.act_ld = fp8_act_pitch(F);
   d.rows = rows;
   d.w = down;
+  d.w_ld = fp8_act_pitch(F);
   d.E = E;
   d.N = H;
   d.K = F;
@@ -998,6 +1003,11 @@ int moe_forward_nvfp4(const uint16_t* x, const uint16_t* w_router, const float* 
   return launch_combine(f.y_perm, rows, f.slot_row, gates, T, H, k, y, stream);
 }
 
+size_t moe_fp8_codes_bytes(int G, int N, int K) {
+  if (G < 1 || N < 1 || K < 1) return 0;
+  return static_cast<size_t>(G) * N * static_cast<size_t>(fp8_act_pitch(K));
+}
+
 int moe_quantize_fp8_weights(const uint16_t* w, int G, int N, int K, uint8_t* codes,
                              float* scale, cudaStream_t stream) {
   if (G < 1 || N < 1 || K < 16) return MOE_ERR_INVALID_ARG;
@@ -1008,7 +1018,8 @@ int moe_quantize_fp8_weights(const uint16_t* w, int G, int N, int K, uint8_t* co
   uint32_t* amax = reinterpret_cast<uint32_t*>(scale);
   int st = launch_amax_bf16(w, static_cast<long long>(N) * K, G, amax, stream);
   if (st) return st;
-  st = launch_quant_fp8(w, K, nullptr, static_cast<long long>(G) * N, K, N, amax, codes, stream);
+  st = launch_quant_fp8(w, K, nullptr, static_cast<long long>(G) * N, K, N, amax, codes,
+                        fp8_act_pitch(K), stream);
   if (st) return st;
   return launch_finalize_fp8_scale(scale, G, stream);
 }
@@ -1209,6 +1220,8 @@ int moe_grouped_ffn_nvfp4_view(int rows, int H, int F, int E, const void* worksp
   out->h_codes = w.hq;
   out->h_scales = w.hsf;
   out->buffer_rows = w.P;
+  out->x_codes_ld = fp4_act_pitch(H);
+  out->h_codes_ld = fp4_act_pitch(F);
   return MOE_OK;
 }
 
@@ -1231,6 +1244,8 @@ int moe_forward_nvfp4_view(int T, int H, int E, int k, int F, const void* worksp
   out->h_codes = w.hq;
   out->h_scales = w.hsf;
   out->buffer_rows = w.P;
+  out->x_codes_ld = fp4_act_pitch(H);
+  out->h_codes_ld = fp4_act_pitch(F);
   return MOE_OK;
 }
 
@@ -1246,6 +1261,8 @@ int moe_grouped_ffn_fp8_view(int rows, int H, int F, int E, const void* workspac
   out->h = w.h;
   out->h_codes = w.hq;
   out->buffer_rows = rows;
+  out->x_codes_ld = fp8_act_pitch(H);
+  out->h_codes_ld = fp8_act_pitch(F);
   return MOE_OK;
 }
 
@@ -1264,6 +1281,8 @@ int moe_forward_fp8_view(int T, int H, int E, int k, int F, const void* workspac
   out->h = w.h;
   out->h_codes = w.hq;
   out->buffer_rows = T * k;
+  out->x_codes_ld = fp8_act_pitch(H);
+  out->h_codes_ld = fp8_act_pitch(F);
   return MOE_OK;
 }
 

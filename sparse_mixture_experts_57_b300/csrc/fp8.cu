@@ -26,11 +26,12 @@ constexpr int kFp8SegVec = 128;  // 16-byte vectors (8 values) per warp segment
 
 // One warp per (row, 1024-value segment): lane t converts the vectors t, t+32, t+64, t+96
 // of the segment, so each 16-byte load and each 8-byte code store of the warp is contiguous.
-// The quantisation is elementwise, so no lane needs its neighbours' values.
+// The quantisation is elementwise, so no lane needs its neighbours' values. Output rows are
+// ldo bytes apart.
 __global__ void k_quant_fp8(const uint16_t* __restrict__ src, long long ld,
                             const int32_t* __restrict__ row_map, long long rows, int K,
                             long long rows_per_scale, const uint32_t* __restrict__ amax,
-                            uint8_t* __restrict__ out) {
+                            uint8_t* __restrict__ out, long long ldo) {
   griddep_wait();
   griddep_launch_dependents();
   const int nvec = K / 8;
@@ -68,19 +69,19 @@ __global__ void k_quant_fp8(const uint16_t* __restrict__ src, long long ld,
         o[k >> 1] |= e4m3x2(__fdiv_rn(lo, s), __fdiv_rn(hi, s)) << (16 * (k & 1));
       }
     }
-    *reinterpret_cast<uint2*>(out + r * K + static_cast<long long>(v) * 8) = make_uint2(o[0], o[1]);
+    *reinterpret_cast<uint2*>(out + r * ldo + static_cast<long long>(v) * 8) = make_uint2(o[0], o[1]);
   }
 }
 
 // Routed tokens, each quantised once and written to every one of its k permuted rows
-// slot_row[t k + j] (E4M3 bytes [rows, K]). A token's codes are the same in all its copies
-// (one scale for the whole token tensor), so this gives the bytes that quantising each
-// gathered row gives, with a sixth of the arithmetic and of the reads at top-6. One warp per
-// (token, 1024-value segment), as k_quant_fp8.
+// slot_row[t k + j] (E4M3 bytes [rows, K], rows ldo bytes apart). A token's codes are the
+// same in all its copies (one scale for the whole token tensor), so this gives the bytes that
+// quantising each gathered row gives, with a sixth of the arithmetic and of the reads at
+// top-6. One warp per (token, 1024-value segment), as k_quant_fp8.
 __global__ void k_quant_fp8_tokens(const uint16_t* __restrict__ src, long long ld, int T, int k,
                                    const int32_t* __restrict__ slot_row, long long rows, int K,
                                    const uint32_t* __restrict__ amax, uint8_t* __restrict__ out,
-                                   int* status) {
+                                   long long ldo, int* status) {
   griddep_wait();
   griddep_launch_dependents();
   const int nvec = K / 8;
@@ -129,7 +130,7 @@ __global__ void k_quant_fp8_tokens(const uint16_t* __restrict__ src, long long l
 #pragma unroll
     for (int m = 0; m < kFp8SegVec / 32; ++m) {
       const int v = seg * kFp8SegVec + m * 32 + lane;
-      if (v < nvec) *reinterpret_cast<uint2*>(out + r * K + static_cast<long long>(v) * 8) = code[m];
+      if (v < nvec) *reinterpret_cast<uint2*>(out + r * ldo + static_cast<long long>(v) * 8) = code[m];
     }
   }
 }
@@ -145,22 +146,22 @@ __global__ void k_finalize_fp8_scale(float* s, int G) {
 
 int launch_quant_fp8(const uint16_t* src, long long ld, const int32_t* row_map, long long rows,
                      int K, long long rows_per_scale, const uint32_t* amax, uint8_t* out,
-                     cudaStream_t s) {
+                     long long ldo, cudaStream_t s) {
   const long long n = rows * ((K / 8 + kFp8SegVec - 1) / kFp8SegVec) * 32;  // one warp per segment
   if (n <= 0) return MOE_OK;
   return launch_pdl(k_quant_fp8, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, s,
-                    src, ld, row_map, rows, K, rows_per_scale, amax, out);
+                    src, ld, row_map, rows, K, rows_per_scale, amax, out, ldo);
 }
 
 int launch_quant_fp8_tokens(const uint16_t* src, long long ld, int T, int k,
                             const int32_t* slot_row, long long rows, int K, const uint32_t* amax,
-                            uint8_t* out, cudaStream_t s) {
+                            uint8_t* out, long long ldo, cudaStream_t s) {
   if (T <= 0) return MOE_OK;
   int* status = status_word();
   if (!status) return MOE_ERR_CUDA;
   const long long n = static_cast<long long>(T) * ((K / 8 + kFp8SegVec - 1) / kFp8SegVec) * 32;
   return launch_pdl(k_quant_fp8_tokens, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
-                    s, src, ld, T, k, slot_row, rows, K, amax, out, status);
+                    s, src, ld, T, k, slot_row, rows, K, amax, out, ldo, status);
 }
 
 int launch_finalize_fp8_scale(float* s, int G, cudaStream_t stream) {

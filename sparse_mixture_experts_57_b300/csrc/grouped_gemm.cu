@@ -699,9 +699,10 @@ int launch_variant(const GroupedGemm& g, const KArgs& ka, cudaStream_t s) {
     const uint32_t ab[2] = {2 * BK, static_cast<uint32_t>(act_box)};
     if (!encode_tmap(&tm_act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.act, ad, as, ab))
       return MOE_ERR_CUDA;
+    const uint64_t wld = g.w_ld ? static_cast<uint64_t>(g.w_ld) : static_cast<uint64_t>(g.K);
     const uint64_t wd[3] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N),
                             static_cast<uint64_t>(g.E)};
-    const uint64_t ws[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N) * g.K};
+    const uint64_t ws[2] = {wld, static_cast<uint64_t>(g.N) * wld};
     const uint32_t wb[3] = {2 * BK, static_cast<uint32_t>(w_box), 1};
     if (!encode_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w, wd, ws, wb))
       return MOE_ERR_CUDA;
@@ -775,8 +776,10 @@ int launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
   if (g.K % BK || g.N % 16 || (g.k_wrap && (g.k_wrap % BK || g.K % g.k_wrap)) || g.E < 1 ||
       g.E > MAX_GROUPS)
     return MOE_ERR_UNSUPPORTED;
-  if (g.fp8 && (g.k_wrap || g.precise || !g.a_amax || !g.w_scale || g.act_ld % 16))
+  if (g.fp8 && (g.k_wrap || g.precise || !g.a_amax || !g.w_scale || g.act_ld % 16 ||
+                (g.w_ld && (g.w_ld < g.K || g.w_ld % 16))))
     return MOE_ERR_UNSUPPORTED;
+  if (!g.fp8 && g.w_ld) return MOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_ADD_BF16 && (!g.add || g.ld_add % 8 || g.precise)) return MOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_COMBINE_I64 &&
       (g.precise || g.fp8 || g.row_token || g.k_wrap || !g.offsets || !g.comb_token ||

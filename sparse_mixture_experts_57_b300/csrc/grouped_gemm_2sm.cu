@@ -417,10 +417,10 @@ int launch_grouped_gemm_2sm(const GroupedGemm& g, cudaStream_t s) {
     if (!encode_tmap(&tm_act, dt, 2, g.act, dims, strides, box)) return MOE_ERR_CUDA;
   }
   {
+    const uint64_t wld = g.w_ld ? static_cast<uint64_t>(g.w_ld) : static_cast<uint64_t>(g.K) * esz;
     const uint64_t dims[3] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.N),
                               static_cast<uint64_t>(E)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(g.K) * esz,
-                                 static_cast<uint64_t>(g.N) * g.K * esz};
+    const uint64_t strides[2] = {wld, static_cast<uint64_t>(g.N) * wld};
     const uint32_t box[3] = {box_k, 128, 1};
     if (!encode_tmap(&tm_w, dt, 3, g.w, dims, strides, box)) return MOE_ERR_CUDA;
   }

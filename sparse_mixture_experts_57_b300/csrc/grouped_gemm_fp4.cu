@@ -484,6 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   if (g.P <= 0) return MOE_OK;
   if (g.K % KSTEP || g.N % 32 || g.E < 1 || g.E > MAXG || g.P % BM || g.ldo % 8 ||
+      g.a_ld < g.K / 2 || g.a_ld % 16 ||
       (reinterpret_cast<uintptr_t>(g.out) & 15))
     return MOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_BF16 && g.epi != EPI_SQRELU_BF16) return MOE_ERR_UNSUPPORTED;
@@ -509,7 +510,7 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   CUtensorMap tm_a, tm_w;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(g.K / 2), static_cast<uint64_t>(g.P)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(g.K / 2)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(g.a_ld)};
     const uint32_t box[2] = {BKB, BM};
     if (!encode_tmap(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box))
       return MOE_ERR_CUDA;

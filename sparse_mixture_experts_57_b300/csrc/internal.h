@@ -165,6 +165,7 @@ struct GroupedGemm {
   const uint32_t* a_amax = nullptr;
   const float* w_scale = nullptr;
   uint32_t* out_amax = nullptr;
+  int64_t w_ld = 0;  // bytes between weight rows (0: Kw times the element size)
   // EPI_COMBINE_I64 only: row r belongs to token comb_token[r] (< comb_T); its gate is
   // comb_gates[t k + j] for the slot j with comb_slot_row[t k + j] == r (k = comb_k).
   const int32_t* comb_token = nullptr;
@@ -241,17 +242,36 @@ constexpr float kFp8Div = 448.0f;
 // of amax[r / rows_per_scale] (rows_per_scale = 0: one scale for all rows).
 int launch_quant_fp8(const uint16_t* src, long long ld, const int32_t* row_map, long long rows,
                      int K, long long rows_per_scale, const uint32_t* amax, uint8_t* out,
-                     cudaStream_t s);
+                     long long ldo, cudaStream_t s);
 // Routed tokens quantised once each and written to their k permuted rows slot_row[t k + j]
-// of out [rows, K]; the same bytes as launch_quant_fp8 with row_map = row_token.
+// of out [rows, K] (rows ldo bytes apart); the same bytes as launch_quant_fp8 with
+// row_map = row_token.
 int launch_quant_fp8_tokens(const uint16_t* src, long long ld, int T, int k,
                             const int32_t* slot_row, long long rows, int K, const uint32_t* amax,
-                            uint8_t* out, cudaStream_t s);
+                            uint8_t* out, long long ldo, cudaStream_t s);
+// Row pitch in bytes of the E4M3 tensors the grouped GEMMs read (activations and weight
+// codes): K rounded up to 128 bytes, so that every row's 128-byte K-slices start on a
+// 128-byte boundary.
+#ifdef __CUDACC__
+#define MOE_HD __host__ __device__
+#else
+#define MOE_HD
+#endif
+MOE_HD inline long long fp8_act_pitch(int K) {
+  return (static_cast<long long>(K) + 127) / 128 * 128;
+}
 // s[i] = amax[i] / 448 in place.
 int launch_finalize_fp8_scale(float* s, int G, cudaStream_t stream);
 
+// Row pitch in bytes of the NVFP4 activation codes the block-scaled GEMMs read: K/2 rounded
+// up to 128 bytes (the weight codes keep K/2).
+MOE_HD inline long long fp4_act_pitch(int K) {
+  return (static_cast<long long>(K / 2) + 127) / 128 * 128;
+}
+
 struct Fp4Gemm {
-  const uint8_t* a_codes;  // [P, K/2], rows padded per group (poff)
+  const uint8_t* a_codes;  // [P, K/2], rows a_ld bytes apart, padded per group (poff)
+  long long a_ld;
   const uint8_t* a_sf;     // atoms of the padded rows
   const uint32_t* a_amax;  // activation amax (fp32 bits); g_a = amax / 2688
   int P;                   // allocated padded rows (bound for poff[E])

@@ -12,7 +12,7 @@
 // fp32 evaluation of the same formulas exactly).
 //
 // Layouts (shared with the block-scaled grouped GEMM): codes [rows, K/2], element 2i in the
-// low nibble; scales as 512-byte atoms, one per (128-row block, 64-element K step): row
+// low nibble (weights: rows K/2 bytes apart; routed activations: fp4_act_pitch(K) apart); scales as 512-byte atoms, one per (128-row block, 64-element K step): row
 // 128 rb + 32 r1 + r0, block kb of the step at byte r0 * 16 + r1 * 4 + kb. One thread
 // quantises one row's 64-element K step: 128 bytes in, 32 code bytes and one 32-bit word of
 // four scales out (for routed activations the warp loads its 32 steps cooperatively).
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
   __syncwarp();
   if (!valid) return;
   uint32_t* word = sf_word(sf, p, j, KS);
-  uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + j * 32);
+  uint4* dst = reinterpret_cast<uint4*>(codes + p * fp4_act_pitch(K) + j * 32);
   if (srow < 0) {  // padding row of a segment
     *word = 0u;
     dst[0] = make_uint4(0u, 0u, 0u, 0u);
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
       continue;
     }
     *sf_word(sf, p, j, KS) = word;
-    uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + j * 32);
+    uint4* dst = reinterpret_cast<uint4*>(codes + p * fp4_act_pitch(K) + j * 32);
     dst[0] = out[0];
     dst[1] = out[1];
   }
@@ -450,7 +450,7 @@ __global__ void k_zero_padding_rows(const int32_t* __restrict__ offsets,
     const long long p = p0 + q / KS;
     const int j = static_cast<int>(q % KS);
     *sf_word(sf, p, j, KS) = 0u;
-    uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + j * 32);
+    uint4* dst = reinterpret_cast<uint4*>(codes + p * fp4_act_pitch(K) + j * 32);
     dst[0] = make_uint4(0u, 0u, 0u, 0u);
     dst[1] = make_uint4(0u, 0u, 0u, 0u);
   }

@@ -14,6 +14,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "scan.cuh"
@@ -673,6 +674,32 @@ __global__ void k_gather_rows(const int32_t* __restrict__ row_token, const uint1
   for (int v = lane; v < H / 8; v += 32) dst[v] = __ldg(src + v);
 }
 
+// Launch set-up state per kernel and device. Kernels of one signature share one
+// instantiation of a generic lambda, so this state cannot live in the lambda's statics: it
+// is kept per kernel address.
+struct KernelSetup {
+  const void* fn = nullptr;
+  int dev = -1;
+  int usable = 0;
+};
+
+KernelSetup& kernel_setup(const void* fn) {
+  constexpr int kSlots = 64;  // this file launches fewer than 20 kernels
+  static std::mutex m;
+  static KernelSetup table[kSlots];
+  static int n = 0;
+  std::lock_guard<std::mutex> lock(m);
+  for (int i = 0; i < n; ++i)
+    if (table[i].fn == fn) return table[i];
+  if (n == kSlots) {  // not reached; a fresh state means the kernel is set up again
+    static KernelSetup spare;
+    spare = KernelSetup{fn, -1, 0};
+    return spare;
+  }
+  table[n].fn = fn;
+  return table[n++];
+}
+
 }  // namespace
 
 int launch_router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_router, int T, int D,
@@ -682,13 +709,13 @@ int launch_router_logits(const uint16_t* x, int64_t ldx, const uint16_t* w_route
     const dim3 grid((T + kSmallTok - 1) / kSmallTok, (E + kSmallExp - 1) / kSmallExp);
     const size_t smem = static_cast<size_t>(kSmallTok) * parts * D * 2;
     auto go = [&](auto kern) -> int {
-      static int configured_device = -1;
+      KernelSetup& su = kernel_setup(reinterpret_cast<const void*>(kern));
       int dev = 0;
       MOE_CUDA(cudaGetDevice(&dev));
-      if (configured_device != dev) {
+      if (su.dev != dev) {
         MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kSmallTok * kSmallMaxElems * 2));
-        configured_device = dev;
+        su.dev = dev;
       }
       return launch_pdl(kern, grid, dim3(32 * kSmallExp), smem, s, x,
                         static_cast<long long>(ldx), w_router, T, D, E, logits);
@@ -750,13 +777,13 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
                                static_cast<size_t>(W) * E * 8);
   const int perm = row_token != nullptr;
   auto go = [&](auto kern) -> int {
-    static int configured_device = -1;
+    KernelSetup& su = kernel_setup(reinterpret_cast<const void*>(kern));
     int dev = 0;
     MOE_CUDA(cudaGetDevice(&dev));
-    if (configured_device != dev) {
+    if (su.dev != dev) {
       MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kSmallTok * kSmallMaxElems * 2));
-      configured_device = dev;
+      su.dev = dev;
     }
     return launch_pdl(kern, grid, dim3(256), smem, s, x, static_cast<long long>(ldx), w_router,
                       bias, T, D, E, k, logits, idx, gates, tie, perm, counts, offsets,
@@ -767,7 +794,7 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
   // than 8 is a non-portable cluster size). Returns 1 when it cannot run here (the caller
   // then launches k_route_small).
   auto go_cluster = [&](auto kern) -> int {
-    static int ready_device = -1, usable = 0;
+    KernelSetup& su = kernel_setup(reinterpret_cast<const void*>(kern));
     int dev = 0;
     MOE_CUDA(cudaGetDevice(&dev));
     cudaLaunchConfig_t cfg{};
@@ -784,7 +811,7 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (ready_device != dev) {
+    if (su.dev != dev) {
       MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kSmallTok * kSmallMaxElems * 2));
       MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
@@ -796,11 +823,11 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
       probe.dynamicSmemBytes = kSmallTok * kSmallMaxElems * 2;
       probe.attrs = &pattr;
       int n = 0;
-      usable = cudaOccupancyMaxActiveClusters(&n, kern, &probe) == cudaSuccess && n > 0;
+      su.usable = cudaOccupancyMaxActiveClusters(&n, kern, &probe) == cudaSuccess && n > 0;
       cudaGetLastError();  // a refused query is not an error of this call
-      ready_device = dev;
+      su.dev = dev;
     }
-    if (!usable) return 1;
+    if (!su.usable) return 1;
     cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, x, static_cast<long long>(ldx),
                                              w_router, bias, T, D, E, k, idx, gates, tie, perm,
@@ -811,7 +838,7 @@ int launch_route_fused(const uint16_t* x, int64_t ldx, const uint16_t* w_router,
     // a configuration this device refuses (nothing was launched): use k_route_small from now
     cluster_launch_error() = static_cast<int>(e);
     cudaGetLastError();
-    usable = 0;
+    su.usable = 0;
     return 1;
   };
   if (E <= kClusterMaxE && ldx % 8 == 0 && aligned16(x)) {

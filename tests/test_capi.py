@@ -116,15 +116,17 @@ def test_quant_views_are_disjoint_slices_of_the_workspace(call, dims, size_fn):
         sf = lambda K: (P + 127) // 128 * (K // 64) * 512  # noqa: E731
     else:
         assert P == rows
-    ext = {"amax": 8, "x_codes": P * H // (2 if nvfp4 else 1), "h": P * F * 2,
-           "h_codes": P * F // (2 if nvfp4 else 1)}
+    # code rows (NVFP4: two codes per byte) are padded to 128-byte pitches
+    c = 2 if nvfp4 else 1
+    assert (v.x_codes_ld, v.h_codes_ld) == (-(-H // c // 128) * 128, -(-F // c // 128) * 128)
+    ext = {"amax": 8, "x_codes": P * v.x_codes_ld, "h": P * F * 2, "h_codes": P * v.h_codes_ld}
     if nvfp4:
         ext.update(padded_offsets=(E + 1) * 4, x_scales=sf(H), h_scales=sf(F))
     if fwd:
         ext.update(offsets=(E + 1) * 4, row_token=rows * 4)
     spans = []
     for name, _ in QuantView._fields_:
-        if name == "buffer_rows":
+        if name in ("buffer_rows", "x_codes_ld", "h_codes_ld"):
             continue
         p = getattr(v, name)
         if name not in ext:

@@ -79,10 +79,12 @@ def _amax_bits(bits) -> int:
 
 # --------------------------------------------------------------------------- NVFP4 ----
 
-def _check_nvfp4_rows(codes_buf, sf_buf, P, K, poff, counts, src_rows, g_ref, what):
+def _check_nvfp4_rows(codes_buf, ld, sf_buf, P, K, poff, counts, src_rows, g_ref, what):
     """Every real row of the padded buffers equals the oracle's quantisation of its source
-    row with the tensor's global scale; padding rows hold zero codes and scales."""
-    codes = codes_buf.reshape(P, K // 2)
+    row with the tensor's global scale; padding rows hold zero codes and scales. Code rows
+    are ld bytes apart (K/2 rounded up to 128)."""
+    assert ld % 128 == 0 and K // 2 <= ld < K // 2 + 128
+    codes = codes_buf.reshape(P, ld)[:, :K // 2]
     sf = scale_rows(sf_buf, P, K)
     live = np.zeros(P, bool)
     for e, c in enumerate(counts):
@@ -112,7 +114,8 @@ def _check_nvfp4_view(view, ws, counts, H, F, src_rows, x_amax_src, wu):
     # routed tokens
     assert int(amax[0]) == _amax_bits(x_amax_src), "amax of the token tensor"
     gx = O.nvfp4_global_scale(np.max(np.abs(O.widen_bf16(x_amax_src))))
-    live = _check_nvfp4_rows(_slice(ws, view["x_codes"], P * H // 2),
+    ldx, ldh = view["x_codes_ld"], view["h_codes_ld"]
+    live = _check_nvfp4_rows(_slice(ws, view["x_codes"], P * ldx), ldx,
                              _slice(ws, view["x_scales"], moe_nvfp4_sf_bytes(P, H)), P, H, poff,
                              counts, src_rows, gx, "routed tokens")
     # hidden activations: the stored bf16 h, its amax and its quantisation
@@ -122,7 +125,7 @@ def _check_nvfp4_view(view, ws, counts, H, F, src_rows, x_amax_src, wu):
     h_live = h[live]
     assert int(amax[1]) == _amax_bits(h_live), "amax of h"
     gh = O.nvfp4_global_scale(np.max(np.abs(O.widen_bf16(h_live))))
-    _check_nvfp4_rows(_slice(ws, view["h_codes"], P * F // 2),
+    _check_nvfp4_rows(_slice(ws, view["h_codes"], P * ldh), ldh,
                       _slice(ws, view["h_scales"], moe_nvfp4_sf_bytes(P, F)), P, F, poff,
                       counts, h_live, gh, "hidden activations")
     # h itself: squared ReLU of the product of the dequantised operands (bf16 rounding)
@@ -216,13 +219,15 @@ def _check_fp8_view(ws, view, rows, H, F, src_rows, x_amax_src, wu, off):
     assert view["buffer_rows"] == rows
     assert int(amax[0]) == _amax_bits(x_amax_src), "amax of the token tensor"
     sx = O.fp8_scale(np.max(np.abs(O.widen_bf16(x_amax_src))))
-    xq = _slice(ws, view["x_codes"], rows * H).reshape(rows, H)
+    ldx, ldh = view["x_codes_ld"], view["h_codes_ld"]
+    assert ldx % 128 == 0 and ldh % 128 == 0 and ldx >= H and ldh >= F
+    xq = _slice(ws, view["x_codes"], rows * ldx).reshape(rows, ldx)[:, :H]
     ref = O.fp8_quantize(src_rows, sx)
     np.testing.assert_array_equal(decode_e4m3(xq), ref["q"], err_msg="routed tokens: E4M3")
     h = _slice(ws, view["h"], rows * F, np.uint16).reshape(rows, F)
     assert int(amax[1]) == _amax_bits(h), "amax of h"
     sh = O.fp8_scale(np.max(np.abs(O.widen_bf16(h))))
-    hq = _slice(ws, view["h_codes"], rows * F).reshape(rows, F)
+    hq = _slice(ws, view["h_codes"], rows * ldh).reshape(rows, ldh)[:, :F]
     np.testing.assert_array_equal(decode_e4m3(hq), O.fp8_quantize(h, sh)["q"],
                                   err_msg="hidden activations: E4M3")
     href = np.zeros((rows, F))
