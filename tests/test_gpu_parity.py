@@ -216,10 +216,14 @@ def test_grouped_ffn(moe, T, E, k, H, F, skew):
 
 
 @pytest.mark.parametrize("counts,H,F", [
-    # >= 256 rows per group on average: 256-row CTA-pair tiles whose last tile per group holds
-    # 44, 1, 88, 128 or 129 rows (300, 1, 600, 384, 385), or none (512)
-    ([300, 0, 1, 600, 384, 385, 512], 320, 448),
+    # >= 512 rows per group on average: 256-row CTA-pair tiles whose last tile per group holds
+    # 132, 1, 188, 0 (768), 1 (769) or 0 (1024) rows
+    ([900, 0, 1, 700, 768, 769, 1024], 320, 448),
     ([1500, 700, 300, 129], 2688, 1856),       # Nano widths
+    # 256 to 512 rows per group on average: last tiles of 44, 1, 88, 128, 129 and 0 rows
+    # (300, 1, 600, 384, 385, 512), and of 1, 255, 0, 1 and 128 rows (257, 511, 512, 513, 384)
+    ([300, 0, 1, 600, 384, 385, 512], 320, 448),
+    ([256, 257, 511, 512, 513, 1, 0, 384], 320, 448),
 ])
 def test_grouped_ffn_pair_partial_tiles(moe, counts, H, F):
     E = len(counts)
