@@ -141,10 +141,12 @@ def kernels_per_step(w: moe_synth.Workload, gathered: bool = False,
     fused = T <= 256 and E <= 256 and d_route <= 6144 and k <= 32
     words = (T + 31) // 32
     perm = 1 if (words <= 64 and words * E <= 8192) else 3
-    if w.nvfp4:   # route (1 or 2 + perm), amax x, pad, quantise x, zero the padding rows, up,
-        return (1 if fused else 2 + perm) + 8   # quantise h, down, combine
-    if w.fp8:     # route (1 or 2 + perm), amax x, quantise x, up, quantise h, down, combine
-        return (1 if fused else 2 + perm) + 6
+    # routing: one fused kernel, or logits, top-k, the permutation and its map writer
+    route_q = 1 if fused else 2 + perm + 1
+    if w.nvfp4:   # routing, amax x, pad, quantise x, zero the padding rows, up,
+        return route_q + 8   # quantise h, down, combine
+    if w.fp8:     # routing, amax x, quantise x, up, quantise h, down, combine
+        return route_q + 6
     gather_in_gemm = gathered
     if fused:
         route = 1 if gather_in_gemm else 2     # + the row copy
