@@ -65,6 +65,7 @@ def _route_case(moe, T, D, E, k, seed, bias_kind="uniform"):
                                gates_by_expert(ref["idx"], ref["gates"])[same],
                                rtol=1e-4, atol=1e-6)
     np.testing.assert_allclose(g.sum(axis=1), 1.0, atol=1e-6)
+    _check_tie_flags(tie, ref)
     _status_ok(moe)
     return int((ref["gap"] < 1e-5).sum())
 
@@ -104,7 +105,19 @@ def test_route_dispatch(moe, T, D, E, k):
         np.testing.assert_array_equal(p[key].cpu().numpy(), pref[key], err_msg=key)
     np.testing.assert_array_equal(moe_synth.from_torch_bf16(p["x_perm"]),
                                   inp["x"][pref["row_token"]])
-    assert (tie.cpu().numpy() == (ref["gap"] < 1e-5)).mean() > 0.99
+    _check_tie_flags(tie, ref)
+
+
+def _check_tie_flags(tie, ref):
+    """The tie flag (the GPU's fp32 gap u_(k) - u_(k+1) below 1e-5) must equal the oracle's
+    flag for every token whose fp64 gap is not within the GPU's error of the threshold: the
+    logits carry up to about 1e-5 absolute error, so u = sigmoid(z) + b about 2.5e-6 and the
+    gap about 5e-6. Tokens inside that band may go either way."""
+    got = tie.cpu().numpy().astype(bool)
+    want = ref["gap"] < 1e-5
+    firm = np.abs(ref["gap"] - 1e-5) > 5e-6
+    bad = np.nonzero(got[firm] != want[firm])[0]
+    assert bad.size == 0, f"{bad.size} tie flags differ outside the error band"
 
 
 def test_route_nano_prefill_full(moe):
