@@ -9,31 +9,37 @@
 // for the rows r of group e. Activation rows are laid out with every group padded to whole
 // 128-row tiles, so each row tile starts on a scale-atom boundary.
 //
-// One CTA per SM, 448 threads:
-//   warp 0 lane 0  TMA producer: per stage 256 K-elements (128 bytes) of 128 activation rows
-//                  and 256 weight rows (128-byte swizzle), plus the matching scale atoms
-//                  (untiled bulk copies).
+// One CTA per SM, 448 threads, tiles of 256 activation rows (two 128-row halves) by 192
+// output columns:
+//   warp 0 lane 0  TMA producer: per stage 256 K-elements (128 bytes) of the two 128-row
+//                  activation halves and of 192 weight rows (128-byte swizzle), plus the
+//                  matching scale atoms (untiled bulk copies).
 //   warps 10..13   scale writers, one per TMEM lane quadrant: read the stage's scale atoms
-//                  from shared memory and write them into a ring of TMEM scale columns
-//                  (tcgen05.st), in the layout the block-scaled MMA reads (see below).
-//   warp 1 lane 0  MMA issuer: tcgen05.mma kind::mxf4nvf4 (M=128, N=256, K=64) with block
-//                  scales into one fp32 accumulator of 256 TMEM columns.
-//   warps 2..9     epilogue, two warps per lane quadrant (128 columns each): tcgen05.ld of
-//                  the accumulator into registers (global scales, activation, packed to
-//                  bf16), then the accumulator is released to the next tile's MMAs before
-//                  the stores go out. A warp's 32-row band goes out as 32x32 pieces staged in
+//                  from shared memory and write them into a two-slot ring of TMEM scale
+//                  columns (tcgen05.st), in the layout the block-scaled MMA reads (see below).
+//   warp 1 lane 0  MMA issuer: per K step two tcgen05.mma kind::mxf4nvf4 (M=128, N=192,
+//                  K=64) with block scales, one per activation half, both on the same weight
+//                  tile, into two fp32 accumulators of 192 TMEM columns.
+//   warps 2..9     epilogue, one warp per (accumulator, lane quadrant): tcgen05.ld of its
+//                  192 columns into registers (global scales, activation, packed to bf16),
+//                  then the accumulators are released to the next tile's MMAs before the
+//                  stores go out. A warp's 32-row band goes out as 32x16 pieces staged in
 //                  swizzled shared memory and written by TMA stores; only the partial last
 //                  band of an expert is stored row by row.
 //
-// Why N = 256: with block-scaled FP4 MMAs the tensor cores consume operand bytes from shared
-// memory 4x faster than with bf16, and the TMA must write the same bytes into shared memory.
-// An M=128, N=256 tile moves 12 KB per 2M MACs where N = 128 moves 8 KB per 1M.
+// Why two accumulators on one weight tile: with block-scaled FP4 MMAs the tensor cores
+// consume operand bytes 4x faster than with bf16, and every byte must first be written into
+// shared memory by the TMA, whose delivery into one SM (not the L2's output) is the limit.
+// A tile of M x N outputs moves 32 (M + N) bytes per 64-element K step for M N / 16384
+// cycles of MMA work: 96 bytes per MMA cycle at 128 x 256, 75 at 256 x 192.
 //
-// Scale columns read by one MMA with scale addresses (a, b): A row m at lane m, column
-// a + m / 32; B row n at lane 32 q + n % 32, column b + n / 32, for the lane quadrant q
-// of every output row block (so the B scales are written to all four quadrants). MMA j of
-// a stage uses a = A0 + 4 j and b = B0 + 8 j (addresses on 4-column boundaries): per stage
-// 16 A columns (each lane writes the one column of its quadrant per MMA) and 32 B columns.
+// TMEM (512 columns): accumulator 0 in [0, 192), scale slot 0 in [192, 256), accumulator 1
+// in [256, 448), scale slot 1 in [448, 512). Scale columns read by one MMA with scale
+// addresses (a, b): A row m at lane m, column a + m / 32; B row n at lane 32 q + n % 32,
+// column b + n / 32, for the lane quadrant q of every output row block (so the B scales are
+// written to all four quadrants). MMA j of a stage reads, in its slot, the A scales of half h
+// at +16 h + 4 j and the B scales at +32 + 8 j (addresses on 4-column boundaries). The slot
+// of stage i is i mod 2: its scale writers wait until the MMAs of stage i - 2 have completed.
 // Writing the scales with warp stores keeps the tensor pipe's own queue free of copies.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,8 +50,9 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;         // rows of one activation half (one MMA's M)
+constexpr int BM2 = 2 * BM;     // activation rows of a tile
+constexpr int BN = 192;
 constexpr int BKB = 128;        // K bytes per stage and row: 256 E2M1 elements
 constexpr int KSTEP = 64;       // K elements per MMA
 constexpr int STEPS_PER_STAGE = 4;
@@ -53,18 +60,22 @@ constexpr int STAGES = 3;
 constexpr int MAXG = 1024;
 constexpr int NUM_THREADS = 448;
 constexpr int EPI_WARP0 = 2, SFW_WARP0 = 10;
-constexpr uint32_t A_BYTES = BM * BKB;
+constexpr uint32_t A_HALF = BM * BKB;
+constexpr uint32_t A_BYTES = 2 * A_HALF;
 constexpr uint32_t B_BYTES = BN * BKB;
 constexpr uint32_t ATOM = 512;
-constexpr uint32_t SFA_STAGE = STEPS_PER_STAGE * ATOM;      // one 128-row block, 4 K steps
-constexpr uint32_t SFB_STAGE = 2 * STEPS_PER_STAGE * ATOM;  // two 128-row blocks
+constexpr uint32_t SF_ONE = STEPS_PER_STAGE * ATOM;  // one 128-row block, 4 K steps
+constexpr uint32_t SFA_STAGE = 2 * SF_ONE;           // the two activation halves
+constexpr uint32_t SFB_STAGE = 2 * SF_ONE;           // the two 128-row weight blocks touched
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SF_COL0 = BN;                 // accumulator in columns [0, 256)
-constexpr uint32_t SF_COLS_PER_STAGE = 64;       // A at +0 (16 columns), B at +32 (32)
-constexpr uint32_t STG_BYTES = 2048;             // one 32 x 32 bf16 output piece
-constexpr int NUM_EPI_WARPS = 8;
+constexpr uint32_t ACC_STRIDE = 256;  // accumulator h at column 256 h
+constexpr uint32_t SF_COL0 = BN;      // scale slot s at column 192 + 256 s
 constexpr uint32_t SF_B_OFF = 32;
-static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+constexpr uint32_t STG_BYTES = 1024;  // one 32 x 16 bf16 output piece
+constexpr int NUM_EPI_WARPS = 8;
+static_assert(SF_COL0 + 64 <= ACC_STRIDE && ACC_STRIDE + SF_COL0 + 64 <= TMEM_COLS,
+              "TMEM budget");
+static_assert(BN % 64 == 0 && BN <= 256, "weight tiles start on 64-row boundaries");
 constexpr uint32_t IDESC = idesc_nvfp4_f32(BM, BN);
 
 struct KArgs {
@@ -105,12 +116,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sB = sA + STAGES * A_BYTES;
   uint8_t* sSFA = sB + STAGES * B_BYTES;
   uint8_t* sSFB = sSFA + STAGES * SFA_STAGE;
-  uint8_t* sStage = sSFB + STAGES * SFB_STAGE;  // per epilogue warp: two 2 KB pieces
+  uint8_t* sStage = sSFB + STAGES * SFB_STAGE;  // per epilogue warp: two 1 KB pieces
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + NUM_EPI_WARPS * 2 * STG_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* sfull = empty + STAGES;  // the stage's scales are in TMEM
-  uint64_t* tfull = sfull + STAGES;  // the accumulator holds a finished tile
-  uint64_t* tempty = tfull + 1;      // the epilogue has read the accumulator
+  uint64_t* tfull = sfull + STAGES;  // the accumulators hold a finished tile
+  uint64_t* tempty = tfull + 1;      // the epilogue has read the accumulators
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_pref = reinterpret_cast<int*>(tmem_slot + 4);  // row-tile prefix per group
@@ -141,15 +152,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   griddep_wait();
   griddep_launch_dependents();
   if (warp == 2) {
-    // Row-tile prefix over the groups' padded segments (whole 128-row tiles). A group whose
-    // offsets are inconsistent is reported and gets no tiles, so no role ever reads it.
+    // Row-tile prefix over the groups' padded segments (whole 128-row blocks, 256-row
+    // tiles). A group whose offsets are inconsistent is reported and gets no tiles, so no
+    // role ever reads it.
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
     int local = 0;
     bool bad = false;
     for (int e = e0; e < e1; ++e) {
       const int lo = a.poff[e], hi = a.poff[e + 1];
-      int tiles = (hi - lo) / BM;
+      int tiles = (hi - lo + BM2 - 1) / BM2;
       if (lo < 0 || hi < lo || hi > a.P || ((lo | hi) & (BM - 1))) {
         bad = true;
         tiles = 0;
@@ -206,6 +218,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     e = lo;
     rt = rtg - s_pref[lo];
   };
+  // Whether the tile's second activation half lies inside the group's padded segment.
+  auto second_half = [&](int e, int rt) {
+    return rt * BM2 + BM < __ldg(a.poff + e + 1) - __ldg(a.poff + e);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -218,12 +234,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, rt, ct;
         decode(tile, e, rt, ct);
-        const int row0 = __ldg(a.poff + e) + rt * BM;
+        const int row0 = __ldg(a.poff + e) + rt * BM2;
+        const bool two_a = second_half(e, rt);
         const int col0 = ct * BN;
-        const bool two = 2 * ct + 1 < nbw;  // the tile's second 128-row weight block exists
+        const int wb0 = col0 / 128;         // first weight scale row block of the tile
+        const bool two_b = wb0 + 1 < nbw;   // the second one exists
         const uint8_t* sfa = a.a_sf + (static_cast<long long>(row0 / BM) * KS) * ATOM;
-        const uint8_t* sfw =
-            a.w_sf + ((static_cast<long long>(e) * nbw + 2 * ct) * KS) * ATOM;
+        const uint8_t* sfw = a.w_sf + ((static_cast<long long>(e) * nbw + wb0) * KS) * ATOM;
+        const long long next_block = static_cast<long long>(KS) * ATOM;
         for (int kb = 0; kb < NST; ++kb) {
           const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -231,16 +249,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           const uint32_t sf_bytes = nsteps * ATOM;
-          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + (two ? 3u : 2u) * sf_bytes);
+          const uint32_t halves = two_a ? 2u : 1u, wblocks = two_b ? 2u : 1u;
+          mbar_arrive_expect_tx(&full[stage],
+                                halves * A_HALF + B_BYTES + (halves + wblocks) * sf_bytes);
           ++armed;
-          tma_load_2d(sA + stage * A_BYTES, &tm_a, &full[stage], kb * BKB, row0, pol);
+          uint8_t* dA = sA + stage * A_BYTES;
+          tma_load_2d(dA, &tm_a, &full[stage], kb * BKB, row0, pol);
+          if (two_a) tma_load_2d(dA + A_HALF, &tm_a, &full[stage], kb * BKB, row0 + BM, pol);
           tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kb * BKB, col0, e, pol);
           const long long so = static_cast<long long>(kb) * STEPS_PER_STAGE * ATOM;
           bulk_load(sSFA + stage * SFA_STAGE, sfa + so, sf_bytes, &full[stage], pol);
+          if (two_a)
+            bulk_load(sSFA + stage * SFA_STAGE + SF_ONE, sfa + next_block + so, sf_bytes,
+                      &full[stage], pol);
           bulk_load(sSFB + stage * SFB_STAGE, sfw + so, sf_bytes, &full[stage], pol);
-          if (two)
-            bulk_load(sSFB + stage * SFB_STAGE + SFA_STAGE, sfw + static_cast<long long>(KS) * ATOM + so,
-                      sf_bytes, &full[stage], pol);
+          if (two_b)
+            bulk_load(sSFB + stage * SFB_STAGE + SF_ONE, sfw + next_block + so, sf_bytes,
+                      &full[stage], pol);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -259,8 +284,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
+      uint32_t slot = 0;  // scale slot of the stage: the stage count mod 2
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int e, rt, ct;
+        decode(tile, e, rt, ct);
+        const bool two_a = second_half(e, rt);
         if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -274,14 +303,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_col = SF_COL0 + stage * SF_COLS_PER_STAGE;
-          const uint32_t sfb_col = sfa_col + SF_B_OFF;
+          const uint32_t sf = tmem_base + SF_COL0 + slot * ACC_STRIDE;
           const uint64_t adesc = sdesc_k_sw128(smem_u32(sA + stage * A_BYTES));
+          const uint64_t adesc1 = sdesc_k_sw128(smem_u32(sA + stage * A_BYTES + A_HALF));
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(sB + stage * B_BYTES));
-          for (int j = 0; j < nsteps; ++j)
-            umma_nvfp4(tmem_base, adesc + 2u * j, bdesc + 2u * j, IDESC,
-                       tmem_base + sfa_col + 4 * j, tmem_base + sfb_col + 8 * j, (kb | j) != 0);
+          for (int j = 0; j < nsteps; ++j) {
+            const uint32_t acc = (kb | j) != 0;
+            umma_nvfp4(tmem_base, adesc + 2u * j, bdesc + 2u * j, IDESC, sf + 4 * j,
+                       sf + SF_B_OFF + 8 * j, acc);
+            if (two_a)
+              umma_nvfp4(tmem_base + ACC_STRIDE, adesc1 + 2u * j, bdesc + 2u * j, IDESC,
+                         sf + 16 + 4 * j, sf + SF_B_OFF + 8 * j, acc);
+          }
           umma_commit(&empty[stage]);
+          slot ^= 1u;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -299,53 +334,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= SFW_WARP0) {
     // -------------------------------------------------------------------- scale writers
     // Quadrant q of TMEM, lane r0 = this lane. The smem atoms hold row 32 r1 + r0 of step j
-    // at byte j * 512 + r0 * 16 + r1 * 4 (four E4M3 scales, one per 16 K elements); the B
-    // stage holds the tile's first 128 weight rows, then the second.
+    // at byte j * 512 + r0 * 16 + r1 * 4 (four E4M3 scales, one per 16 K elements). The A
+    // stage holds the first activation half's atoms, then the second's; the B stage the
+    // atoms of weight row blocks wb0 and wb0 + 1, of which the tile's 192 rows start at row
+    // 0 or 64 of the first.
     const int q = warp & 3;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int stage = 0;
     uint32_t phase = 0;
+    int it = 0;  // stages so far: the scale slot is it mod 2
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       int e, rt, ct;
       decode(tile, e, rt, ct);
-      const bool two = 2 * ct + 1 < nbw;
-      for (int kb = 0; kb < NST; ++kb) {
+      const bool two_a = second_half(e, rt);
+      const int col0 = ct * BN;
+      const bool two_b = col0 / 128 + 1 < nbw;
+      const bool mid = (col0 & 127) != 0;  // the tile starts at row 64 of its first block
+      for (int kb = 0; kb < NST; ++kb, ++it) {
         const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
         if (!mbar_wait(&full[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
+        // The slot was last read by the MMAs of stage it - 2 (committed to empty[] of that
+        // stage, whose completion parity is its use count mod 2).
+        if (it >= 2 && !mbar_wait(&empty[(it - 2) % STAGES], ((it - 2) / STAGES) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         const uint8_t* sa = sSFA + stage * SFA_STAGE;
         const uint8_t* sb = sSFB + stage * SFB_STAGE;
-        uint32_t wa[STEPS_PER_STAGE];
+        uint32_t wa0[STEPS_PER_STAGE], wa1[STEPS_PER_STAGE];
         uint32_t wb[2][16];
 #pragma unroll
         for (int j = 0; j < STEPS_PER_STAGE; ++j) {
           uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-          wa[j] = 0u;
+          wa0[j] = 0u;
+          wa1[j] = 0u;
           if (j < nsteps) {
-            wa[j] = *reinterpret_cast<const uint32_t*>(sa + j * ATOM + lane * 16 + q * 4);
+            wa0[j] = *reinterpret_cast<const uint32_t*>(sa + j * ATOM + lane * 16 + q * 4);
+            if (two_a)
+              wa1[j] = *reinterpret_cast<const uint32_t*>(sa + SF_ONE + j * ATOM + lane * 16 + q * 4);
             v0 = *reinterpret_cast<const uint4*>(sb + j * ATOM + lane * 16);
-            if (two) v1 = *reinterpret_cast<const uint4*>(sb + SFA_STAGE + j * ATOM + lane * 16);
+            if (two_b) v1 = *reinterpret_cast<const uint4*>(sb + SF_ONE + j * ATOM + lane * 16);
           }
+          // column c of MMA j: weight row 32 c + lane of the tile
           uint32_t* w = wb[j >> 1] + 8 * (j & 1);
-          w[0] = v0.x;
-          w[1] = v0.y;
-          w[2] = v0.z;
-          w[3] = v0.w;
-          w[4] = v1.x;
-          w[5] = v1.y;
-          w[6] = v1.z;
-          w[7] = v1.w;
+          w[0] = mid ? v0.z : v0.x;
+          w[1] = mid ? v0.w : v0.y;
+          w[2] = mid ? v1.x : v0.z;
+          w[3] = mid ? v1.y : v0.w;
+          w[4] = mid ? v1.z : v1.x;
+          w[5] = mid ? v1.w : v1.y;
+          w[6] = 0u;
+          w[7] = 0u;
         }
-        // The ring slot of this stage was last read by MMAs that completed before the
-        // stage's smem was refilled, i.e. before full[stage] fired for this phase.
-        const uint32_t sfa_col = SF_COL0 + stage * SF_COLS_PER_STAGE;  // 64-column aligned
+        const uint32_t sf = SF_COL0 + static_cast<uint32_t>(it & 1) * ACC_STRIDE;
 #pragma unroll
-        for (int j = 0; j < STEPS_PER_STAGE; ++j) tmem_st1(lane_base + sfa_col + 4 * j + q, wa[j]);
-        tmem_st16(lane_base + sfa_col + SF_B_OFF, wb[0]);
-        tmem_st16(lane_base + sfa_col + SF_B_OFF + 16, wb[1]);
+        for (int j = 0; j < STEPS_PER_STAGE; ++j) {
+          tmem_st1(lane_base + sf + 4 * j + q, wa0[j]);
+          tmem_st1(lane_base + sf + 16 + 4 * j + q, wa1[j]);
+        }
+        tmem_st16(lane_base + sf + SF_B_OFF, wb[0]);
+        tmem_st16(lane_base + sf + SF_B_OFF + 16, wb[1]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -363,17 +415,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    const int half = (warp - EPI_WARP0) >> 2;  // columns [128 half, 128 half + 128)
+    const int h = (warp - EPI_WARP0) >> 2;  // accumulator: rows [128 h, 128 h + 128) of the tile
     const int m = q * 32 + lane;
     const float ga = __fdiv_rn(__uint_as_float(*a.a_amax), kNvfp4GlobalDiv);
-    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + 128 * half;
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ACC_STRIDE * h;
     uint8_t* stg = sStage + (warp - EPI_WARP0) * 2 * STG_BYTES;
     float vmax = 0.f;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, rt, ct;
       decode(tile, e, rt, ct);
-      const int local = rt * BM + m;
+      const int local = rt * BM2 + h * BM + m;
       int ocnt, obase;
       if (a.out_off) {
         obase = __ldg(a.out_off + e);
@@ -384,8 +436,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const bool valid = local < ocnt;
       const long long row = static_cast<long long>(obase) + local;
-      const int c0 = ct * BN + 128 * half;           // first column of this warp
-      const int ncols = max(0, min(128, a.N - c0));  // warp-uniform, a multiple of 16
+      const int c0 = ct * BN;                       // first column of the tile
+      const int ncols = max(0, min(BN, a.N - c0));  // warp-uniform, a multiple of 32
       const float scale = ga * __ldg(a.w_gscale + e);
       if (!mbar_wait(tfull, acc_phase, abort_flag)) {
         *abort_flag = 1;
@@ -393,58 +445,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      uint32_t p[64];  // this row's 128 outputs, packed bf16 pairs
+      uint32_t p[BN / 2];  // this row's outputs, packed bf16 pairs
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (32 * c < ncols) {
-          uint32_t r0[16], r1[16];
-          tmem_ld16(tb + 32 * c, r0);
-          tmem_ld16(tb + 32 * c + 16, r1);
+      for (int c = 0; c < BN / 16; ++c) {
+        if (16 * c < ncols) {
+          uint32_t r[16];
+          tmem_ld16(tb + 16 * c, r);
           tmem_ld_wait();
-          float v[32];
+          float v[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            v[i] = __uint_as_float(r0[i]) * scale;
-            v[16 + i] = __uint_as_float(r1[i]) * scale;
-          }
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * scale;
           if (a.epi == EPI_SQRELU_BF16) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               const float t = fmaxf(v[i], 0.f);
               v[i] = t * t;
             }
             if (valid) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) vmax = fmaxf(vmax, v[i]);
+              for (int i = 0; i < 16; ++i) vmax = fmaxf(vmax, v[i]);
             }
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) p[16 * c + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+          for (int i = 0; i < 8; ++i) p[8 * c + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
         }
       }
-      // The accumulator is in registers: let the next tile's MMAs start.
+      // The accumulators are in registers: let the next tile's MMAs start.
       tc_fence_before();
       mbar_arrive(tempty);
       acc_phase ^= 1u;
-      const int band0 = rt * BM + q * 32;  // first local row of this warp's band
+      const int band0 = rt * BM2 + h * BM + q * 32;  // first local row of this warp's band
       if (band0 + 32 <= ocnt) {
-        // Whole band valid: 32 x 32 pieces through shared memory (64-byte swizzle: 16-byte
-        // chunk c of row r at chunk c ^ ((r >> 1) & 3)), written by TMA.
+        // Whole band valid: 32 x 16 pieces through shared memory (32-byte swizzle: 16-byte
+        // chunk i of row r at chunk i ^ ((r >> 2) & 1)), written by TMA.
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (32 * c < ncols) {
+        for (int c = 0; c < BN / 16; ++c) {
+          if (16 * c < ncols) {
             uint8_t* buf = stg + (c & 1) * STG_BYTES;
             if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf is done
             __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4)) =
-                  make_uint4(p[16 * c + 4 * i], p[16 * c + 4 * i + 1], p[16 * c + 4 * i + 2],
-                             p[16 * c + 4 * i + 3]);
+            for (int i = 0; i < 2; ++i)
+              *reinterpret_cast<uint4*>(buf + lane * 32 + ((i ^ ((lane >> 2) & 1)) << 4)) =
+                  make_uint4(p[8 * c + 4 * i], p[8 * c + 4 * i + 1], p[8 * c + 4 * i + 2],
+                             p[8 * c + 4 * i + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tm_out, buf, c0 + 32 * c, obase + band0);
+              tma_store_2d(&tm_out, buf, c0 + 16 * c, obase + band0);
               bulk_commit_group();
             }
           }
@@ -452,12 +500,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else if (valid) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * a.ldo + c0);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (32 * c < ncols) {
+        for (int c = 0; c < BN / 16; ++c) {
+          if (16 * c < ncols) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[4 * c + i] = make_uint4(p[16 * c + 4 * i], p[16 * c + 4 * i + 1],
-                                          p[16 * c + 4 * i + 2], p[16 * c + 4 * i + 3]);
+            for (int i = 0; i < 2; ++i)
+              dst[2 * c + i] = make_uint4(p[8 * c + 4 * i], p[8 * c + 4 * i + 1],
+                                          p[8 * c + 4 * i + 2], p[8 * c + 4 * i + 3]);
           }
         }
       }
@@ -528,9 +576,9 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.out_rows)};
     const uint64_t strides[1] = {static_cast<uint64_t>(g.ldo) * 2};
-    const uint32_t box[2] = {32, 32};
+    const uint32_t box[2] = {16, 32};
     if (!encode_tmap(&tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.out, dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_64B))
+                     CU_TENSOR_MAP_SWIZZLE_32B))
       return MOE_ERR_CUDA;
   }
   constexpr size_t smem = smem_bytes();
@@ -543,6 +591,7 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
                                   static_cast<int>(smem)));
     configured_device = dev;
   }
+  // at most one tile per 128-row block and column tile (a group's last tile may be half)
   const long long tiles = static_cast<long long>(g.P / BM) * ((g.N + BN - 1) / BN);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   if (grid <= 0) return MOE_OK;
