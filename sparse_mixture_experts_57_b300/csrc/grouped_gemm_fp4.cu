@@ -11,9 +11,10 @@
 //
 // One CTA per SM, 448 threads, tiles of 256 activation rows (two 128-row halves) by 192
 // output columns:
-//   warp 0 lane 0  TMA producer: per stage 256 K-elements (128 bytes) of the two 128-row
-//                  activation halves and of 192 weight rows (128-byte swizzle), plus the
-//                  matching scale atoms (untiled bulk copies).
+//   warp 0 lane 0  TMA producer: per stage four tensor copies, 256 K-elements (128 bytes)
+//                  of the tile's 256 activation rows and of its 192 weight rows (128-byte
+//                  swizzle), and the matching scale atoms of both activation halves and of
+//                  both weight row blocks the tile touches (two 2 KB rows each).
 //   warps 10..13   scale writers, one per TMEM lane quadrant: read the stage's scale atoms
 //                  from shared memory and write them into a two-slot ring of TMEM scale
 //                  columns (tcgen05.st), in the layout the block-scaled MMA reads (see below).
@@ -77,6 +78,8 @@ static_assert(SF_COL0 + 64 <= ACC_STRIDE && ACC_STRIDE + SF_COL0 + 64 <= TMEM_CO
               "TMEM budget");
 static_assert(BN % 64 == 0 && BN <= 256, "weight tiles start on 64-row boundaries");
 constexpr uint32_t IDESC = idesc_nvfp4_f32(BM, BN);
+// Bytes landing per stage: every box is copied whole (rows outside a tensor read as zeros).
+constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + SFA_STAGE + SFB_STAGE;
 
 struct KArgs {
   const int* poff;
@@ -95,8 +98,7 @@ struct KArgs {
 };
 
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(STAGES) * (A_BYTES + B_BYTES + SFA_STAGE + SFB_STAGE) +
-         size_t(NUM_EPI_WARPS) * 2 * STG_BYTES + (3 * STAGES + 2) * 8 + 16 + (MAXG + 1) * 4;
+  return 1024 + size_t(STAGES) * STAGE_TX + size_t(NUM_EPI_WARPS) * 2 * STG_BYTES + (3 * STAGES + 2) * 8 + 16 + (MAXG + 1) * 4;
 }
 
 __device__ __forceinline__ void record(int* status, int code) { atomicCAS(status, 0, code); }
@@ -108,6 +110,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_fp4_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+               const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfw,
                const __grid_constant__ CUtensorMap tm_out, const KArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -144,6 +147,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_sfa);
+    prefetch_tmap(&tm_sfw);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -199,7 +204,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const uint32_t tmem_base = *tmem_slot;
   const int n_ct = (a.N + BN - 1) / BN;
-  const int nbw = (a.N + 127) / 128;                               // weight scale row blocks
   const int total = s_pref[E] * n_ct;
   const int KS = a.K / KSTEP;                                      // MMA steps along K
   const int NST = (KS + STEPS_PER_STAGE - 1) / STEPS_PER_STAGE;    // pipeline stages along K
@@ -235,37 +239,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int e, rt, ct;
         decode(tile, e, rt, ct);
         const int row0 = __ldg(a.poff + e) + rt * BM2;
-        const bool two_a = second_half(e, rt);
         const int col0 = ct * BN;
-        const int wb0 = col0 / 128;         // first weight scale row block of the tile
-        const bool two_b = wb0 + 1 < nbw;   // the second one exists
-        const uint8_t* sfa = a.a_sf + (static_cast<long long>(row0 / BM) * KS) * ATOM;
-        const uint8_t* sfw = a.w_sf + ((static_cast<long long>(e) * nbw + wb0) * KS) * ATOM;
-        const long long next_block = static_cast<long long>(KS) * ATOM;
         for (int kb = 0; kb < NST; ++kb) {
-          const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t sf_bytes = nsteps * ATOM;
-          const uint32_t halves = two_a ? 2u : 1u, wblocks = two_b ? 2u : 1u;
-          mbar_arrive_expect_tx(&full[stage],
-                                halves * A_HALF + B_BYTES + (halves + wblocks) * sf_bytes);
+          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
           ++armed;
-          uint8_t* dA = sA + stage * A_BYTES;
-          tma_load_2d(dA, &tm_a, &full[stage], kb * BKB, row0, pol);
-          if (two_a) tma_load_2d(dA + A_HALF, &tm_a, &full[stage], kb * BKB, row0 + BM, pol);
+          // Rows past a group's segment (a half tile) are loaded and not used; rows past the
+          // end of a tensor read as zeros.
+          tma_load_2d(sA + stage * A_BYTES, &tm_a, &full[stage], kb * BKB, row0, pol);
           tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kb * BKB, col0, e, pol);
-          const long long so = static_cast<long long>(kb) * STEPS_PER_STAGE * ATOM;
-          bulk_load(sSFA + stage * SFA_STAGE, sfa + so, sf_bytes, &full[stage], pol);
-          if (two_a)
-            bulk_load(sSFA + stage * SFA_STAGE + SF_ONE, sfa + next_block + so, sf_bytes,
-                      &full[stage], pol);
-          bulk_load(sSFB + stage * SFB_STAGE, sfw + so, sf_bytes, &full[stage], pol);
-          if (two_b)
-            bulk_load(sSFB + stage * SFB_STAGE + SF_ONE, sfw + next_block + so, sf_bytes,
-                      &full[stage], pol);
+          // scale atoms: 8-byte elements, 256 per row block and stage
+          tma_load_2d(sSFA + stage * SFA_STAGE, &tm_sfa, &full[stage], kb * 256, row0 / BM, pol);
+          tma_load_3d(sSFB + stage * SFB_STAGE, &tm_sfw, &full[stage], kb * 256, col0 / 128, e,
+                      pol);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -336,8 +325,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Quadrant q of TMEM, lane r0 = this lane. The smem atoms hold row 32 r1 + r0 of step j
     // at byte j * 512 + r0 * 16 + r1 * 4 (four E4M3 scales, one per 16 K elements). The A
     // stage holds the first activation half's atoms, then the second's; the B stage the
-    // atoms of weight row blocks wb0 and wb0 + 1, of which the tile's 192 rows start at row
-    // 0 or 64 of the first.
+    // atoms of the weight row block holding the tile's first row and of the next block
+    // (zeros past the last), the tile's 192 rows starting at row 0 or 64 of the first.
     const int q = warp & 3;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int stage = 0;
@@ -347,10 +336,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       int e, rt, ct;
       decode(tile, e, rt, ct);
-      const bool two_a = second_half(e, rt);
-      const int col0 = ct * BN;
-      const bool two_b = col0 / 128 + 1 < nbw;
-      const bool mid = (col0 & 127) != 0;  // the tile starts at row 64 of its first block
+      const bool mid = ((ct * BN) & 127) != 0;  // the tile starts at row 64 of its first block
       for (int kb = 0; kb < NST; ++kb, ++it) {
         const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
         if (!mbar_wait(&full[stage], phase, abort_flag)) {
@@ -374,10 +360,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           wa1[j] = 0u;
           if (j < nsteps) {
             wa0[j] = *reinterpret_cast<const uint32_t*>(sa + j * ATOM + lane * 16 + q * 4);
-            if (two_a)
-              wa1[j] = *reinterpret_cast<const uint32_t*>(sa + SF_ONE + j * ATOM + lane * 16 + q * 4);
+            wa1[j] = *reinterpret_cast<const uint32_t*>(sa + SF_ONE + j * ATOM + lane * 16 + q * 4);
             v0 = *reinterpret_cast<const uint4*>(sb + j * ATOM + lane * 16);
-            if (two_b) v1 = *reinterpret_cast<const uint4*>(sb + SF_ONE + j * ATOM + lane * 16);
+            v1 = *reinterpret_cast<const uint4*>(sb + SF_ONE + j * ATOM + lane * 16);
           }
           // column c of MMA j: weight row 32 c + lane of the tile
           uint32_t* w = wb[j >> 1] + 8 * (j & 1);
@@ -533,7 +518,9 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   if (g.P <= 0) return MOE_OK;
   if (g.K % KSTEP || g.N % 32 || g.E < 1 || g.E > MAXG || g.P % BM || g.ldo % 8 ||
       g.a_ld < g.K / 2 || g.a_ld % 16 ||
-      (reinterpret_cast<uintptr_t>(g.out) & 15))
+      ((reinterpret_cast<uintptr_t>(g.out) | reinterpret_cast<uintptr_t>(g.a_codes) |
+        reinterpret_cast<uintptr_t>(g.w_codes) | reinterpret_cast<uintptr_t>(g.a_sf) |
+        reinterpret_cast<uintptr_t>(g.w_sf)) & 15))
     return MOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_BF16 && g.epi != EPI_SQRELU_BF16) return MOE_ERR_UNSUPPORTED;
   KArgs ka;
@@ -559,7 +546,7 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(g.K / 2), static_cast<uint64_t>(g.P)};
     const uint64_t strides[1] = {static_cast<uint64_t>(g.a_ld)};
-    const uint32_t box[2] = {BKB, BM};
+    const uint32_t box[2] = {BKB, BM2};
     if (!encode_tmap(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box))
       return MOE_ERR_CUDA;
   }
@@ -570,6 +557,29 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
                                  static_cast<uint64_t>(g.N) * (g.K / 2)};
     const uint32_t box[3] = {BKB, BN, 1};
     if (!encode_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_codes, dims, strides, box))
+      return MOE_ERR_CUDA;
+  }
+  // Scale atoms as rows of 8-byte elements: one row per 128-row block, K/64 atoms of 64
+  // elements along it.
+  const int KS = g.K / KSTEP;
+  CUtensorMap tm_sfa, tm_sfw;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(KS) * (ATOM / 8), static_cast<uint64_t>(g.P / BM)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(KS) * ATOM};
+    const uint32_t box[2] = {SF_ONE / 8, 2};
+    if (!encode_tmap(&tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, g.a_sf, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_CUDA;
+  }
+  {
+    const int nbw = (g.N + 127) / 128;
+    const uint64_t dims[3] = {static_cast<uint64_t>(KS) * (ATOM / 8), static_cast<uint64_t>(nbw),
+                              static_cast<uint64_t>(g.E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(KS) * ATOM,
+                                 static_cast<uint64_t>(nbw) * KS * ATOM};
+    const uint32_t box[3] = {SF_ONE / 8, 2, 1};
+    if (!encode_tmap(&tm_sfw, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, g.w_sf, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
       return MOE_ERR_CUDA;
   }
   CUtensorMap tm_out;
@@ -595,7 +605,8 @@ int launch_fp4_gemm(const Fp4Gemm& g, cudaStream_t s) {
   const long long tiles = static_cast<long long>(g.P / BM) * ((g.N + BN - 1) / BN);
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   if (grid <= 0) return MOE_OK;
-  return launch_pdl(k_fp4_gemm, dim3(grid), dim3(NUM_THREADS), smem, s, tm_a, tm_w, tm_out, ka);
+  return launch_pdl(k_fp4_gemm, dim3(grid), dim3(NUM_THREADS), smem, s, tm_a, tm_w, tm_sfa,
+                    tm_sfw, tm_out, ka);
 }
 
 }  // namespace moe
