@@ -432,27 +432,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       uint32_t p[BN / 2];  // this row's outputs, packed bf16 pairs
 #pragma unroll
-      for (int c = 0; c < BN / 16; ++c) {
-        if (16 * c < ncols) {
-          uint32_t r[16];
-          tmem_ld16(tb + 16 * c, r);
+      for (int c = 0; c < BN / 32; ++c) {
+        if (32 * c < ncols) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(tb + 32 * c, r0);
+          tmem_ld16(tb + 32 * c + 16, r1);
           tmem_ld_wait();
-          float v[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * scale;
-          if (a.epi == EPI_SQRELU_BF16) {
+          for (int hh = 0; hh < 2; ++hh) {
+            float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float t = fmaxf(v[i], 0.f);
-              v[i] = t * t;
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(hh ? r1[i] : r0[i]) * scale;
+            if (a.epi == EPI_SQRELU_BF16) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float t = fmaxf(v[i], 0.f);
+                v[i] = t * t;
+              }
+              if (valid) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) vmax = fmaxf(vmax, v[i]);
+              }
             }
-            if (valid) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) vmax = fmaxf(vmax, v[i]);
-            }
+            for (int i = 0; i < 8; ++i) p[16 * c + 8 * hh + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
           }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) p[8 * c + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
         }
       }
       // The accumulators are in registers: let the next tile's MMAs start.
