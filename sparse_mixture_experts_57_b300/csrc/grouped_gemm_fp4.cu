@@ -22,15 +22,19 @@
 //                  K=64) with block scales, one per activation half, both on the same weight
 //                  tile, into two fp32 accumulators of 192 TMEM columns.
 //   warps 2..9     epilogue, one warp per (accumulator, lane quadrant): tcgen05.ld of its
-//                  192 columns into registers (global scales, activation, packed to bf16),
-//                  then the accumulators are released to the next tile's MMAs before the
-//                  stores go out. A warp's 32-row band goes out as 32x16 pieces staged in
-//                  swizzled shared memory and written by TMA stores; only the partial last
-//                  band of an expert is stored row by row.
+//                  192 columns into registers, 32 columns per tcgen05.wait::ld (global
+//                  scales, activation, packed to bf16), then the accumulators are released
+//                  to the next tile's MMAs before the stores go out. A warp's 32-row band
+//                  goes out as 32x16 pieces staged in swizzled shared memory and written by
+//                  TMA stores; only the partial last band of an expert is stored row by row.
+//                  The accumulators are single-buffered (two of 192 columns fill TMEM with
+//                  the scale ring), so the time this read takes lies between one tile's
+//                  MMAs and the next.
 //
 // Why two accumulators on one weight tile: with block-scaled FP4 MMAs the tensor cores
 // consume operand bytes 4x faster than with bf16, and every byte must first be written into
-// shared memory by the TMA, whose delivery into one SM (not the L2's output) is the limit.
+// shared memory by the TMA, whose delivery into one SM (not the L2's output) is the limit:
+// three 64 KB stages in flight against about two microseconds of L2 latency under load.
 // A tile of M x N outputs moves 32 (M + N) bytes per 64-element K step for M N / 16384
 // cycles of MMA work: 96 bytes per MMA cycle at 128 x 256, 75 at 256 x 192.
 //
