@@ -140,11 +140,14 @@ def _offsets(counts):
     # single column tile (N = 192) and a K tail of one MMA step in a partial stage (K = 320)
     ([300, 0, 1, 129, 1000, 600], 320, 192),
     ([90, 410, 5, 700, 300], 2688, 1856),      # Nano widths, many row tiles per group
-    # several row tiles per group, odd tile counts, a single-row and an empty group; N = 448
-    # gives a partial second weight block in the up-projection, N = 320 a last column tile
-    # with no second weight block in the down-projection
+    # several row tiles per group, odd 128-row block counts (a half-filled last 256-row
+    # tile), a single-row and an empty group. With 192-column tiles, N = 448 gives tiles
+    # of 192, 192 and 64 columns: the second starts half way into a 128-row weight scale
+    # block, the last has no second block (its scale box reads zeros past the tensor);
+    # N = 320 gives 192 and 128, the second block partly past N
     ([600, 520, 130, 900], 320, 448),
     ([1200, 1, 800, 900, 0], 256, 448),
+    ([385, 640, 1], 256, 576),                 # N = 576: three full 192-column tiles
     ([700, 900, 520, 1300], 2688, 1856),
 ])
 def test_grouped_ffn_nvfp4(moe, counts, H, F):
