@@ -14,10 +14,12 @@
 //   warp 0 lane 0  TMA producer: per stage four tensor copies, 256 K-elements (128 bytes)
 //                  of the tile's 256 activation rows and of its 192 weight rows (128-byte
 //                  swizzle), and the matching scale atoms of both activation halves and of
-//                  both weight row blocks the tile touches (two 2 KB rows each).
-//   warps 10..13   scale writers, one per TMEM lane quadrant: read the stage's scale atoms
-//                  from shared memory and write them into a two-slot ring of TMEM scale
-//                  columns (tcgen05.st), in the layout the block-scaled MMA reads (see below).
+//                  both weight row blocks the tile touches (two 2 KB rows each). The scale
+//                  copies go first and complete on their own barrier.
+//   warps 10..13   scale writers, one per TMEM lane quadrant: once a stage's scale atoms
+//                  have landed (its operand codes may still be arriving), read them from
+//                  shared memory and write them into a two-slot ring of TMEM scale columns
+//                  (tcgen05.st), in the layout the block-scaled MMA reads (see below).
 //   warp 1 lane 0  MMA issuer: per K step two tcgen05.mma kind::mxf4nvf4 (M=128, N=192,
 //                  K=64) with block scales, one per activation half, both on the same weight
 //                  tile, into two fp32 accumulators of 192 TMEM columns.
@@ -84,6 +86,7 @@ static_assert(BN % 64 == 0 && BN <= 256, "weight tiles start on 64-row boundarie
 constexpr uint32_t IDESC = idesc_nvfp4_f32(BM, BN);
 // Bytes landing per stage: every box is copied whole (rows outside a tensor read as zeros).
 constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + SFA_STAGE + SFB_STAGE;
+constexpr uint32_t SF_TX = SFA_STAGE + SFB_STAGE;  // the scale boxes, on their own barrier
 
 struct KArgs {
   const int* poff;
@@ -102,7 +105,7 @@ struct KArgs {
 };
 
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(STAGES) * STAGE_TX + size_t(NUM_EPI_WARPS) * 2 * STG_BYTES + (3 * STAGES + 2) * 8 + 16 + (MAXG + 1) * 4;
+  return 1024 + size_t(STAGES) * STAGE_TX + size_t(NUM_EPI_WARPS) * 2 * STG_BYTES + (4 * STAGES + 2) * 8 + 16 + (MAXG + 1) * 4;
 }
 
 __device__ __forceinline__ void record(int* status, int code) { atomicCAS(status, 0, code); }
@@ -129,7 +132,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* sfull = empty + STAGES;  // the stage's scales are in TMEM
   uint64_t* tfull = sfull + STAGES;  // the accumulators hold a finished tile
   uint64_t* tempty = tfull + 1;      // the epilogue has read the accumulators
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 1);
+  uint64_t* sffull = tempty + 1;     // the stage's scale atoms have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sffull + STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_pref = reinterpret_cast<int*>(tmem_slot + 4);  // row-tile prefix per group
 
@@ -142,6 +146,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
       mbar_init(&sfull[i], 4);
+      mbar_init(&sffull[i], 1);
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, 32 * (SFW_WARP0 - EPI_WARP0));
@@ -249,16 +254,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+          // The scale atoms first, on their own barrier: the scale writers can put them into
+          // TMEM while the operand codes are still arriving. 8-byte elements, 256 per row
+          // block and stage.
+          mbar_arrive_expect_tx(&sffull[stage], SF_TX);
+          tma_load_2d(sSFA + stage * SFA_STAGE, &tm_sfa, &sffull[stage], kb * 256, row0 / BM, pol);
+          tma_load_3d(sSFB + stage * SFB_STAGE, &tm_sfw, &sffull[stage], kb * 256, col0 / 128, e,
+                      pol);
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
           ++armed;
           // Rows past a group's segment (a half tile) are loaded and not used; rows past the
           // end of a tensor read as zeros.
           tma_load_2d(sA + stage * A_BYTES, &tm_a, &full[stage], kb * BKB, row0, pol);
           tma_load_3d(sB + stage * B_BYTES, &tm_w, &full[stage], kb * BKB, col0, e, pol);
-          // scale atoms: 8-byte elements, 256 per row block and stage
-          tma_load_2d(sSFA + stage * SFA_STAGE, &tm_sfa, &full[stage], kb * 256, row0 / BM, pol);
-          tma_load_3d(sSFB + stage * SFB_STAGE, &tm_sfw, &full[stage], kb * 256, col0 / 128, e,
-                      pol);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -270,6 +278,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         record(a.status, MOE_ERR_TIMEOUT);
       }
       if (!drain_stages(full, STAGES, stage, phase, armed)) record(a.status, MOE_ERR_TIMEOUT);
+      if (!drain_stages(sffull, STAGES, stage, phase, armed)) record(a.status, MOE_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -290,8 +299,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         for (int kb = 0; kb < NST; ++kb) {
           const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
-          // the scale writers arrive only after the stage's operands have landed
-          if (!mbar_wait(&sfull[stage], phase, abort_flag)) {
+          // the stage's scales are in TMEM and its operand codes have landed
+          if (!mbar_wait(&sfull[stage], phase, abort_flag) ||
+              !mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool mid = ((ct * BN) & 127) != 0;  // the tile starts at row 64 of its first block
       for (int kb = 0; kb < NST; ++kb, ++it) {
         const int nsteps = min(STEPS_PER_STAGE, KS - kb * STEPS_PER_STAGE);
-        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+        if (!mbar_wait(&sffull[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
